@@ -1,0 +1,330 @@
+"""Pins of the fp64 oracle against what the pages and the mathematics fix.
+
+Each ``check_*`` function takes the oracle module, so that ``test_pins_catch_mutations``
+can run the same checks against deliberately broken copies of the oracle (mistakes
+planted on the CPU only) and show that every planted mistake fails at least one pin.
+"""
+import itertools
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle.moe as moe_oracle
+import workloads
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _load(name):
+    with open(os.path.join(GOLDEN, name)) as fh:
+        return json.load(fh)
+
+
+def _expr(s):
+    """Closed-form values stored in fixtures: integers, decimals, fractions, log(q)."""
+    s = s.strip()
+    if s.startswith("log(") and s.endswith(")"):
+        return math.log(float(Fraction(s[4:-1])))
+    return float(Fraction(s))
+
+
+def _rand(shape, seed, scale=1.0):
+    return np.random.default_rng(seed).standard_normal(shape) * scale
+
+
+# ------------------------------------------------------------------------------------------
+# checks (module-parameterised)
+# ------------------------------------------------------------------------------------------
+def check_worked_example(o):
+    fx = _load("gate_worked_example.json")
+    l = np.array([[_expr(v) for v in fx["logits"]]])
+    G = o.masked_softmax(o.topk_mask(l, fx["k"]))
+    idx = o.topk_select(l, fx["k"])
+    assert idx.tolist() == [fx["expected_idx"]]
+    np.testing.assert_allclose(G[0], [_expr(v) for v in fx["expected_G"]], rtol=0, atol=1e-15)
+
+
+def check_gate_invariants(o):
+    for n, k, seed in [(8, 2, 0), (8, 1, 1), (8, 8, 2), (5, 3, 3), (32, 2, 4), (1, 1, 5)]:
+        x = _rand((64, 16), seed)
+        wg = _rand((16, n), seed + 100, 0.5)
+        idx, w, G, l = o.gate(x, wg, k)
+        assert G.shape == (64, n) and idx.shape == (64, k)
+        assert np.all(G >= 0)
+        assert np.all(np.count_nonzero(G, axis=1) == k)           # exactly K non-zeros
+        np.testing.assert_allclose(G.sum(axis=1), 1.0, rtol=0, atol=1e-14)
+        np.testing.assert_allclose(w.sum(axis=1), 1.0, rtol=0, atol=1e-14)
+        # the non-zero entries sit exactly at the selected experts
+        nz = [sorted(np.flatnonzero(r).tolist()) for r in G]
+        assert nz == [sorted(r) for r in idx.tolist()]
+        # slots are in descending logit order
+        kept = np.take_along_axis(l, idx, axis=1)
+        assert np.all(np.diff(kept, axis=1) <= 0)
+
+
+def _rank_count_topk(row, k):
+    """Brute force: expert i is selected iff fewer than k experts beat it, where j
+    beats i when l_j > l_i, or l_j == l_i and j < i.  Returned in beat-count order."""
+    n = len(row)
+    beaten_by = [sum(1 for j in range(n) if row[j] > row[i] or (row[j] == row[i] and j < i))
+                 for i in range(n)]
+    chosen = [i for i in range(n) if beaten_by[i] < k]
+    return sorted(chosen, key=lambda i: beaten_by[i])
+
+
+def check_topk_bruteforce(o):
+    vals = [0.0, 1.0, 2.0]
+    for n in (1, 2, 3, 4):
+        rows = np.array(list(itertools.product(vals, repeat=n)), dtype=np.float64)
+        for k in range(1, n + 1):
+            got = o.topk_select(rows, k)
+            want = np.array([_rank_count_topk(r, k) for r in rows])
+            assert np.array_equal(got, want), (n, k)
+    # random, continuous, n=8
+    rows = _rand((500, 8), 7)
+    for k in (1, 2, 3, 8):
+        assert np.array_equal(o.topk_select(rows, k), np.array([_rank_count_topk(r, k) for r in rows]))
+
+
+def check_softmax_order_equivalence(o):
+    l = _rand((200, 8), 11, 2.0)
+    for k in (1, 2, 4, 8):
+        G = o.masked_softmax(o.topk_mask(l, k))
+        # independent route: torch softmax over all n, zero outside the top-k, renormalise
+        p = torch.softmax(torch.from_numpy(l), dim=1)
+        top = torch.topk(p, k, dim=1).indices
+        keep = torch.zeros_like(p).scatter(1, top, 1.0)
+        ref = (p * keep) / (p * keep).sum(dim=1, keepdim=True)
+        np.testing.assert_allclose(G, ref.numpy(), rtol=1e-13, atol=1e-15)
+        np.testing.assert_allclose(o.gate_softmax_then_topk(l, k), ref.numpy(), rtol=1e-13, atol=1e-15)
+
+
+def _torch_swiglu(x, w1e, w3e, w2e):
+    x, w1e, w3e, w2e = (torch.from_numpy(np.asarray(a, dtype=np.float64)) for a in (x, w1e, w3e, w2e))
+    return F.linear(F.silu(F.linear(x, w1e)) * F.linear(x, w3e), w2e).numpy()
+
+
+def check_single_expert_is_plain_ffn(o):
+    T, d, f = 12, 24, 40
+    x = _rand((T, d), 21)
+    wg = _rand((d, 1), 22)
+    w1 = _rand((1, f, d), 23, d ** -0.5)
+    w3 = _rand((1, f, d), 24, d ** -0.5)
+    w2 = _rand((1, d, f), 25, f ** -0.5)
+    y = o.moe_layer(x, wg, w1, w3, w2, 1)
+    np.testing.assert_allclose(y, _torch_swiglu(x, w1[0], w3[0], w2[0]), rtol=1e-12, atol=1e-13)
+
+
+def check_k_equals_n_is_dense_softmax_mixture(o):
+    T, d, f, n = 10, 16, 20, 4
+    x = _rand((T, d), 31)
+    wg = _rand((d, n), 32, 0.3)
+    w1 = _rand((n, f, d), 33, d ** -0.5)
+    w3 = _rand((n, f, d), 34, d ** -0.5)
+    w2 = _rand((n, d, f), 35, f ** -0.5)
+    y = o.moe_layer(x, wg, w1, w3, w2, n)
+    p = torch.softmax(torch.from_numpy(x) @ torch.from_numpy(wg), dim=1).numpy()
+    ref = sum(p[:, i:i + 1] * _torch_swiglu(x, w1[i], w3[i], w2[i]) for i in range(n))
+    np.testing.assert_allclose(y, ref, rtol=1e-12, atol=1e-13)
+
+
+def check_sparse_equals_dense(o):
+    w = workloads.workload(1)
+    inp = workloads.make_inputs(w)
+    args = [workloads.as_f32(inp[t], w) for t in ("x", "wg", "w1", "w3", "w2")]
+    y = o.moe_layer(*args, w.k)
+    yd = o.moe_layer_dense(*args, w.k)
+    np.testing.assert_allclose(y, yd, rtol=1e-12, atol=1e-12)
+    # the dense sum with torch ops over all experts and the page's G
+    _, _, G, _ = o.gate(args[0], args[1], w.k)
+    ref = sum(G[:, i:i + 1] * _torch_swiglu(args[0], args[2][i], args[3][i], args[4][i]) for i in range(w.n))
+    np.testing.assert_allclose(y, ref, rtol=1e-11, atol=1e-12)
+
+
+def check_grouping(o):
+    rng = np.random.default_rng(41)
+    cases = [
+        (rng.integers(0, 8, size=(64, 2)), 8),
+        (np.zeros((33, 2), dtype=np.int64), 8),                        # every token to expert 0
+        (np.array([[7, 3]] * 5), 8),                                   # empty experts around
+        (rng.integers(0, 3, size=(17, 3)), 5),                         # ragged, experts 3,4 empty
+        (np.zeros((0, 2), dtype=np.int64), 4),                         # no tokens
+        (rng.integers(0, 32, size=(1000, 2)), 32),
+    ]
+    for idx, n in cases:
+        off, perm, inv = o.group_by_expert(idx, n)
+        flat = idx.reshape(-1).tolist()
+        A = len(flat)
+        # brute force by counting
+        counts = [flat.count(e) for e in range(n)]
+        assert off.tolist() == [sum(counts[:e]) for e in range(n + 1)]
+        want = [a for e in range(n) for a in range(A) if flat[a] == e]
+        assert perm.tolist() == want
+        assert sorted(perm.tolist()) == list(range(A))                  # bijection
+        assert all(inv[perm[p]] == p for p in range(A))
+        # permute rows then unpermute is the identity
+        X = rng.standard_normal((A, 3))
+        assert np.array_equal(X[perm][inv], X)
+
+
+def check_silu(o):
+    z = np.concatenate([np.linspace(-40, 40, 2001), [0.0, -1e-300, 1e-300, -745.0, 710.0]])
+    np.testing.assert_allclose(o.silu(z), F.silu(torch.from_numpy(z)).numpy(), rtol=1e-14, atol=1e-300)
+    # odd-part identity: silu(z) - silu(-z) = z
+    np.testing.assert_allclose(o.silu(z) - o.silu(-z), z, rtol=1e-13, atol=1e-13)
+    # sigmoid(ln 3) = 3/4
+    assert abs(o.silu(np.array([math.log(3)]))[0] - 0.75 * math.log(3)) < 1e-15
+
+
+def check_bias_enters_before_topk(o):
+    # logits 0.2 > 0.1 > 0 without bias; a bias of +1 on expert 2 moves it to the top
+    x = np.array([[1.0]])
+    wg = np.array([[0.2, 0.1, 0.0]])
+    b = np.array([0.0, 0.0, 1.0])
+    idx, w, G, l = o.gate(x, wg, 2, b)
+    assert idx.tolist() == [[2, 0]]
+    e = math.exp(1.0 - 0.2)
+    np.testing.assert_allclose(w[0], [e / (1 + e), 1 / (1 + e)], rtol=1e-14)
+    assert o.gate(x, wg, 2)[0].tolist() == [[0, 1]]
+
+
+def check_rmsnorm(o):
+    h = _rand((9, 64), 51, 3.0)
+    ref = F.rms_norm(torch.from_numpy(h), (64,), eps=1e-5).numpy()
+    np.testing.assert_allclose(o.rmsnorm(h, 1e-5), ref, rtol=1e-13, atol=1e-14)
+    # stacked layer = h + MoE(RMSNorm(h)) with a single always-on expert
+    x = _rand((5, 8), 52)
+    wg = np.ones((8, 1))
+    w1, w3, w2 = _rand((1, 6, 8), 53), _rand((1, 6, 8), 54), _rand((1, 8, 6), 55)
+    xn = F.rms_norm(torch.from_numpy(x), (8,), eps=1e-5).numpy()
+    np.testing.assert_allclose(o.stacked_layer(x, wg, w1, w3, w2, 1), x + _torch_swiglu(xn, w1[0], w3[0], w2[0]),
+                               rtol=1e-12, atol=1e-13)
+
+
+def check_param_counts(o):
+    fx = _load("param_counts.json")
+    c = o.param_counts(fx["d"], fx["f"], fx["n"], fx["k"], fx["layers"], fx["heads"], fx["kv_heads"])
+    # 32 * 8 * 3 * 4096 * 14336 and 32 * 2 * 3 * 4096 * 14336
+    assert c["expert"] == 45_097_156_608 and c["active_expert"] == 11_274_289_152
+    rest_total = fx["total_params_printed"] - (c["expert"] + c["attention"])
+    rest_active = fx["active_params_printed"] - (c["active_expert"] + c["attention"])
+    # what is left (embeddings, norms, router) is small, positive and the same in both counts
+    assert 0 < rest_total < 0.6e9 and 0 < rest_active < 0.6e9
+    assert abs(rest_total - rest_active) <= 2 * fx["printed_rounding"]
+
+
+def check_locality_metric(o):
+    assert o.consecutive_same_expert_rate(np.array([[0, 1], [0, 2], [1, 0], [1, 3], [1, 0]])) == 0.75
+    rng = np.random.default_rng(61)
+    r = o.consecutive_same_expert_rate(rng.integers(0, 8, size=(200_000, 2)))
+    assert abs(r - 1 / 8) < 0.005          # the random-assignment rate of 12.5% for n = 8
+
+
+CHECKS = [check_worked_example, check_gate_invariants, check_topk_bruteforce,
+          check_softmax_order_equivalence, check_single_expert_is_plain_ffn,
+          check_k_equals_n_is_dense_softmax_mixture, check_sparse_equals_dense, check_grouping,
+          check_silu, check_bias_enters_before_topk, check_rmsnorm, check_param_counts,
+          check_locality_metric]
+
+
+@pytest.mark.parametrize("check", CHECKS, ids=lambda c: c.__name__[6:])
+def test_oracle_pin(check):
+    check(moe_oracle)
+
+
+# ------------------------------------------------------------------------------------------
+# planted mistakes (CPU only): each must be caught by at least one pin
+# ------------------------------------------------------------------------------------------
+_ORIG_SWIGLU = moe_oracle.expert_swiglu
+_ORIG_GROUP = moe_oracle.group_by_expert
+
+
+def _mut_sigmoid_for_silu(z):
+    z = np.asarray(z, dtype=np.float64)
+    return 1.0 / (1.0 + np.exp(-z))
+
+
+def _mut_swap_w1_w3(xs, w1_e, w3_e, w2_e):
+    return _ORIG_SWIGLU(xs, w3_e, w1_e, w2_e)
+
+
+def _mut_drop_w3(xs, w1_e, w3_e, w2_e):
+    xs = np.asarray(xs, dtype=np.float64)
+    return moe_oracle.silu(xs @ np.asarray(w1_e).T) @ np.asarray(w2_e).T
+
+
+def _mut_transpose_w2(xs, w1_e, w3_e, w2_e):
+    xs = np.asarray(xs, dtype=np.float64)
+    h = moe_oracle.silu(xs @ np.asarray(w1_e).T) * (xs @ np.asarray(w3_e).T)
+    w2 = np.asarray(w2_e)
+    return h @ w2.reshape(w2.shape[1], w2.shape[0])  # a plausible layout mix-up
+
+
+def _mut_no_topk(logits, k):
+    return np.asarray(logits, dtype=np.float64)
+
+
+def _mut_ties_to_higher(logits, k):
+    l = np.asarray(logits, dtype=np.float64)
+    n = l.shape[1]
+    order = np.argsort(-l[:, ::-1], axis=1, kind="stable")
+    return (n - 1 - order)[:, :k].astype(np.int64)
+
+
+def _mut_unstable_group(idx, n):
+    off, perm, inv = _ORIG_GROUP(idx, n)
+    for e in range(n):
+        perm[off[e]:off[e + 1]] = perm[off[e]:off[e + 1]][::-1].copy()
+    inv = np.empty_like(perm)
+    inv[perm] = np.arange(perm.size)
+    return off, perm, inv
+
+
+def _mut_bias_after_topk(x, wg, bias=None):
+    return np.asarray(x, dtype=np.float64) @ np.asarray(wg, dtype=np.float64)
+
+
+def _mut_softmax_sign(z):
+    z = np.asarray(z, dtype=np.float64)
+    m = np.max(z, axis=-1, keepdims=True)
+    e = np.exp(-(z - m))
+    e[np.isinf(z)] = 0.0
+    return e / np.sum(e, axis=-1, keepdims=True)
+
+
+def _mut_rms_no_sqrt(h, eps=1e-5):
+    h = np.asarray(h, dtype=np.float64)
+    return h / (np.mean(h * h, axis=-1, keepdims=True) + eps)
+
+
+MUTATIONS = {
+    "silu->sigmoid": ("silu", _mut_sigmoid_for_silu),
+    "swap w1/w3": ("expert_swiglu", _mut_swap_w1_w3),
+    "drop w3 branch": ("expert_swiglu", _mut_drop_w3),
+    "w2 layout mix-up": ("expert_swiglu", _mut_transpose_w2),
+    "no TopK mask": ("topk_mask", _mut_no_topk),
+    "ties to higher index": ("topk_select", _mut_ties_to_higher),
+    "unstable grouping": ("group_by_expert", _mut_unstable_group),
+    "bias ignored": ("router_logits", _mut_bias_after_topk),
+    "softmax sign flip": ("masked_softmax", _mut_softmax_sign),
+    "rmsnorm without sqrt": ("rmsnorm", _mut_rms_no_sqrt),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_pins_catch_mutations(name, monkeypatch):
+    attr, fn = MUTATIONS[name]
+    monkeypatch.setattr(moe_oracle, attr, fn)
+    failed = []
+    for check in CHECKS:
+        try:
+            check(moe_oracle)
+        except (AssertionError, ValueError, IndexError):
+            failed.append(check.__name__)
+    assert failed, f"planted mistake '{name}' passed every pin"

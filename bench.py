@@ -1,0 +1,485 @@
+#!/usr/bin/env python3
+"""Throughput of the sparse MoE feed-forward layer on B300, one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload I] [--impl ours|reference]
+
+A step is one pass of the whole layer (router/top-2/softmax -> grouping -> expert
+up-projection with SwiGLU -> down-projection -> gate-weighted combine; for the stacked
+workload, RMSNorm + layer + residual for each of its 4 layers) over one batch of seeded
+synthetic input, through the C ABI of libmoe.so.  Inputs are resident in HBM when the
+timed region starts; the expert weights (2.82 GB per layer) are larger than the 126 MB
+L2, so no flush is needed between steps.  `value` is tokens/s of the whole job (all ranks).
+
+Default workload: the Mixtral-shaped decode batch (T=32 tokens, d=4096, f=14336, 8
+experts, top-2).  `--impl reference` times the fp64 CPU oracle instead (the slow
+reference arm), on a bounded sample of the same workload.
+Under torchrun each rank runs an independent replica on its own GPU (the layer needs no
+exchange between ranks), timed with a barrier on both sides and the maximum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "MoE-layer tokens/s and TFLOP/s (or HBM GB/s) on 1 B300 vs roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--workload", type=int, default=2, choices=sorted(workloads.WORKLOADS))
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--seed", type=int, default=0)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args()
+
+
+# ----------------------------------------------------------------------------------------------
+# distributed plumbing (one process per GPU)
+# ----------------------------------------------------------------------------------------------
+class Dist:
+    def __init__(self):
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+
+    def init(self, backend):
+        if self.world > 1:
+            import torch.distributed as td
+            td.init_process_group(backend=backend)
+            self.pg = td
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, v: float) -> float:
+        if not self.pg:
+            return v
+        import torch
+        t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------------------------
+# clocks during the timed region (NVML reads only)
+# ----------------------------------------------------------------------------------------------
+REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+           0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+           0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting"}
+
+
+class ClockSampler:
+    def __init__(self, torch_dev):
+        self.samples = []
+        self.ok = False
+        self._stop = threading.Event()
+        self._thr = None
+        try:
+            import pynvml
+            import torch
+            pynvml.nvmlInit()
+            uuid = str(torch.cuda.get_device_properties(torch_dev).uuid)
+            if not uuid.startswith("GPU-"):
+                uuid = "GPU-" + uuid
+            self.h = pynvml.nvmlDeviceGetHandleByUUID(uuid)
+            self.nv = pynvml
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+            self.ok = True
+        except Exception as exc:  # no NVML: clocks are reported as unknown
+            self.err = repr(exc)
+
+    def _reasons(self):
+        nv = self.nv
+        fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(nv, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        return int(fn(self.h))
+
+    def _run(self):
+        while not self._stop.is_set():
+            try:
+                mhz = self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM)
+                self.samples.append((mhz, self._reasons()))
+            except Exception:
+                pass
+            time.sleep(0.002)
+
+    def start(self):
+        if self.ok:
+            self._thr = threading.Thread(target=self._run, daemon=True)
+            self._thr.start()
+
+    def stop(self):
+        if self._thr:
+            self._stop.set()
+            self._thr.join()
+
+    def summary(self):
+        if not self.ok or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": getattr(self, "max_mhz", None), "reasons": [],
+                    "samples": 0, "note": getattr(self, "err", "no samples")}
+        mhz = [s[0] for s in self.samples]
+        bits = 0
+        for _, r in self.samples:
+            bits |= r
+        names = [n for b, n in REASONS.items() if bits & b and n != "gpu_idle"]
+        return {"sm_mhz": float(statistics.median(mhz)), "sm_max_mhz": float(self.max_mhz),
+                "reasons": names, "samples": len(self.samples)}
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            p = json.load(fh)
+        return p, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the current
+    source of the kernel (profiles/<kernel>__<workload>.md holds 'traffic_bytes_per_launch:'
+    and 'source_sha256:' lines); None otherwise."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}__{workload}.md")
+    src = os.path.join(ROOT, "sparse_mixture_experts_56_b300", "csrc", "grouped_tc.cu")
+    try:
+        text = open(path).read()
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    except OSError:
+        return None
+    fields = {}
+    for line in text.splitlines():
+        if ":" in line:
+            k, v = line.split(":", 1)
+            fields[k.strip().lstrip("-* ").strip("`")] = v.strip().strip("`")
+    if fields.get("source_sha256") != sha:
+        return None
+    try:
+        return float(fields["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ----------------------------------------------------------------------------------------------
+# inputs
+# ----------------------------------------------------------------------------------------------
+def host_inputs(w, seed):
+    """Per layer: dict of stored tensors (bf16 bit patterns or fp32) + the activations."""
+    layers = [workloads.make_inputs(w, seed=seed, layer=l, tensors=("wg", "w1", "w3", "w2"))
+              for l in range(w.layers)]
+    x = workloads.make_inputs(w, seed=seed, tensors=("x",))["x"]
+    bias = workloads.logit_bias_vector(w.n) if w.skew_bias else None
+    return x, layers, bias
+
+
+def to_dev(a, w, dev):
+    import torch
+    if w.dtype == "bf16":
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(dev)
+
+
+# ----------------------------------------------------------------------------------------------
+# the oracle arm (CPU)
+# ----------------------------------------------------------------------------------------------
+def oracle_prepare(w, x, layers, bias):
+    """Expands the stored inputs to float64 once (input preparation, outside any timing)."""
+    xf = workloads.as_f32(x, w).astype(np.float64)
+    lf = []
+    for L in layers:
+        lf.append({k: workloads.as_f32(L[k], w).astype(np.float64) for k in ("wg", "w1", "w3", "w2")})
+    return xf, lf, bias
+
+
+def oracle_step(w, xf, lf, bias, tokens):
+    import oracle
+    if w.layers == 1:
+        return oracle.moe_layer(xf, lf[0]["wg"], lf[0]["w1"], lf[0]["w3"], lf[0]["w2"], w.k, bias,
+                                tokens=tokens)
+    h = xf[tokens]
+    for L in lf:
+        h = oracle.stacked_layer(h, L["wg"], L["w1"], L["w3"], L["w2"], w.k, w.rms_eps)
+    return h
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_sample_tokens(w, budget_tokens: int, rng):
+    return np.sort(rng.choice(w.T, size=min(w.T, budget_tokens), replace=False))
+
+
+def run_cpu_baseline(w, xf, lf, bias, target_s=10.0):
+    """Times the oracle on a bounded sample of the workload's tokens."""
+    rng = np.random.default_rng(1234)
+    n_tok = {1: 64, 2: 32, 3: 256, 4: 256, 5: 64}.get(w.wid, 64)
+    tokens = oracle_sample_tokens(w, n_tok, rng)
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        oracle_step(w, xf, lf, bias, tokens)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= target_s or (w.wid != 1 and reps >= 1 and el * (reps + 1) / reps > 30):
+            break
+    return {"value": reps * len(tokens) / el, "unit": "tokens/s", "cores": cpu_cores(),
+            "kind": "oracle",
+            "sample": f"{len(tokens)} of the {w.T} tokens x {reps} repetition(s), fp64 NumPy "
+                      f"({el:.1f} s); inputs expanded to float64 before timing"}
+
+
+def reference_arm(args, w, dist):
+    if dist.rank != 0:
+        return
+    x, layers, bias = host_inputs(w, args.seed)
+    xf, lf, _ = oracle_prepare(w, x, layers, bias)
+    del layers
+    rng = np.random.default_rng(4321)
+    per_step = w.T if w.wid == 1 else 1
+    for _ in range(args.warmup):
+        oracle_step(w, xf, lf, bias, oracle_sample_tokens(w, per_step, rng))
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(w, xf, lf, bias, oracle_sample_tokens(w, per_step, rng))
+    el = time.perf_counter() - t0
+    value = per_step * args.steps / el
+    cores = cpu_cores()
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": w.name, "T": w.T, "d_model": w.d, "d_ff": w.f, "n_experts": w.n,
+                       "top_k": w.k, "layers": w.layers, "tokens_per_step": per_step},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": f"{per_step} token(s) of the {w.T}-token batch per step"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------------------------
+# our arm
+# ----------------------------------------------------------------------------------------------
+def ours_arm(args, w, dist):
+    import torch
+    import sparse_mixture_experts_56_b300 as moe
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device")
+    dev = torch.device("cuda", dist.local)
+    torch.cuda.set_device(dev)
+    moe._native.lib()
+
+    x_h, layers_h, bias_h = host_inputs(w, args.seed)
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    esz = 2 if w.dtype == "bf16" else 4
+    x = to_dev(x_h, w, dev)
+    layers = [{k: to_dev(L[k], w, dev) for k in ("wg", "w1", "w3", "w2")} for L in layers_h]
+    bias = torch.from_numpy(bias_h).to(dev) if bias_h is not None else None
+    T, d, f, n, k = w.T, w.d, w.f, w.n, w.k
+    A = T * k
+    ws = moe.workspace(T, d, f, n, k, tdt, dev)
+    idx = torch.empty((T, k), dtype=torch.int32, device=dev)
+    gw = torch.empty((T, k), dtype=torch.float32, device=dev)
+    off = torch.empty(n + 1, dtype=torch.int32, device=dev)
+    perm = torch.empty(A, dtype=torch.int32, device=dev)
+    inv = torch.empty(A, dtype=torch.int32, device=dev)
+    hbuf = torch.empty((A, f), dtype=tdt, device=dev)
+    yp = torch.empty((A, d), dtype=tdt, device=dev)
+    hs = [x.clone() for _ in range(2)]
+    xn = torch.empty_like(x)
+    stream = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+
+    def layer(inp, L, out, residual, marks=None):
+        moe.moe_router_topk(inp, L["wg"], k, bias, topk_idx=idx, topk_w=gw)
+        moe.moe_permute(idx, n, ws, expert_offsets=off, perm=perm, inv_perm=inv)
+        if marks:
+            marks[0].record(stream)
+        moe.moe_expert_up(inp, perm, off, L["w1"], L["w3"], k, ws, h=hbuf)
+        if marks:
+            marks[1].record(stream)
+        moe.moe_expert_down(hbuf, off, L["w2"], k, ws, y_perm=yp)
+        if marks:
+            marks[2].record(stream)
+        moe.moe_combine(yp, inv, gw, residual, y=out)
+
+    def step(marks=None):
+        if w.layers == 1:
+            layer(x, layers[0], hs[0], None, marks)
+            return
+        h_in = x
+        for li, L in enumerate(layers):
+            moe.moe_rmsnorm(h_in, w.rms_eps, x=xn)
+            out = hs[li % 2]
+            layer(xn, L, out, h_in, marks if li == 0 else None)
+            h_in = out
+
+    launches_per_layer = 1 + (1 if A <= 32768 else 3) + 1 + 1 + 1 + 1
+    launches_per_step = w.layers * (launches_per_layer + (1 if w.layers > 1 else 0))
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    st = moe.moe_check_device_error(ws)
+    if st != 0:
+        raise SystemExit(f"device status {st} after warm-up")
+
+    sampler = ClockSampler(dev)
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    start.record(stream)
+    for i in range(args.steps):
+        step(ev[i])
+    stop.record(stream)
+    torch.cuda.synchronize()
+    sampler.stop()
+    dist.barrier()
+    ms_total = start.elapsed_time(stop)
+    st = moe.moe_check_device_error(ws)
+    if st != 0:
+        raise SystemExit(f"device status {st} in the timed region")
+    ms_total = dist.max(ms_total)
+    up_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    down_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+
+    value = T * dist.world * args.steps / (ms_total / 1e3)
+    flops_step = workloads.active_flops(w) * w.layers
+    counts = np.diff(off.cpu().numpy())
+    touched = int((counts > 0).sum())
+
+    # roofline of the dominant kernel: the w1|w3 up-projection with SwiGLU (moe_expert_up:
+    # row gather + grouped tcgen05 GEMM), per launch
+    up_bytes = touched * 2 * f * d * esz + A * d * esz * 2 + A * f * esz   # weights + x read/gathered + h
+    up_flops = 2.0 * A * d * 2 * f
+    pk, pk_kind = peaks()
+    hbm_peak = float(pk.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    tc_peak = float(pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    ai = up_flops / up_bytes
+    ridge = tc_peak * 1e12 / (hbm_peak * 1e9)
+    if ai < ridge:
+        ach = up_bytes / (up_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": ach, "peak": hbm_peak, "unit": "GB/s", "frac": ach / hbm_peak}
+    else:
+        ach = up_flops / (up_ms / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": ach, "peak": tc_peak, "unit": "TFLOP/s", "frac": ach / tc_peak}
+    roof.update({"traffic": kernel_traffic("expert_up", w.name), "kernel": "moe_expert_up (gather + w1|w3 tcgen05 GEMM + SwiGLU)",
+                 "algorithmic": up_bytes if roof["bound"] == "hbm" else up_flops,
+                 "ms_per_launch": up_ms, "peak_source": f"{pk_kind} (MEASURED_PEAKS.json)" if pk_kind == "measured" else "fallback",
+                 "down_ms_per_launch": down_ms})
+
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": dist.world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": w.dtype, "data": "synthetic (seeded Gaussian, Mixtral-shaped)",
+            "config": {"workload": w.name, "T": T, "d_model": d, "d_ff": f, "n_experts": n, "top_k": k,
+                       "layers": w.layers, "skewed_bias": w.skew_bias, "global_batch": T * dist.world,
+                       "parallelism": f"replicas x{dist.world}",
+                       "l2": "no flush: per-step inputs (expert weights, %.2f GB/layer) exceed the 126 MB L2"
+                             % (3 * n * d * f * esz / 1e9)},
+            "tflops": flops_step * dist.world * args.steps / (ms_total / 1e3) / 1e12,
+            "roofline": roof, "gpu_launches": launches_per_step * args.steps,
+            "clocks": sampler.summary(), "expert_counts": counts.tolist()}
+
+    if not args.no_e2e:
+        # end to end through the public call with host buffers: pinned H2D of x, the layer,
+        # D2H of y, every step
+        x_pin = torch.from_numpy(np.ascontiguousarray(x_h).view(np.int16) if w.dtype == "bf16" else x_h)
+        x_pin = (x_pin.view(torch.bfloat16) if w.dtype == "bf16" else x_pin).pin_memory()
+        y_pin = torch.empty_like(x_pin).pin_memory()
+        x_dev = torch.empty_like(x)
+        y_dev = torch.empty_like(x)
+        ws_full = ws
+        xn2 = torch.empty_like(x)
+        hbuf2 = [torch.empty_like(x) for _ in range(2)]
+
+        def e2e_step():
+            x_dev.copy_(x_pin, non_blocking=True)
+            if w.layers == 1:
+                moe.moe_layer_forward(x_dev, layers[0]["wg"], layers[0]["w1"], layers[0]["w3"],
+                                      layers[0]["w2"], k, ws_full, logit_bias=bias, y=y_dev)
+                y_pin.copy_(y_dev, non_blocking=True)
+            else:
+                h_in = x_dev
+                for li, L in enumerate(layers):
+                    moe.moe_rmsnorm(h_in, w.rms_eps, x=xn2)
+                    out = hbuf2[li % 2]
+                    moe.moe_layer_forward(xn2, L["wg"], L["w1"], L["w3"], L["w2"], k, ws_full,
+                                          residual=h_in, y=out)
+                    h_in = out
+                y_pin.copy_(h_in, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        dist.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        dist.barrier()
+        e_ms = dist.max(e0.elapsed_time(e1))
+        line["e2e"] = {"value": T * dist.world * args.steps / (e_ms / 1e3), "unit": "tokens/s",
+                       "h2d_bytes_per_step": T * d * esz, "d2h_bytes_per_step": T * d * esz,
+                       "ms_per_step": e_ms / args.steps, "api": "moe_layer_forward"}
+        if moe.moe_check_device_error(ws) != 0:
+            raise SystemExit("device status set in the end-to-end loop")
+
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+        del layers
+        xf, lf, _ = oracle_prepare(w, x_h, layers_h, bias_h)
+        del layers_h
+        line["cpu_baseline"] = run_cpu_baseline(w, xf, lf, bias_h)
+    if dist.rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    w = workloads.workload(args.workload)
+    dist = Dist()
+    if args.impl == "reference":
+        reference_arm(args, w, dist)   # rank 0 only; the other ranks exit without work
+        return
+    import torch
+    dist.init("nccl" if torch.cuda.is_available() else "gloo")
+    try:
+        ours_arm(args, w, dist)
+    finally:
+        dist.close()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,198 @@
+/*
+ * moe.h — C ABI of the sparse mixture-of-experts feed-forward layer (libmoe.so).
+ *
+ * The layer, as the Mixtral 8x7B pages define it ("Mixtral of Experts", xyznot.com
+ * summary, section "Método (con las ecuaciones clave)"; blog.csdn.net post
+ * "《Mixtral of Experts》Mixtral 8x7B：稀疏专家混合模型的突破性进展", section
+ * "MOE数学公式"):
+ *
+ *     l    = x · W_g                       router logits, W_g in R^{d x n}
+ *     G(x) = Softmax(TopK(l))              TopK keeps the K largest logits, the rest -> -inf
+ *     y    = sum_i G(x)_i · E_i(x)         E_i(x) = w2_i · (SiLU(w1_i · x) ⊙ (w3_i · x))
+ *
+ * Only the K experts with a non-zero gate are evaluated, on the group of tokens routed
+ * to them, and their outputs return to the original token positions ("Mixtral 8x7B:
+ * 疎な専門家混合言語モデル", ja.news.hada.io, sections "MoEレイヤーの計算方式" and
+ * "実装と推論効率").
+ *
+ * Conventions for every call
+ *   - All tensor pointers are DEVICE pointers (cudaMalloc / torch CUDA memory) unless
+ *     stated otherwise; the caller owns every buffer, including the workspace.  The
+ *     library allocates nothing and frees nothing.
+ *   - Calls are asynchronous and ordered on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream).  No call synchronises except moe_check_device_error().
+ *   - Arguments are validated on the host before anything is launched.  On a non-OK
+ *     status no kernel was launched and no output was written, except MOE_ERR_CUDA
+ *     (a launch failed part-way; outputs are undefined).
+ *   - Layouts are dense row-major with no padding:
+ *       x, residual, y   [T, d]        activations
+ *       w_gate           [d, n]        router weight (logits = x · w_gate)
+ *       w1, w3           [n, f, d]     expert gate / up projections, out x in
+ *       w2               [n, d, f]     expert down projection, out x in
+ *       topk_idx         [T, k] int32  chosen experts, descending logit, ties -> lower index
+ *       topk_w           [T, k] fp32   their gate values (sum to 1 per token)
+ *       expert_offsets   [n + 1] int32 exclusive prefix sum of per-expert counts
+ *       perm             [T*k] int32   perm[p] = assignment a = t*k + slot at position p,
+ *                                      positions ordered by (expert, a)
+ *       inv_perm         [T*k] int32   inv_perm[a] = position of assignment a
+ *       y_perm           [T*k, d]      expert outputs E_e(x_t), one row per position p
+ *   - dtype MOE_F32: x, w_gate, w1, w3, w2, residual, y_perm, y are float32.
+ *     dtype MOE_BF16: they are bfloat16; products accumulate in fp32; the intermediate
+ *     SiLU(a)⊙b and y_perm are rounded to bf16.  logit_bias, logits and topk_w are
+ *     always float32.
+ *   - Supported sizes: T >= 0, d >= 1, f >= 1, 1 <= k <= n <= 32, T*k < 2^31.  Tensor
+ *     pointers must be 16-byte aligned.  MOE_BF16 experts run on the tensor cores when
+ *     d % 64 == 0 and f % 64 == 0, otherwise on an fp32 CUDA-core kernel.
+ *   - Device status: kernels report a timed-out wait or a bad expert index by setting bits
+ *     of a status word in the first 256 bytes of the workspace.  The bits stay set until
+ *     moe_check_device_error() reads and clears them, so a new workspace must start with
+ *     those 256 bytes zeroed (cudaMemset once, or one moe_check_device_error call).
+ */
+#ifndef MOE_H_
+#define MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1, /* null pointer, bad size, misaligned pointer, bad dtype       */
+  MOE_ERR_UNSUPPORTED = 2, /* valid but outside what the kernels implement                  */
+  MOE_ERR_WORKSPACE = 3,   /* workspace null or smaller than moe_workspace_size()           */
+  MOE_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed                          */
+  MOE_ERR_TIMEOUT = 5,     /* a kernel wait ran past its limit; the kernel gave up cleanly  */
+  MOE_ERR_DEVICE_INDEX = 6 /* a kernel met an expert index outside [0, n)                   */
+} moe_status;
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
+
+/* Human-readable name of a status code.  Never NULL. */
+const char* moe_status_string(int status);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int moe_version(void);
+
+/*
+ * Bytes of device workspace needed by moe_layer_forward (and enough for
+ * moe_permute and moe_grouped_swiglu) for these sizes.  Returns 0 for invalid sizes.
+ * The workspace holds a status header, the router outputs, the permutation, the
+ * expert-ordered copy of x, the SwiGLU intermediate [T*k, f] and y_perm [T*k, d].  Apart
+ * from the status header (see above) it needs no initialisation.
+ */
+size_t moe_workspace_size(int T, int d, int f, int n, int k, int dtype);
+
+/*
+ * Router and gate: logits l = x · w_gate (+ logit_bias), TopK, softmax over the K
+ * kept logits ("Mixtral of Experts", Método, eq. G; blog.csdn.net MOE数学公式 §2.1-§2.3).
+ *   x          [T, d]   dtype
+ *   w_gate     [d, n]   dtype
+ *   logit_bias [n] fp32, nullable: added to the logits before TopK and softmax
+ *   topk_idx   [T, k] int32 out
+ *   topk_w     [T, k] fp32 out
+ *   logits     [T, n] fp32 out, nullable (biased logits, fp32 accumulation)
+ * One warp per token; fp32 accumulation of the products.
+ */
+moe_status moe_router_topk(const void* x, const void* w_gate, const float* logit_bias, int T, int d,
+                           int n, int k, int dtype, int32_t* topk_idx, float* topk_w, float* logits,
+                           void* stream);
+
+/*
+ * Group the T*k assignments by expert: counts per expert, exclusive prefix sum into
+ * expert_offsets, and a stable rank that yields perm / inv_perm (see layouts above).
+ * Deterministic and bit-exact: within one expert, assignments keep ascending a = t*k+slot.
+ *   topk_idx       [T, k] int32 in (values must be in [0, n))
+ *   expert_offsets [n+1] int32 out; perm, inv_perm [T*k] int32 out
+ *   ws, ws_bytes   workspace of at least moe_workspace_size(T, 64, 64, n, k, MOE_BF16)
+ *                  bytes (only its status header and, for large T*k, per-block counts
+ *                  are used)
+ * An index outside [0, n) is reported by moe_check_device_error() as
+ * MOE_ERR_DEVICE_INDEX; the outputs are then undefined.
+ */
+moe_status moe_permute(const int32_t* topk_idx, int T, int k, int n, int32_t* expert_offsets,
+                       int32_t* perm, int32_t* inv_perm, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * The experts: for every expert e with rows p in [offsets[e], offsets[e+1]) and token
+ * t = perm[p] / k,   y_perm[p] = w2_e · (SiLU(w1_e · x_t) ⊙ (w3_e · x_t))
+ * ("Mixtral of Experts", Método: SwiGLU experts; ja.news.hada.io MoEレイヤーの計算方式:
+ * experts with a zero gate are not computed).  Gate weights are NOT applied here.
+ *   x [T, d], w1/w3 [n, f, d], w2 [n, d, f]: dtype;  y_perm [T*k, d]: dtype out
+ *   perm, expert_offsets: as produced by moe_permute (read on the device; the host never
+ *   sees the per-expert counts, so the call needs no synchronisation)
+ * MOE_BF16 (d, f multiples of 64) runs two persistent tcgen05 grouped GEMMs (w1|w3 with
+ * SiLU⊙ fused, then w2) fed by TMA; otherwise an fp32 CUDA-core kernel runs.
+ *   ws, ws_bytes: at least moe_workspace_size(T, d, f, n, k, dtype) bytes.
+ */
+moe_status moe_grouped_swiglu(const void* x, const int32_t* perm, const int32_t* expert_offsets,
+                              const void* w1, const void* w3, const void* w2, int T, int d, int f,
+                              int n, int k, int dtype, void* y_perm, void* ws, size_t ws_bytes,
+                              void* stream);
+
+/*
+ * The two halves of moe_grouped_swiglu, for callers that keep the intermediate themselves
+ * or time the projections separately.  Together they compute exactly moe_grouped_swiglu.
+ *   moe_expert_up:   h[p] = SiLU(w1_e · x_t) ⊙ (w3_e · x_t),  t = perm[p] / k
+ *                    h [T*k, f] dtype out (bf16: rounded once).  ws as for moe_grouped_swiglu
+ *                    (holds the expert-ordered copy of x).
+ *   moe_expert_down: y_perm[p] = w2_e · h[p]      (ws: only its status header is used)
+ */
+moe_status moe_expert_up(const void* x, const int32_t* perm, const int32_t* expert_offsets,
+                         const void* w1, const void* w3, int T, int d, int f, int n, int k,
+                         int dtype, void* h, void* ws, size_t ws_bytes, void* stream);
+moe_status moe_expert_down(const void* h, const int32_t* expert_offsets, const void* w2, int T,
+                           int d, int f, int n, int k, int dtype, void* y_perm, void* ws,
+                           size_t ws_bytes, void* stream);
+
+/*
+ * Gate-weighted sum back in token order ("Mixtral of Experts", Método, eq. y):
+ *   y[t] = sum_{slot<k} topk_w[t, slot] · y_perm[inv_perm[t*k + slot]]  (+ residual[t])
+ * fp32 accumulation in ascending slot order (deterministic), one rounding to dtype.
+ *   residual [T, d] dtype, nullable.   y may alias residual.
+ */
+moe_status moe_combine(const void* y_perm, const int32_t* inv_perm, const float* topk_w,
+                       const void* residual, int T, int d, int k, int dtype, void* y, void* stream);
+
+/*
+ * Row-wise RMSNorm with unit weight, x[t] = h[t] / sqrt(mean(h[t]^2) + eps), fp32 math,
+ * one rounding to dtype.  Not part of the pages' layer; used by stacked layers
+ * h <- h + MoE(RMSNorm(h)).   x may not alias h.
+ */
+moe_status moe_rmsnorm(const void* h, int T, int d, float eps, int dtype, void* x, void* stream);
+
+/*
+ * One whole MoE layer: router_topk -> permute -> grouped_swiglu -> combine, all on
+ * `stream`, no host synchronisation (the sequence can be captured in a CUDA graph).
+ *   residual          [T, d] nullable: y = residual + MoE(x)
+ *   topk_idx_out      [T, k] int32 nullable: copy of the chosen experts
+ *   expert_offsets_out[n+1] int32 nullable: copy of the per-expert offsets
+ *   ws, ws_bytes      at least moe_workspace_size(T, d, f, n, k, dtype) bytes
+ */
+moe_status moe_layer_forward(const void* x, const void* w_gate, const float* logit_bias,
+                             const void* w1, const void* w3, const void* w2, const void* residual,
+                             int T, int d, int f, int n, int k, int dtype, void* y,
+                             int32_t* topk_idx_out, int32_t* expert_offsets_out, void* ws,
+                             size_t ws_bytes, void* stream);
+
+/*
+ * Synchronise `stream`, read the device status word that the kernels of the last calls
+ * using this workspace may have set, and clear it.  Returns MOE_OK, MOE_ERR_TIMEOUT or
+ * MOE_ERR_DEVICE_INDEX (or MOE_ERR_CUDA if the synchronisation itself failed).
+ */
+moe_status moe_check_device_error(void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Wait limit, in nanoseconds, of every bounded wait inside the tensor-core kernels
+ * (default 2e9).  A wait that runs past it makes its kernel stop cleanly and set
+ * MOE_ERR_TIMEOUT.  Process-wide; takes effect at the next launch.  0 restores the default.
+ */
+void moe_set_wait_limit_ns(unsigned long long ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H_ */

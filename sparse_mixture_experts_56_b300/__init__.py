@@ -1,0 +1,202 @@
+"""B300-native sparse mixture-of-experts feed-forward layer (Mixtral 8x7B style).
+
+    G(x) = Softmax(TopK(x · W_g)),   y = sum_i G(x)_i · w2_i (SiLU(w1_i x) ⊙ (w3_i x))
+
+Thin Python binding of libmoe.so.  Each function marshals torch CUDA tensors (device
+memory and the current stream) into the C call of the same name declared in
+include/moe.h; every step of the layer runs in the library's CUDA kernels.  When a result
+tensor is not passed in, it is allocated with torch on the input's device.
+"""
+from __future__ import annotations
+
+from typing import Optional, Tuple
+
+import torch
+
+from . import _native
+from ._native import MOE_BF16, MOE_F32, MoEError, check
+
+__all__ = [
+    "MOE_F32", "MOE_BF16", "MoEError", "dtype_code", "moe_workspace_size", "workspace",
+    "moe_router_topk", "moe_permute", "moe_grouped_swiglu", "moe_expert_up", "moe_expert_down",
+    "moe_combine", "moe_rmsnorm",
+    "moe_layer_forward", "moe_check_device_error", "moe_set_wait_limit_ns", "moe_version",
+    "library_path",
+]
+
+
+def library_path() -> str:
+    return _native.LIB_PATH
+
+
+def dtype_code(dt: torch.dtype) -> int:
+    if dt == torch.float32:
+        return MOE_F32
+    if dt == torch.bfloat16:
+        return MOE_BF16
+    raise ValueError(f"unsupported dtype {dt}: float32 or bfloat16")
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensors must live on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def moe_version() -> int:
+    return _native.lib().moe_version()
+
+
+def moe_workspace_size(T: int, d: int, f: int, n: int, k: int, dtype) -> int:
+    code = dtype if isinstance(dtype, int) else dtype_code(dtype)
+    return int(_native.lib().moe_workspace_size(T, d, f, n, k, code))
+
+
+def workspace(T: int, d: int, f: int, n: int, k: int, dtype, device="cuda") -> torch.Tensor:
+    """A zeroed workspace buffer of moe_workspace_size bytes."""
+    size = moe_workspace_size(T, d, f, n, k, dtype)
+    if size == 0:
+        raise ValueError("invalid sizes")
+    return torch.zeros(size, dtype=torch.uint8, device=device)
+
+
+def moe_set_wait_limit_ns(ns: int) -> None:
+    _native.lib().moe_set_wait_limit_ns(int(ns))
+
+
+def moe_check_device_error(ws: torch.Tensor, stream=None) -> int:
+    """Synchronises the stream and returns (and clears) the workspace's device status."""
+    return int(_native.lib().moe_check_device_error(_ptr(ws), ws.numel(), _stream(stream)))
+
+
+def moe_router_topk(x: torch.Tensor, w_gate: torch.Tensor, k: int,
+                    logit_bias: Optional[torch.Tensor] = None, *, want_logits: bool = False,
+                    topk_idx: Optional[torch.Tensor] = None, topk_w: Optional[torch.Tensor] = None,
+                    logits: Optional[torch.Tensor] = None, stream=None):
+    T, d = x.shape
+    n = w_gate.shape[1]
+    dev = x.device
+    if topk_idx is None:
+        topk_idx = torch.empty((T, k), dtype=torch.int32, device=dev)
+    if topk_w is None:
+        topk_w = torch.empty((T, k), dtype=torch.float32, device=dev)
+    if want_logits and logits is None:
+        logits = torch.empty((T, n), dtype=torch.float32, device=dev)
+    st = _native.lib().moe_router_topk(_ptr(x), _ptr(w_gate), _ptr(logit_bias), T, d, n, k,
+                                       dtype_code(x.dtype), _ptr(topk_idx), _ptr(topk_w),
+                                       _ptr(logits), _stream(stream))
+    check("moe_router_topk", st)
+    return topk_idx, topk_w, logits
+
+
+def moe_permute(topk_idx: torch.Tensor, n: int, ws: torch.Tensor, *,
+                expert_offsets: Optional[torch.Tensor] = None, perm: Optional[torch.Tensor] = None,
+                inv_perm: Optional[torch.Tensor] = None, stream=None):
+    T, k = topk_idx.shape
+    dev = topk_idx.device
+    if expert_offsets is None:
+        expert_offsets = torch.empty(n + 1, dtype=torch.int32, device=dev)
+    if perm is None:
+        perm = torch.empty(T * k, dtype=torch.int32, device=dev)
+    if inv_perm is None:
+        inv_perm = torch.empty(T * k, dtype=torch.int32, device=dev)
+    st = _native.lib().moe_permute(_ptr(topk_idx), T, k, n, _ptr(expert_offsets), _ptr(perm),
+                                   _ptr(inv_perm), _ptr(ws), ws.numel(), _stream(stream))
+    check("moe_permute", st)
+    return expert_offsets, perm, inv_perm
+
+
+def moe_grouped_swiglu(x: torch.Tensor, perm: torch.Tensor, expert_offsets: torch.Tensor,
+                       w1: torch.Tensor, w3: torch.Tensor, w2: torch.Tensor, k: int,
+                       ws: torch.Tensor, *, y_perm: Optional[torch.Tensor] = None, stream=None):
+    T, d = x.shape
+    n, f, _ = w1.shape
+    if y_perm is None:
+        y_perm = torch.empty((T * k, d), dtype=x.dtype, device=x.device)
+    st = _native.lib().moe_grouped_swiglu(_ptr(x), _ptr(perm), _ptr(expert_offsets), _ptr(w1),
+                                          _ptr(w3), _ptr(w2), T, d, f, n, k, dtype_code(x.dtype),
+                                          _ptr(y_perm), _ptr(ws), ws.numel(), _stream(stream))
+    check("moe_grouped_swiglu", st)
+    return y_perm
+
+
+def moe_expert_up(x: torch.Tensor, perm: torch.Tensor, expert_offsets: torch.Tensor,
+                  w1: torch.Tensor, w3: torch.Tensor, k: int, ws: torch.Tensor, *,
+                  h: Optional[torch.Tensor] = None, stream=None):
+    T, d = x.shape
+    n, f, _ = w1.shape
+    if h is None:
+        h = torch.empty((T * k, f), dtype=x.dtype, device=x.device)
+    st = _native.lib().moe_expert_up(_ptr(x), _ptr(perm), _ptr(expert_offsets), _ptr(w1), _ptr(w3),
+                                     T, d, f, n, k, dtype_code(x.dtype), _ptr(h), _ptr(ws),
+                                     ws.numel(), _stream(stream))
+    check("moe_expert_up", st)
+    return h
+
+
+def moe_expert_down(h: torch.Tensor, expert_offsets: torch.Tensor, w2: torch.Tensor, k: int,
+                    ws: torch.Tensor, *, y_perm: Optional[torch.Tensor] = None, stream=None):
+    A, f = h.shape
+    n, d, _ = w2.shape
+    T = A // k
+    if y_perm is None:
+        y_perm = torch.empty((A, d), dtype=h.dtype, device=h.device)
+    st = _native.lib().moe_expert_down(_ptr(h), _ptr(expert_offsets), _ptr(w2), T, d, f, n, k,
+                                       dtype_code(h.dtype), _ptr(y_perm), _ptr(ws), ws.numel(),
+                                       _stream(stream))
+    check("moe_expert_down", st)
+    return y_perm
+
+
+def moe_combine(y_perm: torch.Tensor, inv_perm: torch.Tensor, topk_w: torch.Tensor,
+                residual: Optional[torch.Tensor] = None, *, y: Optional[torch.Tensor] = None,
+                stream=None):
+    T, k = topk_w.shape
+    d = y_perm.shape[1]
+    if y is None:
+        y = torch.empty((T, d), dtype=y_perm.dtype, device=y_perm.device)
+    st = _native.lib().moe_combine(_ptr(y_perm), _ptr(inv_perm), _ptr(topk_w), _ptr(residual), T, d,
+                                   k, dtype_code(y_perm.dtype), _ptr(y), _stream(stream))
+    check("moe_combine", st)
+    return y
+
+
+def moe_rmsnorm(h: torch.Tensor, eps: float = 1e-5, *, x: Optional[torch.Tensor] = None,
+                stream=None):
+    T, d = h.shape
+    if x is None:
+        x = torch.empty_like(h)
+    st = _native.lib().moe_rmsnorm(_ptr(h), T, d, float(eps), dtype_code(h.dtype), _ptr(x),
+                                   _stream(stream))
+    check("moe_rmsnorm", st)
+    return x
+
+
+def moe_layer_forward(x: torch.Tensor, w_gate: torch.Tensor, w1: torch.Tensor, w3: torch.Tensor,
+                      w2: torch.Tensor, k: int, ws: torch.Tensor, *,
+                      logit_bias: Optional[torch.Tensor] = None,
+                      residual: Optional[torch.Tensor] = None, y: Optional[torch.Tensor] = None,
+                      topk_idx_out: Optional[torch.Tensor] = None,
+                      expert_offsets_out: Optional[torch.Tensor] = None, stream=None):
+    T, d = x.shape
+    n, f, _ = w1.shape
+    if y is None:
+        y = torch.empty_like(x)
+    st = _native.lib().moe_layer_forward(_ptr(x), _ptr(w_gate), _ptr(logit_bias), _ptr(w1), _ptr(w3),
+                                         _ptr(w2), _ptr(residual), T, d, f, n, k, dtype_code(x.dtype),
+                                         _ptr(y), _ptr(topk_idx_out), _ptr(expert_offsets_out),
+                                         _ptr(ws), ws.numel(), _stream(stream))
+    check("moe_layer_forward", st)
+    return y

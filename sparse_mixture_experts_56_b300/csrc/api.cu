@@ -1,0 +1,294 @@
+// C ABI of libmoe.so: argument validation, workspace layout and the launch sequence of
+// the MoE layer  y = sum_i G(x)_i · E_i(x),  G(x) = Softmax(TopK(x · W_g))
+// ("Mixtral of Experts" (xyznot.com summary), Método; blog.csdn.net MOE数学公式).
+// Everything is stream-ordered; nothing here synchronises except moe_check_device_error.
+#include <atomic>
+#include <mutex>
+
+#include "moe_internal.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr unsigned long long kDefaultWaitNs = 2000000000ull;
+std::atomic<unsigned long long> g_wait_ns{kDefaultWaitNs};
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+struct Layout {
+  size_t scratch, idx, w, offsets, perm, inv_perm, x_perm, h, y_perm;
+  size_t permute_end, grouped_end, total;
+};
+
+Layout layout(long long T, long long d, long long f, int n, int k, int dtype) {
+  const size_t esz = dtype == MOE_BF16 ? 2 : 4;
+  const long long A = T * k;
+  Layout L;
+  size_t off = kAlign;  // status header
+  L.scratch = off;
+  off += align_up((size_t)2 * permute_blocks(A) * n * sizeof(int32_t));
+  L.permute_end = off;
+  L.idx = off;
+  off += align_up((size_t)A * sizeof(int32_t));
+  L.w = off;
+  off += align_up((size_t)A * sizeof(float));
+  L.offsets = off;
+  off += align_up((size_t)(n + 1) * sizeof(int32_t));
+  L.perm = off;
+  off += align_up((size_t)A * sizeof(int32_t));
+  L.inv_perm = off;
+  off += align_up((size_t)A * sizeof(int32_t));
+  L.x_perm = off;
+  off += align_up((size_t)A * d * esz);
+  L.h = off;
+  off += align_up((size_t)A * f * esz);
+  L.grouped_end = off;
+  L.y_perm = off;
+  off += align_up((size_t)A * d * esz);
+  L.total = off;
+  return L;
+}
+
+inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+inline bool dtype_ok(int dt) { return dt == MOE_F32 || dt == MOE_BF16; }
+
+bool sizes_ok(long long T, long long d, long long f, int n, int k) {
+  if (T < 0 || d < 1 || f < 1) return false;
+  if (n < 1 || n > kMaxExperts || k < 1 || k > n) return false;
+  if (T * k >= (1ll << 31)) return false;
+  if (d >= (1ll << 31) || f >= (1ll << 31)) return false;
+  return true;
+}
+
+inline moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+inline uint32_t* status_word(void* ws) { return reinterpret_cast<uint32_t*>(ws); }
+
+// The tensor-core path takes bf16 shapes whose rows are whole 64-element swizzle atoms.
+inline bool use_tc(int dtype, int d, int f) { return dtype == MOE_BF16 && d % 64 == 0 && f % 64 == 0; }
+
+moe_status up_impl(const void* x, const int32_t* perm, const int32_t* offsets, const void* w1,
+                   const void* w3, int T, int d, int f, int n, int k, int dtype, void* h, void* ws,
+                   const Layout& L, cudaStream_t s) {
+  const int A = T * k;
+  if (A == 0) return MOE_OK;
+  void* x_perm = static_cast<char*>(ws) + L.x_perm;
+  const size_t esz = dtype == MOE_BF16 ? 2 : 4;
+  cudaError_t e = launch_gather_rows(x, perm, A, k, (size_t)d * esz, x_perm, s);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  if (use_tc(dtype, d, f))
+    e = launch_up_tc((const bf16*)x_perm, offsets, (const bf16*)w1, (const bf16*)w3, A, d, f, n,
+                     (bf16*)h, status_word(ws), g_wait_ns.load(), s);
+  else
+    e = launch_up_simt(x_perm, offsets, w1, w3, A, d, f, n, dtype, h, s);
+  return cuda_status(e);
+}
+
+moe_status down_impl(const void* h, const int32_t* offsets, const void* w2, int T, int d, int f,
+                     int n, int k, int dtype, void* y_perm, void* ws, cudaStream_t s) {
+  const int A = T * k;
+  if (A == 0) return MOE_OK;
+  cudaError_t e;
+  if (use_tc(dtype, d, f))
+    e = launch_down_tc((const bf16*)h, offsets, (const bf16*)w2, A, d, f, n, (bf16*)y_perm,
+                       status_word(ws), g_wait_ns.load(), s);
+  else
+    e = launch_down_simt(h, offsets, w2, A, d, f, n, dtype, y_perm, s);
+  return cuda_status(e);
+}
+
+moe_status grouped_impl(const void* x, const int32_t* perm, const int32_t* offsets, const void* w1,
+                        const void* w3, const void* w2, int T, int d, int f, int n, int k, int dtype,
+                        void* y_perm, void* ws, const Layout& L, cudaStream_t s) {
+  void* h = static_cast<char*>(ws) + L.h;
+  moe_status st = up_impl(x, perm, offsets, w1, w3, T, d, f, n, k, dtype, h, ws, L, s);
+  if (st != MOE_OK) return st;
+  return down_impl(h, offsets, w2, T, d, f, n, k, dtype, y_perm, ws, s);
+}
+
+}  // namespace
+
+int device_sm_count() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 148;
+  if (dev < 64 && cache[dev] > 0) return cache[dev];
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+    sms = 148;
+  if (dev < 64) cache[dev] = sms;
+  return sms;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+const char* moe_status_string(int status) {
+  switch (status) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+    case MOE_ERR_DEVICE_INDEX: return "MOE_ERR_DEVICE_INDEX";
+    default: return "MOE_ERR_UNKNOWN";
+  }
+}
+
+int moe_version(void) { return 100; }
+
+size_t moe_workspace_size(int T, int d, int f, int n, int k, int dtype) {
+  if (!dtype_ok(dtype) || !sizes_ok(T, d, f, n, k)) return 0;
+  return layout(T, d, f, n, k, dtype).total;
+}
+
+moe_status moe_router_topk(const void* x, const void* w_gate, const float* logit_bias, int T, int d,
+                           int n, int k, int dtype, int32_t* topk_idx, float* topk_w, float* logits,
+                           void* stream) {
+  if (!dtype_ok(dtype) || !sizes_ok(T, d, 1, n, k)) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!x || !w_gate || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w_gate)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_router_topk(x, w_gate, logit_bias, T, d, n, k, dtype, topk_idx, topk_w,
+                                        logits, (cudaStream_t)stream));
+}
+
+moe_status moe_permute(const int32_t* topk_idx, int T, int k, int n, int32_t* expert_offsets,
+                       int32_t* perm, int32_t* inv_perm, void* ws, size_t ws_bytes, void* stream) {
+  if (!sizes_ok(T, 64, 64, n, k)) return MOE_ERR_INVALID_ARG;
+  if (!expert_offsets || (T > 0 && (!topk_idx || !perm || !inv_perm))) return MOE_ERR_INVALID_ARG;
+  const Layout L = layout(T, 64, 64, n, k, MOE_BF16);
+  if (!ws || ws_bytes < L.permute_end || !aligned16(ws)) return MOE_ERR_WORKSPACE;
+  char* base = static_cast<char*>(ws);
+  return cuda_status(launch_permute(topk_idx, T * k, n, expert_offsets, perm, inv_perm,
+                                    reinterpret_cast<int32_t*>(base + L.scratch), status_word(ws),
+                                    (cudaStream_t)stream));
+}
+
+moe_status moe_grouped_swiglu(const void* x, const int32_t* perm, const int32_t* expert_offsets,
+                              const void* w1, const void* w3, const void* w2, int T, int d, int f,
+                              int n, int k, int dtype, void* y_perm, void* ws, size_t ws_bytes,
+                              void* stream) {
+  if (!dtype_ok(dtype) || !sizes_ok(T, d, f, n, k)) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!x || !perm || !expert_offsets || !w1 || !w3 || !w2 || !y_perm) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w1) || !aligned16(w3) || !aligned16(w2) || !aligned16(y_perm))
+    return MOE_ERR_INVALID_ARG;
+  const Layout L = layout(T, d, f, n, k, dtype);
+  if (!ws || ws_bytes < L.grouped_end || !aligned16(ws)) return MOE_ERR_WORKSPACE;
+  return grouped_impl(x, perm, expert_offsets, w1, w3, w2, T, d, f, n, k, dtype, y_perm, ws, L,
+                      (cudaStream_t)stream);
+}
+
+moe_status moe_expert_up(const void* x, const int32_t* perm, const int32_t* expert_offsets,
+                         const void* w1, const void* w3, int T, int d, int f, int n, int k,
+                         int dtype, void* h, void* ws, size_t ws_bytes, void* stream) {
+  if (!dtype_ok(dtype) || !sizes_ok(T, d, f, n, k)) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!x || !perm || !expert_offsets || !w1 || !w3 || !h) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w1) || !aligned16(w3) || !aligned16(h)) return MOE_ERR_INVALID_ARG;
+  const Layout L = layout(T, d, f, n, k, dtype);
+  if (!ws || ws_bytes < L.grouped_end || !aligned16(ws)) return MOE_ERR_WORKSPACE;
+  return up_impl(x, perm, expert_offsets, w1, w3, T, d, f, n, k, dtype, h, ws, L,
+                 (cudaStream_t)stream);
+}
+
+moe_status moe_expert_down(const void* h, const int32_t* expert_offsets, const void* w2, int T,
+                           int d, int f, int n, int k, int dtype, void* y_perm, void* ws,
+                           size_t ws_bytes, void* stream) {
+  if (!dtype_ok(dtype) || !sizes_ok(T, d, f, n, k)) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!h || !expert_offsets || !w2 || !y_perm) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(h) || !aligned16(w2) || !aligned16(y_perm)) return MOE_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < kAlign || !aligned16(ws)) return MOE_ERR_WORKSPACE;
+  return down_impl(h, expert_offsets, w2, T, d, f, n, k, dtype, y_perm, ws, (cudaStream_t)stream);
+}
+
+moe_status moe_combine(const void* y_perm, const int32_t* inv_perm, const float* topk_w,
+                       const void* residual, int T, int d, int k, int dtype, void* y, void* stream) {
+  if (!dtype_ok(dtype) || !sizes_ok(T, d, 1, k, k)) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!y_perm || !inv_perm || !topk_w || !y) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(y_perm) || !aligned16(y) || (residual && !aligned16(residual)))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_combine(y_perm, inv_perm, topk_w, residual, T, d, k, dtype, y,
+                                    (cudaStream_t)stream));
+}
+
+moe_status moe_rmsnorm(const void* h, int T, int d, float eps, int dtype, void* x, void* stream) {
+  if (!dtype_ok(dtype) || !sizes_ok(T, d, 1, 1, 1) || !(eps >= 0.f)) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!h || !x || h == x || !aligned16(h) || !aligned16(x)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_rmsnorm(h, T, d, eps, dtype, x, (cudaStream_t)stream));
+}
+
+moe_status moe_layer_forward(const void* x, const void* w_gate, const float* logit_bias,
+                             const void* w1, const void* w3, const void* w2, const void* residual,
+                             int T, int d, int f, int n, int k, int dtype, void* y,
+                             int32_t* topk_idx_out, int32_t* expert_offsets_out, void* ws,
+                             size_t ws_bytes, void* stream) {
+  if (!dtype_ok(dtype) || !sizes_ok(T, d, f, n, k)) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (T == 0) {
+    if (expert_offsets_out)
+      return cuda_status(cudaMemsetAsync(expert_offsets_out, 0, (size_t)(n + 1) * 4, s));
+    return MOE_OK;
+  }
+  if (!x || !w_gate || !w1 || !w3 || !w2 || !y) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w_gate) || !aligned16(w1) || !aligned16(w3) || !aligned16(w2) ||
+      !aligned16(y) || (residual && !aligned16(residual)))
+    return MOE_ERR_INVALID_ARG;
+  const Layout L = layout(T, d, f, n, k, dtype);
+  if (!ws || ws_bytes < L.total || !aligned16(ws)) return MOE_ERR_WORKSPACE;
+  char* base = static_cast<char*>(ws);
+  int32_t* idx = reinterpret_cast<int32_t*>(base + L.idx);
+  float* w = reinterpret_cast<float*>(base + L.w);
+  int32_t* offsets = reinterpret_cast<int32_t*>(base + L.offsets);
+  int32_t* perm = reinterpret_cast<int32_t*>(base + L.perm);
+  int32_t* inv_perm = reinterpret_cast<int32_t*>(base + L.inv_perm);
+  void* y_perm = base + L.y_perm;
+  const int A = T * k;
+
+  cudaError_t e = launch_router_topk(x, w_gate, logit_bias, T, d, n, k, dtype, idx, w, nullptr, s);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  e = launch_permute(idx, A, n, offsets, perm, inv_perm, reinterpret_cast<int32_t*>(base + L.scratch),
+                     status_word(ws), s);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  moe_status st = grouped_impl(x, perm, offsets, w1, w3, w2, T, d, f, n, k, dtype, y_perm, ws, L, s);
+  if (st != MOE_OK) return st;
+  e = launch_combine(y_perm, inv_perm, w, residual, T, d, k, dtype, y, s);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  if (topk_idx_out &&
+      cudaMemcpyAsync(topk_idx_out, idx, (size_t)A * 4, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (expert_offsets_out && cudaMemcpyAsync(expert_offsets_out, offsets, (size_t)(n + 1) * 4,
+                                            cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+moe_status moe_check_device_error(void* ws, size_t ws_bytes, void* stream) {
+  if (!ws || ws_bytes < kAlign) return MOE_ERR_WORKSPACE;
+  cudaStream_t s = (cudaStream_t)stream;
+  uint32_t word = 0;
+  if (cudaMemcpyAsync(&word, ws, sizeof(word), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (word != 0) {
+    if (cudaMemsetAsync(ws, 0, sizeof(word), s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  if (word & kDevErrTimeout) return MOE_ERR_TIMEOUT;
+  if (word & kDevErrIndex) return MOE_ERR_DEVICE_INDEX;
+  return MOE_OK;
+}
+
+void moe_set_wait_limit_ns(unsigned long long ns) { g_wait_ns.store(ns ? ns : kDefaultWaitNs); }
+
+}  // extern "C"

@@ -1,0 +1,570 @@
+// Experts on the 5th-generation tensor cores (bf16 in, fp32 accumulate in TMEM):
+//   GEMM1  h[p, :]      = SiLU(x_p · w1_eᵀ) ⊙ (x_p · w3_eᵀ)      (SwiGLU fused in the epilogue)
+//   GEMM2  y_perm[p, :] = h[p, :] · w2_eᵀ
+// for the rows p in [offsets[e], offsets[e+1]) of every expert e ("Mixtral of Experts"
+// (xyznot.com summary), Método: each expert is a SwiGLU network of intermediate size 14336;
+// ja.news.hada.io, 実装と推論効率: experts receive variable numbers of tokens).
+//
+// Design (one persistent CTA per SM, 256 threads):
+//   warp 0      TMA producer: A tile [128 x 64] + B tile [256 x 64] per stage, 128-byte
+//               swizzle, into a 4-stage shared-memory ring (48 KB per stage).
+//   warp 1      MMA issuer: tcgen05.mma.cta_group::1.kind::f16, M=128 N=256 K=16, four per
+//               stage, into one of two TMEM accumulators (2 x 256 columns = all 512).
+//   warp 2      allocates / frees the 512 TMEM columns.
+//   warps 4-7   epilogue: tcgen05.ld 32x32b (warp w reads TMEM lanes 32*(w-4)...), then
+//               GEMM1: SiLU(a)⊙b -> bf16 h;  GEMM2: -> bf16 y_perm.  Rows beyond the
+//               expert's count are computed but never stored.
+// For GEMM1 the B tile stacks 128 rows of w1_e over the same 128 rows of w3_e, so one
+// N=256 MMA fills both halves of the accumulator that the SwiGLU epilogue pairs up.
+// Work list: tiles (expert, m-tile, n-tile) enumerated on the device from expert_offsets
+// (no host synchronisation); within an expert, groups of 16 m-tiles sweep all n-tiles so
+// that the weight tiles of concurrently running CTAs are shared through L2.
+//
+// Every wait is bounded (globaltimer).  A wait that runs past the limit raises the CTA's
+// abort flag and sets the timeout bit of the device status word; every role then stops,
+// the producer waits (bounded) for its copies in flight, the MMA warp waits for its MMAs,
+// and the TMEM columns are freed before the CTA exits.
+#include <cuda.h>
+
+#include <mutex>
+
+#include "moe_internal.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128;                 // tile rows (tokens)  = UMMA M
+constexpr int BK = 64;                  // K per stage: one 128-byte swizzle atom of bf16
+constexpr int BN = 256;                 // B rows per stage    = UMMA N = accumulator columns
+constexpr int UMMA_K = 16;
+constexpr int STAGES = 4;
+constexpr int ACC = 2;                  // TMEM accumulators
+constexpr uint32_t TMEM_COLS = 512;
+constexpr int GROUP_M = 16;
+constexpr uint32_t A_BYTES = BM * BK * 2;
+constexpr uint32_t B_BYTES = BN * BK * 2;
+constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr uint64_t kDrainNs = 200ull * 1000 * 1000;
+
+// instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A bf16 (7-9 = 1), B bf16
+// (10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 at bits 17-22, M >> 4 at bits 24-28.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
+                            ((uint32_t)(BM >> 4) << 24);
+
+enum Mode { kSwiGLU = 0, kDown = 1 };
+
+struct TcArgs {
+  const int32_t* offsets;
+  int n;
+  int kdim;   // reduction length: d (GEMM1) or f (GEMM2)
+  int ndim;   // output columns: f (GEMM1) or d (GEMM2)
+  int ntiles; // n-tiles per expert
+  bf16* out;  // [A, ndim]
+  uint32_t* status;
+  unsigned long long wait_ns;
+};
+
+struct Shared {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t tfull[ACC];
+  uint64_t tempty[ACC];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+  int total;
+  int tile_base[kMaxExperts + 1];
+  int mtiles[kMaxExperts];
+  int off[kMaxExperts + 1];
+};
+
+constexpr size_t kSmemBytes = 1024 + (size_t)STAGES * STAGE_BYTES + sizeof(Shared);
+
+// ------------------------------------------------------------------------------------------
+// PTX wrappers
+// ------------------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ uint64_t gtimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.b32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"((uint64_t)map), "r"(bar), "r"(c0), "r"(c1)
+      : "memory");
+}
+__device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)map) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row atoms 1024 bytes apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | (1ull << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         (1ull << 46) | (2ull << 61);
+}
+__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   bar)
+               : "memory");
+}
+
+#define MOE_R32(r)                                                                               \
+  "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),           \
+      "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),   \
+      "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),             \
+      "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),             \
+      "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+#define MOE_P32(r)                                                                               \
+  "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),           \
+      "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),   \
+      "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]),             \
+      "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]),             \
+      "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+      "%28, %29, %30, %31}, [%32];"
+      : MOE_R32(r)
+      : "r"(taddr));
+}
+// Waits for the thread's outstanding tcgen05.ld; the registers are threaded through the asm
+// so that no use of them can be scheduled before the wait.
+__device__ __forceinline__ void tmem_wait(uint32_t (&r)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" : MOE_P32(r)::"memory");
+}
+
+// ------------------------------------------------------------------------------------------
+// bounded waits
+// ------------------------------------------------------------------------------------------
+__device__ __forceinline__ void raise_abort(volatile int* abort, uint32_t* status) {
+  if (!*abort) {
+    *abort = 1;
+    atomicOr(status, kDevErrTimeout);
+  }
+}
+// Waits for the phase of parity `parity` of `bar`; false on abort or after limit_ns.
+__device__ __noinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort,
+                                        uint64_t limit_ns) {
+  if (mbar_test(bar, parity)) return true;
+  const uint64_t t0 = gtimer();
+  for (;;) {
+    if (mbar_test(bar, parity)) return true;
+    if (*abort) return false;
+    if (gtimer() - t0 > limit_ns) return false;
+  }
+}
+// Same, ignoring the abort flag (used to drain work already in flight).
+__device__ __noinline__ bool drain_phase(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = gtimer();
+  for (;;) {
+    if (mbar_test(bar, parity)) return true;
+    if (gtimer() - t0 > limit_ns) return false;
+  }
+}
+
+struct Tile {
+  int e, mt, nt, row0, rows;
+};
+
+__device__ __forceinline__ Tile decode_tile(const Shared& sh, int n, int ntiles, int tile) {
+  int e = 0;
+  while (e + 1 < n && sh.tile_base[e + 1] <= tile) ++e;
+  const int u = tile - sh.tile_base[e];
+  const int per_group = GROUP_M * ntiles;
+  const int g = u / per_group, r = u - g * per_group;
+  const int gsz = min(GROUP_M, sh.mtiles[e] - g * GROUP_M);
+  Tile t;
+  t.e = e;
+  t.mt = g * GROUP_M + r % gsz;
+  t.nt = r / gsz;
+  t.row0 = sh.off[e] + t.mt * BM;
+  t.rows = min(BM, sh.off[e + 1] - sh.off[e] - t.mt * BM);
+  return t;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ void store_row32(bf16* dst, const float (&v)[32]) {
+  uint4* q = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    uint4 o;
+    o.x = pack_bf16x2(v[8 * j + 0], v[8 * j + 1]);
+    o.y = pack_bf16x2(v[8 * j + 2], v[8 * j + 3]);
+    o.z = pack_bf16x2(v[8 * j + 4], v[8 * j + 5]);
+    o.w = pack_bf16x2(v[8 * j + 6], v[8 * j + 7]);
+    q[j] = o;
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+// the kernel
+// ------------------------------------------------------------------------------------------
+template <int MODE>
+__global__ void __launch_bounds__(256, 1)
+    grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
+                           const __grid_constant__ CUtensorMap tmB0,
+                           const __grid_constant__ CUtensorMap tmB1, const TcArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;                              // STAGES x 16 KB
+  uint8_t* sB = smem + STAGES * A_BYTES;           // STAGES x 32 KB
+  Shared& sh = *reinterpret_cast<Shared*>(smem + STAGES * STAGE_BYTES);
+  volatile int* abort = &sh.abort;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n = args.n;
+  const int KB = args.kdim / BK;
+
+  if (threadIdx.x == 0) {
+    int acc = 0;
+    for (int e = 0; e < n; ++e) {
+      const int o0 = args.offsets[e], o1 = args.offsets[e + 1];
+      const int mt = (o1 - o0 + BM - 1) / BM;
+      sh.off[e] = o0;
+      sh.mtiles[e] = mt;
+      sh.tile_base[e] = acc;
+      acc += mt * args.ntiles;
+    }
+    sh.off[n] = args.offsets[n];
+    sh.tile_base[n] = acc;
+    sh.total = acc;
+    sh.abort = 0;
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&sh.full[s]), 1);
+      mbar_init(smem_u32(&sh.empty[s]), 1);
+    }
+    for (int a = 0; a < ACC; ++a) {
+      mbar_init(smem_u32(&sh.tfull[a]), 1);
+      mbar_init(smem_u32(&sh.tempty[a]), 4);
+    }
+    mbar_init(smem_u32(&sh.drain), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 2) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&sh.tmem_base)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = sh.tmem_base;
+  const int total = sh.total;
+  const uint64_t limit = args.wait_ns;
+
+  if (warp == 0 && lane == 0) {
+    // ---------------------------------------------------------------- TMA producer
+    prefetch_map(&tmA);
+    prefetch_map(&tmB0);
+    if (MODE == kSwiGLU) prefetch_map(&tmB1);
+    int stage = 0;
+    uint32_t phase = 0, issued = 0, iphase = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+      const Tile t = decode_tile(sh, n, args.ntiles, tile);
+      const int brow = t.e * args.ndim + t.nt * (MODE == kSwiGLU ? BN / 2 : BN);
+      for (int kb = 0; kb < KB; ++kb) {
+        if (!wait_phase(smem_u32(&sh.empty[stage]), phase ^ 1u, abort, limit)) {
+          raise_abort(abort, args.status);
+          ok = false;
+          break;
+        }
+        const uint32_t fb = smem_u32(&sh.full[stage]);
+        mbar_expect_tx(fb, STAGE_BYTES);
+        tma_load_2d(smem_u32(sA + stage * A_BYTES), &tmA, fb, kb * BK, t.row0);
+        tma_load_2d(smem_u32(sB + stage * B_BYTES), &tmB0, fb, kb * BK, brow);
+        if (MODE == kSwiGLU)
+          tma_load_2d(smem_u32(sB + stage * B_BYTES + B_BYTES / 2), &tmB1, fb, kb * BK, brow);
+        issued |= 1u << stage;
+        iphase = (iphase & ~(1u << stage)) | (phase << stage);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    // every copy issued must have landed before the CTA may exit
+    for (int s = 0; s < STAGES; ++s)
+      if ((issued >> s) & 1u)
+        if (!drain_phase(smem_u32(&sh.full[s]), (iphase >> s) & 1u, kDrainNs))
+          atomicOr(args.status, kDevErrTimeout);
+  } else if (warp == 1 && lane == 0) {
+    // ---------------------------------------------------------------- MMA issuer
+    int stage = 0, acc = 0;
+    uint32_t phase = 0, acc_phase = 0;
+    bool ok = true, any_mma = false;
+    for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+      if (!wait_phase(smem_u32(&sh.tempty[acc]), acc_phase ^ 1u, abort, limit)) {
+        raise_abort(abort, args.status);
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+      for (int kb = 0; kb < KB; ++kb) {
+        if (!wait_phase(smem_u32(&sh.full[stage]), phase, abort, limit)) {
+          raise_abort(abort, args.status);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a0 = smem_u32(sA + stage * A_BYTES);
+        const uint32_t b0 = smem_u32(sB + stage * B_BYTES);
+#pragma unroll
+        for (int kk = 0; kk < BK / UMMA_K; ++kk)
+          umma_bf16(d_tmem, sw128_desc(a0 + kk * UMMA_K * 2), sw128_desc(b0 + kk * UMMA_K * 2),
+                    (kb | kk) != 0 ? 1u : 0u);
+        any_mma = true;
+        umma_commit(smem_u32(&sh.empty[stage]));
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+      umma_commit(smem_u32(&sh.tfull[acc]));
+      if (++acc == ACC) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+    // all MMAs issued by this thread must finish before the TMEM columns are freed
+    if (any_mma) {
+      umma_commit(smem_u32(&sh.drain));
+      if (!drain_phase(smem_u32(&sh.drain), 0, kDrainNs)) atomicOr(args.status, kDevErrTimeout);
+    }
+  } else if (warp >= 4) {
+    // ---------------------------------------------------------------- epilogue
+    const int q = warp - 4;  // TMEM lane quarter
+    const int r = q * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      const Tile t = decode_tile(sh, n, args.ntiles, tile);
+      int ok = 1;
+      if (lane == 0) {
+        ok = wait_phase(smem_u32(&sh.tfull[acc]), acc_phase, abort, limit) ? 1 : 0;
+        if (!ok) raise_abort(abort, args.status);
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
+      const bool row_ok = r < t.rows;
+      const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+      const uint32_t tempty = smem_u32(&sh.tempty[acc]);
+      if (MODE == kSwiGLU) {
+        const int col0 = t.nt * (BN / 2);
+        bf16* orow = args.out + (size_t)(t.row0 + r) * args.ndim + col0;
+#pragma unroll 1
+        for (int c = 0; c < BN / 64; ++c) {
+          uint32_t a[32], b[32];
+          tmem_ld32(tb + c * 32, a);
+          tmem_ld32(tb + BN / 2 + c * 32, b);
+          tmem_wait(a);
+          tmem_wait(b);
+          if (c == BN / 64 - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty);
+          }
+          if (row_ok && col0 + c * 32 < args.ndim) {
+            float v[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const float av = __uint_as_float(a[j]);
+              const float bv = __uint_as_float(b[j]);
+              v[j] = av / (1.0f + __expf(-av)) * bv;
+            }
+            store_row32(orow + c * 32, v);
+          }
+        }
+      } else {
+        const int col0 = t.nt * BN;
+        bf16* orow = args.out + (size_t)(t.row0 + r) * args.ndim + col0;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t a[32];
+          tmem_ld32(tb + c * 32, a);
+          tmem_wait(a);
+          if (c == BN / 32 - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty);
+          }
+          if (row_ok && col0 + c * 32 < args.ndim) {
+            float v[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(a[j]);
+            store_row32(orow + c * 32, v);
+          }
+        }
+      }
+      if (++acc == ACC) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(TMEM_COLS)
+                 : "memory");
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+// host side
+// ------------------------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2-D bf16 tensor [rows, cols] (cols contiguous), boxes of [box_rows, 64], 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)BK, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int MODE>
+cudaError_t set_smem_attr() {
+  static cudaError_t err = cudaErrorNotReady;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    err = cudaFuncSetAttribute(grouped_gemm_tc_kernel<MODE>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  });
+  return err;
+}
+
+}  // namespace
+
+cudaError_t launch_up_tc(const bf16* x_perm, const int32_t* offsets, const bf16* w1, const bf16* w3,
+                         int A, int d, int f, int n, bf16* h, uint32_t* status,
+                         unsigned long long wait_ns, cudaStream_t s) {
+  if (A == 0) return cudaSuccess;
+  cudaError_t e = set_smem_attr<kSwiGLU>();
+  if (e != cudaSuccess) return e;
+  CUtensorMap mA, mW1, mW3;
+  if (!make_map(&mA, x_perm, (uint64_t)A, (uint64_t)d, BM) ||
+      !make_map(&mW1, w1, (uint64_t)n * f, (uint64_t)d, BN / 2) ||
+      !make_map(&mW3, w3, (uint64_t)n * f, (uint64_t)d, BN / 2))
+    return cudaErrorInvalidValue;
+  TcArgs a;
+  a.offsets = offsets;
+  a.n = n;
+  a.kdim = d;
+  a.ndim = f;
+  a.ntiles = (f + BN / 2 - 1) / (BN / 2);
+  a.out = h;
+  a.status = status;
+  a.wait_ns = wait_ns;
+  const long long tiles = ((long long)(A + BM - 1) / BM + n) * a.ntiles;
+  const int sms = device_sm_count();
+  grouped_gemm_tc_kernel<kSwiGLU><<<(int)(tiles < sms ? tiles : sms), 256, kSmemBytes, s>>>(
+      mA, mW1, mW3, a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_down_tc(const bf16* h, const int32_t* offsets, const bf16* w2, int A, int d,
+                           int f, int n, bf16* y_perm, uint32_t* status, unsigned long long wait_ns,
+                           cudaStream_t s) {
+  if (A == 0) return cudaSuccess;
+  cudaError_t e = set_smem_attr<kDown>();
+  if (e != cudaSuccess) return e;
+  CUtensorMap mA, mW2;
+  if (!make_map(&mA, h, (uint64_t)A, (uint64_t)f, BM) ||
+      !make_map(&mW2, w2, (uint64_t)n * d, (uint64_t)f, BN))
+    return cudaErrorInvalidValue;
+  TcArgs a;
+  a.offsets = offsets;
+  a.n = n;
+  a.kdim = f;
+  a.ndim = d;
+  a.ntiles = (d + BN - 1) / BN;
+  a.out = y_perm;
+  a.status = status;
+  a.wait_ns = wait_ns;
+  const long long tiles = ((long long)(A + BM - 1) / BM + n) * a.ntiles;
+  const int sms = device_sm_count();
+  grouped_gemm_tc_kernel<kDown><<<(int)(tiles < sms ? tiles : sms), 256, kSmemBytes, s>>>(
+      mA, mW2, mW2, a);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

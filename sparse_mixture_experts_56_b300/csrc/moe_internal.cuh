@@ -1,0 +1,74 @@
+// Internal declarations shared by the kernel files and the C-ABI layer of libmoe.so.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "moe.h"
+
+namespace moe {
+
+// Bits of the device status word (first 4 bytes of the workspace).
+enum : uint32_t { kDevErrTimeout = 1u, kDevErrIndex = 2u };
+
+constexpr int kMaxExperts = 32;
+
+// Assignments handled by one block of the permutation kernels (32 warps x 1024).
+constexpr int kPermuteChunk = 32768;
+
+typedef __nv_bfloat16 bf16;
+
+template <typename T>
+__device__ __forceinline__ float to_f32(T v);
+template <>
+__device__ __forceinline__ float to_f32<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ float to_f32<bf16>(bf16 v) { return __bfloat162float(v); }
+
+template <typename T>
+__device__ __forceinline__ T from_f32(float v);
+template <>
+__device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ bf16 from_f32<bf16>(float v) { return __float2bfloat16_rn(v); }
+
+// ---------------------------------------------------------------------------------------
+// Launchers (host functions; every one returns the launch error of its kernels)
+// ---------------------------------------------------------------------------------------
+cudaError_t launch_router_topk(const void* x, const void* wg, const float* bias, int T, int d, int n,
+                               int k, int dtype, int32_t* idx, float* w, float* logits,
+                               cudaStream_t s);
+cudaError_t launch_rmsnorm(const void* h, int T, int d, float eps, int dtype, void* x, cudaStream_t s);
+
+// Permutation: per-block counts live in `scratch` (2 * nblocks * n int32) when T*k > chunk.
+int permute_blocks(long long A);
+cudaError_t launch_permute(const int32_t* idx, int A, int n, int32_t* offsets, int32_t* perm,
+                           int32_t* inv_perm, int32_t* scratch, uint32_t* status, cudaStream_t s);
+
+// x_perm[p] = x[perm[p] / k]  (rows of `row_bytes` bytes)
+cudaError_t launch_gather_rows(const void* x, const int32_t* perm, int A, int k, size_t row_bytes,
+                               void* x_perm, cudaStream_t s);
+
+cudaError_t launch_combine(const void* y_perm, const int32_t* inv_perm, const float* w,
+                           const void* residual, int T, int d, int k, int dtype, void* y,
+                           cudaStream_t s);
+
+// fp32 / generic CUDA-core experts (x_perm already gathered).
+cudaError_t launch_up_simt(const void* x_perm, const int32_t* offsets, const void* w1, const void* w3,
+                           int A, int d, int f, int n, int dtype, void* h, cudaStream_t s);
+cudaError_t launch_down_simt(const void* h, const int32_t* offsets, const void* w2, int A, int d,
+                             int f, int n, int dtype, void* y_perm, cudaStream_t s);
+
+// bf16 tcgen05 experts: up = w1|w3 GEMM with SiLU(a)*b fused; down = w2 GEMM.
+cudaError_t launch_up_tc(const bf16* x_perm, const int32_t* offsets, const bf16* w1, const bf16* w3,
+                         int A, int d, int f, int n, bf16* h, uint32_t* status,
+                         unsigned long long wait_ns, cudaStream_t s);
+cudaError_t launch_down_tc(const bf16* h, const int32_t* offsets, const bf16* w2, int A, int d,
+                           int f, int n, bf16* y_perm, uint32_t* status, unsigned long long wait_ns,
+                           cudaStream_t s);
+
+int device_sm_count();
+
+}  // namespace moe

@@ -1,0 +1,252 @@
+// Grouping of the T*k token->expert assignments by expert, and the row gather that builds the
+// expert-ordered copy of x.
+//   Experts whose gate is 0 are not computed ("Mixtral 8x7B: 疎な専門家混合言語モデル",
+//   ja.news.hada.io, MoEレイヤーの計算方式); each expert receives a variable number of tokens
+//   and the outputs go back to the original token positions (same page, 実装と推論効率).
+//
+// Outputs: expert_offsets[n+1] (exclusive prefix sum of per-expert counts), perm[p] = the
+// assignment a = t*k + slot at position p, positions ordered by (expert, a), and
+// inv_perm[a] = p.  Stable and deterministic: no atomics decide any position.
+//
+// A block of 32 warps handles a chunk of kPermuteChunk assignments; warp w owns a contiguous
+// sub-chunk.  Ranks within a 32-wide round come from __match_any_sync + popc of the lanes
+// below; per-(warp, expert) counters in shared memory carry the rank across rounds.  One
+// block covers the whole problem when T*k <= kPermuteChunk (a single launch); otherwise a
+// count kernel, a scan kernel and a scatter kernel run over the chunks.
+#include "moe_internal.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kWarps = 32;
+
+struct ChunkBounds {
+  int begin, end;
+};
+
+__device__ __forceinline__ ChunkBounds warp_range(int chunk_begin, int chunk_end, int warp) {
+  const int len = chunk_end - chunk_begin;
+  int per = (len + kWarps - 1) / kWarps;
+  per = (per + 31) & ~31;
+  const int b = chunk_begin + warp * per;
+  const int e = min(chunk_end, b + per);
+  return {b, e};
+}
+
+// Reads the expert of assignment i (or -1 past the end / for a bad index, which is reported
+// when `status` is not null).
+__device__ __forceinline__ int load_expert(const int32_t* __restrict__ idx, int i, int end, int n,
+                                           uint32_t* status) {
+  if (i >= end) return -1;
+  const int e = __ldg(idx + i);
+  if (e < 0 || e >= n) {
+    if (status) atomicOr(status, kDevErrIndex);
+    return -1;
+  }
+  return e;
+}
+
+// cnt[w][e] <- number of assignments of warp w's range that go to expert e.
+__device__ void count_warp(const int32_t* __restrict__ idx, ChunkBounds r, int n, int lane,
+                           int* cnt_row, uint32_t* status) {
+  for (int base = r.begin; base < r.end; base += 32) {
+    const int e = load_expert(idx, base + lane, r.end, n, status);
+    const unsigned m = __match_any_sync(0xffffffffu, e);
+    if (e >= 0 && lane == __ffs(m) - 1) cnt_row[e] += __popc(m);
+    __syncwarp();
+  }
+}
+
+// Writes perm / inv_perm for warp w's range; run_row[e] holds the first position of the
+// warp's assignments to expert e and is advanced as rounds go by.
+__device__ void scatter_warp(const int32_t* __restrict__ idx, ChunkBounds r, int n, int lane,
+                             int* run_row, int32_t* __restrict__ perm,
+                             int32_t* __restrict__ inv_perm, uint32_t* status) {
+  const unsigned lt = (1u << lane) - 1u;
+  for (int base = r.begin; base < r.end; base += 32) {
+    const int i = base + lane;
+    const int e = load_expert(idx, i, r.end, n, status);
+    const unsigned m = __match_any_sync(0xffffffffu, e);
+    int pos = 0;
+    if (e >= 0) {
+      pos = run_row[e] + __popc(m & lt);
+      perm[pos] = i;
+      inv_perm[i] = pos;
+    }
+    __syncwarp();
+    if (e >= 0 && lane == __ffs(m) - 1) run_row[e] += __popc(m);
+    __syncwarp();
+  }
+}
+
+// Single block: count, scan, scatter.
+__global__ void __launch_bounds__(1024) permute_single_kernel(const int32_t* __restrict__ idx,
+                                                              int A, int n,
+                                                              int32_t* __restrict__ offsets,
+                                                              int32_t* __restrict__ perm,
+                                                              int32_t* __restrict__ inv_perm,
+                                                              uint32_t* status) {
+  __shared__ int cnt[kWarps][kMaxExperts + 1];
+  __shared__ int ebase[kMaxExperts + 1];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  cnt[warp][lane] = 0;
+  __syncwarp();
+  const ChunkBounds r = warp_range(0, A, warp);
+  count_warp(idx, r, n, lane, cnt[warp], status);
+  __syncthreads();
+  if (warp == 0) {
+    // lane = expert: exclusive prefix over warps, then over experts
+    int run = 0;
+    for (int w = 0; w < kWarps; ++w) {
+      const int c = cnt[w][lane];
+      cnt[w][lane] = run;
+      run += c;
+    }
+    int incl = run;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    const int excl = incl - run;
+    ebase[lane] = excl;
+    if (lane < n) offsets[lane] = excl;
+    if (lane == 0) offsets[n] = A;
+  }
+  __syncthreads();
+  if (lane < kMaxExperts) cnt[warp][lane] += ebase[lane];
+  __syncwarp();
+  scatter_warp(idx, r, n, lane, cnt[warp], perm, inv_perm, status);
+}
+
+// Multi-block, step 1: per-block counts -> block_cnt[b * n + e].
+__global__ void __launch_bounds__(1024) permute_count_kernel(const int32_t* __restrict__ idx, int A,
+                                                             int n, int32_t* __restrict__ block_cnt,
+                                                             uint32_t* status) {
+  __shared__ int cnt[kWarps][kMaxExperts + 1];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  cnt[warp][lane] = 0;
+  __syncwarp();
+  const int cb = blockIdx.x * kPermuteChunk, ce = min(A, cb + kPermuteChunk);
+  count_warp(idx, warp_range(cb, ce, warp), n, lane, cnt[warp], status);
+  __syncthreads();
+  if (warp == 0 && lane < n) {
+    int s = 0;
+    for (int w = 0; w < kWarps; ++w) s += cnt[w][lane];
+    block_cnt[blockIdx.x * n + lane] = s;
+  }
+}
+
+// Multi-block, step 2 (one warp): block_base[b * n + e] = offsets[e] + counts of blocks < b.
+__global__ void permute_scan_kernel(const int32_t* __restrict__ block_cnt, int nblocks, int A, int n,
+                                    int32_t* __restrict__ block_base,
+                                    int32_t* __restrict__ offsets) {
+  const int lane = threadIdx.x & 31;
+  int run = 0;
+  for (int b = 0; b < nblocks; ++b) {
+    const int c = lane < n ? block_cnt[b * n + lane] : 0;
+    if (lane < n) block_base[b * n + lane] = run;
+    run += c;
+  }
+  int incl = run;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  const int excl = incl - run;
+  if (lane < n) {
+    offsets[lane] = excl;
+    for (int b = 0; b < nblocks; ++b) block_base[b * n + lane] += excl;
+  }
+  if (lane == 0) offsets[n] = A;
+}
+
+// Multi-block, step 3: recount per warp, add the block base, scatter.
+__global__ void __launch_bounds__(1024) permute_scatter_kernel(const int32_t* __restrict__ idx,
+                                                               int A, int n,
+                                                               const int32_t* __restrict__ block_base,
+                                                               int32_t* __restrict__ perm,
+                                                               int32_t* __restrict__ inv_perm,
+                                                               uint32_t* status) {
+  __shared__ int cnt[kWarps][kMaxExperts + 1];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  cnt[warp][lane] = 0;
+  __syncwarp();
+  const int cb = blockIdx.x * kPermuteChunk, ce = min(A, cb + kPermuteChunk);
+  const ChunkBounds r = warp_range(cb, ce, warp);
+  // bad indices were already reported by the count kernel
+  count_warp(idx, r, n, lane, cnt[warp], nullptr);
+  __syncthreads();
+  if (warp == 0) {
+    int run = lane < n ? block_base[blockIdx.x * n + lane] : 0;
+    for (int w = 0; w < kWarps; ++w) {
+      const int c = cnt[w][lane];
+      cnt[w][lane] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  scatter_warp(idx, r, n, lane, cnt[warp], perm, inv_perm, nullptr);
+  (void)status;
+}
+
+// x_perm[p] = x[perm[p] / k], 16-byte vectors when the row allows it.
+__global__ void __launch_bounds__(256) gather_rows_vec_kernel(const uint4* __restrict__ x,
+                                                              const int32_t* __restrict__ perm,
+                                                              int A, int k, int row_vecs,
+                                                              uint4* __restrict__ x_perm) {
+  for (int p = blockIdx.x; p < A; p += gridDim.x) {
+    const int t = __ldg(perm + p) / k;
+    const uint4* src = x + (size_t)t * row_vecs;
+    uint4* dst = x_perm + (size_t)p * row_vecs;
+    for (int c = threadIdx.x; c < row_vecs; c += blockDim.x) dst[c] = __ldg(src + c);
+  }
+}
+
+__global__ void __launch_bounds__(256) gather_rows_byte_kernel(const uint8_t* __restrict__ x,
+                                                               const int32_t* __restrict__ perm,
+                                                               int A, int k, size_t row_bytes,
+                                                               uint8_t* __restrict__ x_perm) {
+  for (int p = blockIdx.x; p < A; p += gridDim.x) {
+    const int t = __ldg(perm + p) / k;
+    for (size_t c = threadIdx.x; c < row_bytes; c += blockDim.x)
+      x_perm[(size_t)p * row_bytes + c] = x[(size_t)t * row_bytes + c];
+  }
+}
+
+}  // namespace
+
+int permute_blocks(long long A) { return (int)((A + kPermuteChunk - 1) / kPermuteChunk); }
+
+cudaError_t launch_permute(const int32_t* idx, int A, int n, int32_t* offsets, int32_t* perm,
+                           int32_t* inv_perm, int32_t* scratch, uint32_t* status, cudaStream_t s) {
+  const int nb = permute_blocks(A);
+  if (nb <= 1) {
+    permute_single_kernel<<<1, 1024, 0, s>>>(idx, A, n, offsets, perm, inv_perm, status);
+    return cudaGetLastError();
+  }
+  int32_t* block_cnt = scratch;
+  int32_t* block_base = scratch + (size_t)nb * n;
+  permute_count_kernel<<<nb, 1024, 0, s>>>(idx, A, n, block_cnt, status);
+  permute_scan_kernel<<<1, 32, 0, s>>>(block_cnt, nb, A, n, block_base, offsets);
+  permute_scatter_kernel<<<nb, 1024, 0, s>>>(idx, A, n, block_base, perm, inv_perm, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_rows(const void* x, const int32_t* perm, int A, int k, size_t row_bytes,
+                               void* x_perm, cudaStream_t s) {
+  if (A == 0) return cudaSuccess;
+  const int cap = device_sm_count() * 8;
+  const int grid = A < cap ? A : cap;
+  if (row_bytes % 16 == 0 && ((uintptr_t)x % 16) == 0 && ((uintptr_t)x_perm % 16) == 0) {
+    gather_rows_vec_kernel<<<grid, 256, 0, s>>>((const uint4*)x, perm, A, k, (int)(row_bytes / 16),
+                                                (uint4*)x_perm);
+  } else {
+    gather_rows_byte_kernel<<<grid, 256, 0, s>>>((const uint8_t*)x, perm, A, k, row_bytes,
+                                                 (uint8_t*)x_perm);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace moe

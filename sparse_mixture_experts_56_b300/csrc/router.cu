@@ -1,0 +1,260 @@
+// Router and gate:  l = x · W_g (+ b);  G(x) = Softmax(TopK(l))
+//   "Mixtral of Experts" (xyznot.com summary), Método, eq. G;
+//   blog.csdn.net "《Mixtral of Experts》…", MOE数学公式 §2.1 (logits), §2.2 (TopK keeps the K
+//   largest logits, the rest become -inf), §2.3 (softmax over the TopK output: only the K
+//   kept experts get weight, and those weights sum to 1).
+// Also the row-wise RMSNorm used by stacked layers (not part of the pages' layer).
+//
+// One warp per token.  The token's row of x is read once (16-byte loads); W_g (d x n,
+// 64 KB for 4096 x 8 bf16) stays hot in L1/L2.  Products accumulate in fp32 per lane,
+// then a butterfly reduction gives every lane all n logits.  Lane 0 selects the top K
+// (ties -> lower index, descending order) and normalises exp(l - l_max) over them.
+#include "moe_internal.cuh"
+
+namespace moe {
+namespace {
+
+template <int NP>
+__device__ __forceinline__ void warp_allreduce(float (&acc)[NP]) {
+#pragma unroll
+  for (int e = 0; e < NP; ++e) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], o);
+  }
+}
+
+// Top-K selection and softmax over the kept logits; run by one lane.
+template <int NP>
+__device__ __forceinline__ void select_and_write(const float (&l)[NP], int n, int k,
+                                                 int32_t* idx_row, float* w_row) {
+  uint32_t taken = 0;
+  int sel[kMaxExperts];
+  float lmax = 0.f;
+  for (int s = 0; s < k; ++s) {
+    int best = -1;
+    float bv = 0.f;
+#pragma unroll
+    for (int e = 0; e < NP; ++e) {
+      if (e < n && !(taken >> e & 1u)) {
+        // strict '>' keeps the lower index on equal logits
+        if (best < 0 || l[e] > bv) {
+          best = e;
+          bv = l[e];
+        }
+      }
+    }
+    taken |= 1u << best;
+    sel[s] = best;
+    if (s == 0) lmax = bv;
+  }
+  float sum = 0.f;
+  float ex[kMaxExperts];
+  for (int s = 0; s < k; ++s) {
+    float v = 0.f;
+#pragma unroll
+    for (int e = 0; e < NP; ++e)
+      if (e == sel[s]) v = l[e];
+    ex[s] = expf(v - lmax);
+    sum += ex[s];
+  }
+  for (int s = 0; s < k; ++s) {
+    idx_row[s] = sel[s];
+    w_row[s] = ex[s] / sum;
+  }
+}
+
+// Generic path: any d, any n <= NP, fp32 or bf16 storage.
+template <typename T, int NP>
+__global__ void __launch_bounds__(256) router_generic_kernel(const T* __restrict__ x,
+                                                             const T* __restrict__ wg,
+                                                             const float* __restrict__ bias, int Tn,
+                                                             int d, int n, int k,
+                                                             int32_t* __restrict__ idx,
+                                                             float* __restrict__ w,
+                                                             float* __restrict__ logits) {
+  const int lane = threadIdx.x & 31;
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < Tn; t += warps) {
+    float acc[NP];
+#pragma unroll
+    for (int e = 0; e < NP; ++e) acc[e] = 0.f;
+    const T* xr = x + (size_t)t * d;
+    for (int i = lane; i < d; i += 32) {
+      const float xv = to_f32(xr[i]);
+      const T* wr = wg + (size_t)i * n;
+#pragma unroll
+      for (int e = 0; e < NP; ++e)
+        if (e < n) acc[e] = fmaf(xv, to_f32(wr[e]), acc[e]);
+    }
+    warp_allreduce<NP>(acc);
+    if (bias) {
+#pragma unroll
+      for (int e = 0; e < NP; ++e)
+        if (e < n) acc[e] += bias[e];
+    }
+    if (logits && lane < n) {
+      float v = 0.f;
+#pragma unroll
+      for (int e = 0; e < NP; ++e)
+        if (e == lane) v = acc[e];
+      logits[(size_t)t * n + lane] = v;
+    }
+    if (lane == 0) select_and_write<NP>(acc, n, k, idx + (size_t)t * k, w + (size_t)t * k);
+  }
+}
+
+// Fast path: bf16, n == 8, d % 256 == 0.  Each lane owns 8 consecutive elements of x per
+// 256-element slab: one 16-byte load of x and eight 16-byte loads of the matching W_g rows.
+__global__ void __launch_bounds__(256) router_bf16_n8_kernel(const bf16* __restrict__ x,
+                                                             const bf16* __restrict__ wg,
+                                                             const float* __restrict__ bias,
+                                                             int Tn, int d, int k,
+                                                             int32_t* __restrict__ idx,
+                                                             float* __restrict__ w,
+                                                             float* __restrict__ logits) {
+  const int lane = threadIdx.x & 31;
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < Tn; t += warps) {
+    float acc[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+    const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)t * d);
+    for (int i0 = lane * 8; i0 < d; i0 += 256) {
+      const uint4 xv = __ldg(xr + (i0 >> 3));
+      const __nv_bfloat162* xp = reinterpret_cast<const __nv_bfloat162*>(&xv);
+      const uint4* wr = reinterpret_cast<const uint4*>(wg + (size_t)i0 * 8);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float2 xf = __bfloat1622float2(xp[j >> 1]);
+        const float xs = (j & 1) ? xf.y : xf.x;
+        const uint4 wv = __ldg(wr + j);
+        const __nv_bfloat162* wp = reinterpret_cast<const __nv_bfloat162*>(&wv);
+#pragma unroll
+        for (int e2 = 0; e2 < 4; ++e2) {
+          const float2 wf = __bfloat1622float2(wp[e2]);
+          acc[2 * e2] = fmaf(xs, wf.x, acc[2 * e2]);
+          acc[2 * e2 + 1] = fmaf(xs, wf.y, acc[2 * e2 + 1]);
+        }
+      }
+    }
+    warp_allreduce<8>(acc);
+    if (bias) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] += bias[e];
+    }
+    if (logits && lane < 8) {
+      float v = 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        if (e == lane) v = acc[e];
+      logits[(size_t)t * 8 + lane] = v;
+    }
+    if (lane == 0) select_and_write<8>(acc, 8, k, idx + (size_t)t * k, w + (size_t)t * k);
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) rmsnorm_kernel(const T* __restrict__ h, int Tn, int d,
+                                                      float eps, T* __restrict__ x) {
+  const int lane = threadIdx.x & 31;
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < Tn; t += warps) {
+    const T* hr = h + (size_t)t * d;
+    float ss = 0.f;
+    for (int i = lane; i < d; i += 32) {
+      const float v = to_f32(hr[i]);
+      ss = fmaf(v, v, ss);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float inv = 1.0f / sqrtf(ss / (float)d + eps);
+    T* xr = x + (size_t)t * d;
+    for (int i = lane; i < d; i += 32) xr[i] = from_f32<T>(to_f32(hr[i]) * inv);
+  }
+}
+
+// bf16 rows with d % 256 == 0: 16-byte loads, the row kept in registers between passes.
+__global__ void __launch_bounds__(256) rmsnorm_bf16_vec_kernel(const bf16* __restrict__ h, int Tn,
+                                                               int d, float eps,
+                                                               bf16* __restrict__ x) {
+  const int lane = threadIdx.x & 31;
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < Tn; t += warps) {
+    const uint4* hr = reinterpret_cast<const uint4*>(h + (size_t)t * d);
+    uint4* xr = reinterpret_cast<uint4*>(x + (size_t)t * d);
+    float ss = 0.f;
+    for (int c = lane; c < (d >> 3); c += 32) {
+      const uint4 v = __ldg(hr + c);
+      const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 f = __bfloat1622float2(p[j]);
+        ss = fmaf(f.x, f.x, ss);
+        ss = fmaf(f.y, f.y, ss);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float inv = 1.0f / sqrtf(ss / (float)d + eps);
+    for (int c = lane; c < (d >> 3); c += 32) {
+      const uint4 v = __ldg(hr + c);
+      const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&v);
+      uint4 o;
+      __nv_bfloat162* q = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 f = __bfloat1622float2(p[j]);
+        q[j] = __floats2bfloat162_rn(f.x * inv, f.y * inv);
+      }
+      xr[c] = o;
+    }
+  }
+}
+
+int grid_for_warps(long long warps_needed) {
+  const long long blocks = (warps_needed + 7) / 8;
+  const long long cap = (long long)device_sm_count() * 16;
+  return (int)(blocks < cap ? (blocks > 0 ? blocks : 1) : cap);
+}
+
+}  // namespace
+
+cudaError_t launch_router_topk(const void* x, const void* wg, const float* bias, int T, int d, int n,
+                               int k, int dtype, int32_t* idx, float* w, float* logits,
+                               cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  const int grid = grid_for_warps(T);
+  if (dtype == MOE_BF16 && n == 8 && d % 256 == 0) {
+    router_bf16_n8_kernel<<<grid, 256, 0, s>>>((const bf16*)x, (const bf16*)wg, bias, T, d, k, idx,
+                                                w, logits);
+  } else if (dtype == MOE_BF16) {
+    if (n <= 8)
+      router_generic_kernel<bf16, 8><<<grid, 256, 0, s>>>((const bf16*)x, (const bf16*)wg, bias, T,
+                                                          d, n, k, idx, w, logits);
+    else
+      router_generic_kernel<bf16, 32><<<grid, 256, 0, s>>>((const bf16*)x, (const bf16*)wg, bias, T,
+                                                           d, n, k, idx, w, logits);
+  } else {
+    if (n <= 8)
+      router_generic_kernel<float, 8><<<grid, 256, 0, s>>>((const float*)x, (const float*)wg, bias,
+                                                           T, d, n, k, idx, w, logits);
+    else
+      router_generic_kernel<float, 32><<<grid, 256, 0, s>>>((const float*)x, (const float*)wg, bias,
+                                                            T, d, n, k, idx, w, logits);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rmsnorm(const void* h, int T, int d, float eps, int dtype, void* x, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  const int grid = grid_for_warps(T);
+  if (dtype == MOE_BF16 && d % 256 == 0)
+    rmsnorm_bf16_vec_kernel<<<grid, 256, 0, s>>>((const bf16*)h, T, d, eps, (bf16*)x);
+  else if (dtype == MOE_BF16)
+    rmsnorm_kernel<bf16><<<grid, 256, 0, s>>>((const bf16*)h, T, d, eps, (bf16*)x);
+  else
+    rmsnorm_kernel<float><<<grid, 256, 0, s>>>((const float*)h, T, d, eps, (float*)x);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -42,8 +42,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=200)
-    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--workload", type=int, default=2, choices=sorted(workloads.WORKLOADS))
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--seed", type=int, default=0)
@@ -94,61 +94,87 @@ REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_c
 
 
 class ClockSampler:
+    """SM clock and clock-event reasons sampled every few ms during the timed region, through
+    NVML when the Python bindings are present, else through `nvidia-smi -lms`."""
+
     def __init__(self, torch_dev):
+        import torch
         self.samples = []
-        self.ok = False
+        self.mode = None
+        self.max_mhz = None
         self._stop = threading.Event()
         self._thr = None
+        self._proc = None
+        uuid = str(torch.cuda.get_device_properties(torch_dev).uuid)
+        self.uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
         try:
             import pynvml
-            import torch
             pynvml.nvmlInit()
-            uuid = str(torch.cuda.get_device_properties(torch_dev).uuid)
-            if not uuid.startswith("GPU-"):
-                uuid = "GPU-" + uuid
-            self.h = pynvml.nvmlDeviceGetHandleByUUID(uuid)
+            self.h = pynvml.nvmlDeviceGetHandleByUUID(self.uuid)
             self.nv = pynvml
             self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
-            self.ok = True
-        except Exception as exc:  # no NVML: clocks are reported as unknown
-            self.err = repr(exc)
+            self.mode = "nvml"
+        except Exception:
+            import shutil
+            if shutil.which("nvidia-smi"):
+                self.mode = "nvidia-smi"
 
-    def _reasons(self):
+    def _run_nvml(self):
         nv = self.nv
         fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
             getattr(nv, "nvmlDeviceGetCurrentClocksThrottleReasons")
-        return int(fn(self.h))
-
-    def _run(self):
         while not self._stop.is_set():
             try:
-                mhz = self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM)
-                self.samples.append((mhz, self._reasons()))
+                self.samples.append((nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM), int(fn(self.h))))
             except Exception:
                 pass
             time.sleep(0.002)
 
+    def _run_smi(self):
+        for line in self._proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            try:
+                mhz, mx, reasons = float(parts[0]), float(parts[1]), int(parts[2], 16)
+            except (ValueError, IndexError):
+                continue
+            self.max_mhz = mx
+            self.samples.append((mhz, reasons))
+
     def start(self):
-        if self.ok:
-            self._thr = threading.Thread(target=self._run, daemon=True)
+        if self.mode == "nvml":
+            self._thr = threading.Thread(target=self._run_nvml, daemon=True)
+        elif self.mode == "nvidia-smi":
+            import subprocess
+            self._proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.uuid,
+                 "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.active",
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._thr = threading.Thread(target=self._run_smi, daemon=True)
+            time.sleep(0.3)   # let the first samples arrive
+        if self._thr:
             self._thr.start()
 
     def stop(self):
+        self._stop.set()
+        if self._proc:
+            self._proc.terminate()
+            self._proc.wait()
         if self._thr:
-            self._stop.set()
-            self._thr.join()
+            self._thr.join(timeout=5)
 
     def summary(self):
-        if not self.ok or not self.samples:
-            return {"sm_mhz": None, "sm_max_mhz": getattr(self, "max_mhz", None), "reasons": [],
-                    "samples": 0, "note": getattr(self, "err", "no samples")}
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0,
+                    "source": self.mode}
         mhz = [s[0] for s in self.samples]
         bits = 0
         for _, r in self.samples:
             bits |= r
         names = [n for b, n in REASONS.items() if bits & b and n != "gpu_idle"]
-        return {"sm_mhz": float(statistics.median(mhz)), "sm_max_mhz": float(self.max_mhz),
-                "reasons": names, "samples": len(self.samples)}
+        return {"sm_mhz": float(statistics.median(mhz)),
+                "sm_max_mhz": float(self.max_mhz) if self.max_mhz else None,
+                "reasons": names, "samples": len(self.samples), "source": self.mode}
 
 
 def peaks():

@@ -1,0 +1,115 @@
+"""GPU parity at the full Mixtral-shaped sizes (d=4096, f=14336, 8 experts, top-2), in the
+launch configuration the benchmark times.
+
+Routing is compared on every token: expert indices bit-exact except near ties (2nd/3rd
+logit gap < 1e-4, counted), offsets bit-exact against the oracle's grouping of the GPU's
+selection and, where no near tie exists, against the oracle's own.  Outputs are compared
+on a sample of tokens (the oracle evaluates them one expert group at a time in fp64)."""
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+from tests.helpers import TOL, assert_close_rel, check_selection, gate_weights_for, to_device, to_numpy_f32
+
+torch = pytest.importorskip("torch")
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def moe():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import sparse_mixture_experts_56_b300 as m
+    m._native.lib()
+    return m
+
+
+def _sample(T, gi, n, rng, per_expert=4, extra=48):
+    """A token sample that touches every expert: a few tokens per expert, the first and
+    last token, and random ones."""
+    picks = {0, T - 1}
+    for e in range(n):
+        rows = np.flatnonzero((gi == e).any(axis=1))
+        if rows.size:
+            picks.update(rng.choice(rows, size=min(per_expert, rows.size), replace=False).tolist())
+    picks.update(rng.choice(T, size=min(extra, T), replace=False).tolist())
+    return np.array(sorted(picks))
+
+
+@pytest.mark.parametrize("wid", [2, 3, 4])
+def test_full_size_layer(moe, wid):
+    w = workloads.workload(wid)
+    inp = workloads.make_inputs(w)
+    g = {k: to_device(inp[k], w, DEV) for k in ("x", "wg", "w1", "w3", "w2")}
+    bias = torch.from_numpy(inp["bias"]).to(DEV) if inp["bias"] is not None else None
+    ws = moe.workspace(w.T, w.d, w.f, w.n, w.k, torch.bfloat16, DEV)
+    idx = torch.empty((w.T, w.k), dtype=torch.int32, device=DEV)
+    off = torch.empty(w.n + 1, dtype=torch.int32, device=DEV)
+    y = moe.moe_layer_forward(g["x"], g["wg"], g["w1"], g["w3"], g["w2"], w.k, ws, logit_bias=bias,
+                              topk_idx_out=idx, expert_offsets_out=off)
+    assert moe.moe_check_device_error(ws) == 0
+    yg = to_numpy_f32(y)
+    del g
+    torch.cuda.empty_cache()
+
+    xf = workloads.as_f32(inp["x"], w)
+    wgf = workloads.as_f32(inp["wg"], w)
+    lref = oracle.router_logits(xf, wgf, inp["bias"])
+    gi = idx.cpu().numpy().astype(np.int64)
+    n_set_ties, n_order_ties = check_selection(gi, lref, w.k)
+    goff = off.cpu().numpy()
+    assert np.array_equal(goff, oracle.group_by_expert(gi, w.n)[0])
+    roff = oracle.group_by_expert(oracle.topk_select(lref, w.k), w.n)[0]
+    if n_set_ties == 0:
+        assert np.array_equal(goff, roff)
+    else:
+        assert np.abs(np.diff(goff) - np.diff(roff)).sum() <= 2 * n_set_ties
+    print(f"\n{w.name}: near ties (set) {n_set_ties}, (order) {n_order_ties}, counts {np.diff(goff).tolist()}")
+
+    rng = np.random.default_rng(wid)
+    tok = _sample(w.T, gi, w.n, rng)
+    f = {k: workloads.as_f32(inp[k], w) for k in ("w1", "w3", "w2")}
+    yref = oracle.moe_layer(xf, wgf, f["w1"], f["w3"], f["w2"], w.k, inp["bias"], idx=gi,
+                            w=gate_weights_for(gi, lref), tokens=tok)
+    rel = assert_close_rel(yg[tok], yref, TOL["bf16"])
+    print(f"{w.name}: {tok.size} sampled tokens, max|err|/max|ref| = {rel:.3e}")
+
+
+def test_full_size_stack_of_four(moe):
+    """Workload 5: h <- h + MoE_l(RMSNorm(h)) for 4 layers, T=8192; the oracle follows a
+    token sample through all 4 layers in fp64 from the same h_0 (each token's trajectory is
+    independent of the others)."""
+    w = workloads.workload(5)
+    h0 = workloads.make_inputs(w, tensors=("x",))["x"]
+    h = to_device(h0, w, DEV)
+    ws = moe.workspace(w.T, w.d, w.f, w.n, w.k, torch.bfloat16, DEV)
+    xn = torch.empty_like(h)
+    rng = np.random.default_rng(5)
+    tok = np.sort(rng.choice(w.T, size=48, replace=False))
+    href = workloads.as_f32(h0, w)[tok].astype(np.float64)
+    excluded = np.zeros(tok.size, dtype=bool)
+    hist = []
+    for layer in range(w.layers):
+        inp = workloads.make_inputs(w, layer=layer, tensors=("wg", "w1", "w3", "w2"))
+        g = {k: to_device(inp[k], w, DEV) for k in ("wg", "w1", "w3", "w2")}
+        moe.moe_rmsnorm(h, w.rms_eps, x=xn)
+        off = torch.empty(w.n + 1, dtype=torch.int32, device=DEV)
+        h = moe.moe_layer_forward(xn, g["wg"], g["w1"], g["w3"], g["w2"], w.k, ws, residual=h,
+                                  y=torch.empty_like(h), expert_offsets_out=off)
+        assert moe.moe_check_device_error(ws) == 0
+        hist.append(np.diff(off.cpu().numpy()).tolist())
+        del g
+        f = {k: workloads.as_f32(inp[k], w) for k in ("wg", "w1", "w3", "w2")}
+        xr = oracle.rmsnorm(href, w.rms_eps)
+        lref = oracle.router_logits(xr, f["wg"])
+        sigma = 2.0 ** -9 / np.sqrt(3) * np.sqrt(((xr[:, :, None] * f["wg"][None]) ** 2).sum(1)).max(1)
+        srt = np.sort(lref, 1)[:, ::-1]
+        excluded |= (srt[:, 1] - srt[:, 2]) < 5 * sigma * (layer + 1)
+        href = oracle.stacked_layer(href, f["wg"], f["w1"], f["w3"], f["w2"], w.k, w.rms_eps)
+        keep = ~excluded
+        assert keep.sum() >= 0.8 * tok.size
+        rel = assert_close_rel(to_numpy_f32(h)[tok][keep], href[keep], TOL["bf16"], f"h after layer {layer}")
+        print(f"\nlayer {layer}: {keep.sum()}/{tok.size} tokens compared, rel err {rel:.3e}, counts {hist[-1]}")
+    assert all(sum(c) == w.T * w.k for c in hist)

@@ -139,14 +139,18 @@ def test_stacked_layers_small(moe):
         assert moe.moe_check_device_error(ws) == 0
         xr = oracle.rmsnorm(href)
         lref = oracle.router_logits(xr, f["wg"])
-        # bf16 storage of the normalised rows and of h moves the logits by ~1e-3; tokens
-        # whose 2nd/3rd gap is inside that band may legitimately route differently
-        band = 8 * 2.0 ** -9 * np.sqrt(((xr[:, :, None] * f["wg"][None]) ** 2).sum(1)).max(1) * (layer + 1)
+        # The GPU stores the normalised rows and h in bf16 (relative rounding error uniform
+        # in +-2^-9, std 2^-9/sqrt(3)), which moves logit e by a random amount of std
+        # sigma_e = 2^-9/sqrt(3) * sqrt(sum_i (x_i W_ie)^2), compounding over layers.  Tokens
+        # whose 2nd/3rd gap is within ~5 sigma of a tie may legitimately route differently;
+        # they are excluded from the comparison (and counted by the assert below).
+        sigma = 2.0 ** -9 / np.sqrt(3) * np.sqrt(((xr[:, :, None] * f["wg"][None]) ** 2).sum(1)).max(1)
+        band = 5 * sigma * (layer + 1)
         srt = np.sort(lref, 1)[:, ::-1]
         excluded |= (srt[:, 1] - srt[:, 2]) < band
         href = oracle.stacked_layer(href, f["wg"], f["w1"], f["w3"], f["w2"], w.k)
         keep = ~excluded
-        assert keep.sum() >= 0.95 * w.T
+        assert keep.sum() >= 0.85 * w.T, f"{(~keep).sum()} of {w.T} tokens excluded"
         assert_close_rel(to_numpy_f32(h)[keep], href[keep], TOL["bf16"], f"h after layer {layer}")
 
 

@@ -116,6 +116,27 @@ moe_status moe_permute(const int32_t* topk_idx, int T, int k, int n, int32_t* ex
                        int32_t* perm, int32_t* inv_perm, void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * moe_permute without a workspace.  The pages have no counterpart to this entry point; it
+ * serves callers that cannot allocate device memory at all and have no workspace to hand
+ * over — for example code that runs while a stream is being captured into a CUDA graph, or
+ * inside a host runtime's enqueue callback, where cudaMalloc is not allowed.  Same inputs,
+ * outputs and results as moe_permute.  Its scratch (a status word and the per-block counts)
+ * is a fixed 33,024-byte array inside libmoe.so, which every GPU that loads the library
+ * keeps until the process exits.
+ *   - T*k must be at most 4,194,304; larger sizes return MOE_ERR_UNSUPPORTED.
+ *   - The first call on a device looks up the array's device address, with that device
+ *     current; make that first call before any stream capture.
+ *   - All calls share the one array and it keeps the last call's contents (each call
+ *     clears the part that must start at zero).  Calls that may overlap on the GPU (for
+ *     instance on two streams with no ordering between them) race: results are undefined.
+ *   - Expert indices outside [0, n) are skipped and leave the outputs undefined; nothing
+ *     reports them here (moe_permute reports them through its workspace).
+ */
+moe_status moe_permute_noalloc(const int32_t* topk_idx, int T, int k, int n,
+                               int32_t* expert_offsets, int32_t* perm, int32_t* inv_perm,
+                               void* stream);
+
+/*
  * The experts: for every expert e with rows p in [offsets[e], offsets[e+1]) and token
  * t = perm[p] / k,   y_perm[p] = w2_e · (SiLU(w1_e · x_t) ⊙ (w3_e · x_t))
  * ("Mixtral of Experts", Método: SwiGLU experts; ja.news.hada.io MoEレイヤーの計算方式:

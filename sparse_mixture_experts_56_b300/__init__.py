@@ -18,7 +18,7 @@ from ._native import MOE_BF16, MOE_F32, MoEError, check
 
 __all__ = [
     "MOE_F32", "MOE_BF16", "MoEError", "dtype_code", "moe_workspace_size", "workspace",
-    "moe_router_topk", "moe_permute", "moe_grouped_swiglu", "moe_expert_up", "moe_expert_down",
+    "moe_router_topk", "moe_permute", "moe_permute_noalloc", "moe_grouped_swiglu", "moe_expert_up", "moe_expert_down",
     "moe_combine", "moe_rmsnorm",
     "moe_layer_forward", "moe_check_device_error", "moe_set_wait_limit_ns", "moe_version",
     "library_path",
@@ -115,6 +115,17 @@ def moe_permute(topk_idx: torch.Tensor, n: int, ws: torch.Tensor, *,
     st = _native.lib().moe_permute(_ptr(topk_idx), T, k, n, _ptr(expert_offsets), _ptr(perm),
                                    _ptr(inv_perm), _ptr(ws), ws.numel(), _stream(stream))
     check("moe_permute", st)
+    return expert_offsets, perm, inv_perm
+
+
+def moe_permute_noalloc(topk_idx: torch.Tensor, n: int, *, expert_offsets: torch.Tensor,
+                        perm: torch.Tensor, inv_perm: torch.Tensor, stream=None):
+    """moe_permute for callers that cannot allocate: no workspace, and every result buffer
+    must be passed in (this wrapper allocates nothing either)."""
+    T, k = topk_idx.shape
+    st = _native.lib().moe_permute_noalloc(_ptr(topk_idx), T, k, n, _ptr(expert_offsets),
+                                           _ptr(perm), _ptr(inv_perm), _stream(stream))
+    check("moe_permute_noalloc", st)
     return expert_offsets, perm, inv_perm
 
 

@@ -30,6 +30,7 @@ SIGNATURES = {
     "moe_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "moe_router_topk": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
     "moe_permute": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _SZ, _P]),
+    "moe_permute_noalloc": (_I, [_P, _I, _I, _I, _P, _P, _P, _P]),
     "moe_grouped_swiglu": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P]),
     "moe_expert_up": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P]),
     "moe_expert_down": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P]),

@@ -13,6 +13,8 @@
 // below; per-(warp, expert) counters in shared memory carry the rank across rounds.  One
 // block covers the whole problem when T*k <= kPermuteChunk (a single launch); otherwise a
 // count kernel, a scan kernel and a scatter kernel run over the chunks.
+#include <mutex>
+
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -249,4 +251,66 @@ cudaError_t launch_gather_rows(const void* x, const int32_t* perm, int A, int k,
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------------------
+// Allocation-free permutation: the same launches as launch_permute, with the per-block
+// counts and the status word in a fixed array of this library instead of a workspace.
+// ---------------------------------------------------------------------------------------
+namespace {
+
+constexpr int kNoAllocMaxBlocks = 128;  // T*k up to 128 * 32768 = 4,194,304 assignments
+constexpr int kNoAllocStatusWords = 64;  // the status word, padded to 256 bytes
+constexpr int kNoAllocWords = kNoAllocStatusWords + 2 * kNoAllocMaxBlocks * kMaxExperts;
+
+// Shared by every call on a device; holds the last call's contents.
+static __device__ __align__(256) int32_t g_noalloc_scratch[kNoAllocWords];
+
+struct NoAllocSlot {
+  int32_t* ptr = nullptr;
+  cudaError_t err = cudaSuccess;
+  bool looked_up = false;
+};
+std::mutex g_noalloc_mu;
+NoAllocSlot g_noalloc_slot[64];
+
+// Device address of the array on the current device; looked up once per device (the
+// name is only a host-side stand-in and must never be handed to a kernel itself).
+cudaError_t noalloc_scratch(int32_t** out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  NoAllocSlot& slot = g_noalloc_slot[dev];
+  if (!slot.looked_up) {
+    void* p = nullptr;
+    slot.err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    slot.ptr = static_cast<int32_t*>(p);
+    slot.looked_up = true;
+  }
+  *out = slot.ptr;
+  return slot.err;
+}
+
+}  // namespace
+
 }  // namespace moe
+
+extern "C" moe_status moe_permute_noalloc(const int32_t* topk_idx, int T, int k, int n,
+                                          int32_t* expert_offsets, int32_t* perm,
+                                          int32_t* inv_perm, void* stream) {
+  using namespace moe;
+  if (T < 0 || n < 1 || n > kMaxExperts || k < 1 || k > n) return MOE_ERR_INVALID_ARG;
+  const long long A = (long long)T * k;
+  if (A >= (1ll << 31)) return MOE_ERR_INVALID_ARG;
+  if (!expert_offsets || (A > 0 && (!topk_idx || !perm || !inv_perm))) return MOE_ERR_INVALID_ARG;
+  if (permute_blocks(A) > kNoAllocMaxBlocks) return MOE_ERR_UNSUPPORTED;
+  int32_t* scratch = nullptr;
+  if (noalloc_scratch(&scratch) != cudaSuccess || !scratch) return MOE_ERR_CUDA;
+  cudaStream_t s = (cudaStream_t)stream;
+  uint32_t* status = reinterpret_cast<uint32_t*>(scratch);
+  // the status word must start at zero; the per-block counts are written before being read
+  if (cudaMemsetAsync(status, 0, sizeof(uint32_t), s) != cudaSuccess) return MOE_ERR_CUDA;
+  const cudaError_t e = launch_permute(topk_idx, (int)A, n, expert_offsets, perm, inv_perm,
+                                       scratch + kNoAllocStatusWords, status, s);
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}

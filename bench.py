@@ -406,7 +406,7 @@ def ours_arm(args, w, dist):
 
     # roofline of the dominant kernel: the w1|w3 up-projection with SwiGLU (moe_expert_up:
     # row gather + grouped tcgen05 GEMM), per launch
-    up_bytes = touched * 2 * f * d * esz + A * d * esz * 2 + A * f * esz   # weights + x read/gathered + h
+    up_bytes = touched * 2 * f * d * esz + A * d * esz + A * f * esz   # w1, w3 of touched experts + x rows + h
     up_flops = 2.0 * A * d * 2 * f
     pk, pk_kind = peaks()
     hbm_peak = float(pk.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))

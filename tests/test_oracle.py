@@ -226,11 +226,49 @@ def check_locality_metric(o):
     assert abs(r - 1 / 8) < 0.005          # the random-assignment rate of 12.5% for n = 8
 
 
+def _pairs_bruteforce(idx, seq_len):
+    """Plain loops over token pairs with Python sets (no NumPy): the routing-statistics
+    definitions written out directly."""
+    rows = [list(map(int, r)) for r in idx]
+    pairs = same_first = same_any = 0
+    for t in range(len(rows) - 1):
+        if seq_len > 0 and (t + 1) % seq_len == 0:
+            continue                      # t+1 starts a new sequence
+        pairs += 1
+        same_first += rows[t][0] == rows[t + 1][0]
+        same_any += len(set(rows[t]) & set(rows[t + 1])) > 0
+    return pairs, same_first, same_any
+
+
+def check_routing_statistics(o):
+    hand = np.array([[0, 1], [0, 2], [1, 0], [1, 3], [1, 0]])
+    c, p, f1, fa = o.routing_statistics(hand, 4)
+    assert c.tolist() == [4, 4, 1, 1] and (p, f1, fa) == (4, 3, 4)
+    c, p, f1, fa = o.routing_statistics(hand, 4, seq_len=2)   # pairs (0,1) and (2,3) only
+    assert (p, f1, fa) == (2, 2, 2)
+    assert o.routing_statistics(hand[:1], 4)[1:] == (0, 0, 0)
+    rng = np.random.default_rng(62)
+    for n, k, T, seq in [(8, 2, 300, 0), (8, 2, 301, 37), (5, 3, 64, 8), (4, 1, 50, 7), (32, 4, 90, 1)]:
+        idx = np.argsort(rng.random((T, n)), axis=1)[:, :k]
+        c, p, f1, fa = o.routing_statistics(idx, n, seq_len=seq)
+        assert (p, f1, fa) == _pairs_bruteforce(idx, seq)
+        assert c.tolist() == [int(np.sum(idx == e)) for e in range(n)] and c.sum() == T * k
+        if k == 1:
+            assert f1 == fa
+    # random routing: first choice repeats with probability 1/n, and two independent
+    # K-subsets of n share an expert with probability 1 - C(n-K, K) / C(n, K)
+    for n, k in [(8, 2), (8, 1), (6, 3)]:
+        idx = np.argsort(rng.random((200_000, n)), axis=1)[:, :k]
+        _, p, f1, fa = o.routing_statistics(idx, n)
+        assert abs(f1 / p - 1 / n) < 0.005
+        assert abs(fa / p - (1 - math.comb(n - k, k) / math.comb(n, k))) < 0.005
+
+
 CHECKS = [check_worked_example, check_gate_invariants, check_topk_bruteforce,
           check_softmax_order_equivalence, check_single_expert_is_plain_ffn,
           check_k_equals_n_is_dense_softmax_mixture, check_sparse_equals_dense, check_grouping,
           check_silu, check_bias_enters_before_topk, check_rmsnorm, check_param_counts,
-          check_locality_metric]
+          check_locality_metric, check_routing_statistics]
 
 
 @pytest.mark.parametrize("check", CHECKS, ids=lambda c: c.__name__[6:])
@@ -303,6 +341,21 @@ def _mut_rms_no_sqrt(h, eps=1e-5):
     return h / (np.mean(h * h, axis=-1, keepdims=True) + eps)
 
 
+_ORIG_STATS = moe_oracle.routing_statistics
+
+
+def _mut_stats_cross_sequences(idx, n, seq_len=0):
+    return _ORIG_STATS(idx, n, 0)
+
+
+def _mut_stats_slotwise_any(idx, n, seq_len=0):
+    c, p, f1, _ = _ORIG_STATS(idx, n, seq_len)
+    e = np.asarray(idx)
+    t = np.arange(1, e.shape[0])
+    inside = np.ones(t.size, bool) if seq_len <= 0 else (t % seq_len) != 0
+    return c, p, f1, int(np.count_nonzero((e[:-1] == e[1:]).any(axis=1)[inside]))
+
+
 MUTATIONS = {
     "silu->sigmoid": ("silu", _mut_sigmoid_for_silu),
     "swap w1/w3": ("expert_swiglu", _mut_swap_w1_w3),
@@ -314,6 +367,8 @@ MUTATIONS = {
     "bias ignored": ("router_logits", _mut_bias_after_topk),
     "softmax sign flip": ("masked_softmax", _mut_softmax_sign),
     "rmsnorm without sqrt": ("rmsnorm", _mut_rms_no_sqrt),
+    "pairs cross sequences": ("routing_statistics", _mut_stats_cross_sequences),
+    "either-choice slot by slot": ("routing_statistics", _mut_stats_slotwise_any),
 }
 
 

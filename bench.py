@@ -437,6 +437,9 @@ def ours_arm(args, w, dist):
             "roofline": roof, "gpu_launches": launches_per_step * args.steps,
             "clocks": sampler.summary(), "expert_counts": counts.tolist()}
 
+    line["routing_stats"] = routing_stats_report(moe, w, step, layer, layers, x, xn, hs, idx, off,
+                                                 stream)
+
     if not args.no_e2e:
         # end to end through the public call with host buffers: pinned H2D of x, the layer,
         # D2H of y, every step
@@ -490,6 +493,59 @@ def ours_arm(args, w, dist):
         line["cpu_baseline"] = run_cpu_baseline(w, xf, lf, bias_h)
     if dist.rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def routing_stats_report(moe, w, step, layer, layers, x, xn, hs, idx, off, stream):
+    """Per-layer expert load and consecutive-token repetition (moe_routing_stats) of one more
+    step, outside the timed region, plus the kernel's own time per launch.  Consecutive
+    tokens of the decode batch belong to different sequences (no pairs); the other
+    workloads are read as sequences of up to 4096 tokens."""
+    import math
+    import torch
+    T, n, k = w.T, w.n, w.k
+    seq_len = 1 if w.wid == 2 else min(T, 4096)
+    counts = torch.empty((w.layers, n), dtype=torch.int64, device=x.device)
+    pairs = torch.empty((w.layers, 3), dtype=torch.int64, device=x.device)
+    hist = torch.empty((w.layers, n + 1), dtype=torch.int32, device=x.device)
+    h_in = x
+    for li, L in enumerate(layers):
+        if w.layers == 1:
+            layer(x, L, hs[0], None)
+        else:
+            moe.moe_rmsnorm(h_in, w.rms_eps, x=xn)
+            layer(xn, L, hs[li % 2], h_in)
+            h_in = hs[li % 2]
+        moe.moe_routing_stats(idx, n, seq_len, expert_counts=counts[li], pair_counts=pairs[li])
+        hist[li].copy_(off)
+    # the kernel is far shorter than a Python call: time a CUDA graph of `reps` launches so
+    # that the host does not set the pace
+    reps = 200
+    graph = torch.cuda.CUDAGraph()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(graph):
+        for _ in range(reps):
+            moe.moe_routing_stats(idx, n, seq_len, expert_counts=counts[-1], pair_counts=pairs[-1])
+    graph.replay()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / reps
+    del graph
+    c, pr, hs_np = counts.cpu().numpy(), pairs.cpu().numpy(), hist.cpu().numpy()
+    per_layer = []
+    for li in range(w.layers):
+        if c[li].tolist() != np.diff(hs_np[li]).tolist():
+            raise SystemExit("routing statistics disagree with the grouping offsets")
+        p = int(pr[li, 0])
+        per_layer.append({"expert_counts": c[li].tolist(), "pairs": p,
+                          "first_choice_rate": pr[li, 1] / p if p else None,
+                          "shared_expert_rate": pr[li, 2] / p if p else None})
+    return {"seq_len": seq_len, "per_layer": per_layer,
+            "random_first_choice_rate": 1.0 / n,
+            "random_shared_expert_rate": 1.0 - math.comb(n - k, k) / math.comb(n, k),
+            "kernel_us_per_launch": us, "bytes_read_per_launch": T * k * 4}
 
 
 def main():

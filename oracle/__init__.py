@@ -13,4 +13,5 @@ from .moe import (  # noqa: F401
     router_logits, topk_select, topk_mask, masked_softmax, gate, gate_softmax_then_topk,
     silu, expert_swiglu, group_by_expert, moe_layer, moe_layer_dense, rmsnorm,
     stacked_layer, near_tie_tokens, param_counts, consecutive_same_expert_rate,
+    routing_statistics,
 )

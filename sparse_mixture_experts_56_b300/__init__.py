@@ -19,7 +19,7 @@ from ._native import MOE_BF16, MOE_F32, MoEError, check
 __all__ = [
     "MOE_F32", "MOE_BF16", "MoEError", "dtype_code", "moe_workspace_size", "workspace",
     "moe_router_topk", "moe_permute", "moe_permute_noalloc", "moe_grouped_swiglu", "moe_expert_up", "moe_expert_down",
-    "moe_combine", "moe_rmsnorm",
+    "moe_combine", "moe_rmsnorm", "moe_routing_stats",
     "moe_layer_forward", "moe_check_device_error", "moe_set_wait_limit_ns", "moe_version",
     "library_path",
 ]
@@ -211,3 +211,22 @@ def moe_layer_forward(x: torch.Tensor, w_gate: torch.Tensor, w1: torch.Tensor, w
                                          _ptr(ws), ws.numel(), _stream(stream))
     check("moe_layer_forward", st)
     return y
+
+
+def moe_routing_stats(topk_idx: torch.Tensor, n: int, seq_len: int = 0, *,
+                      expert_counts: Optional[torch.Tensor] = None,
+                      pair_counts: Optional[torch.Tensor] = None, stream=None):
+    """Expert load and consecutive-token repetition of one layer's TopK selections.
+
+    Returns (expert_counts int64 [n], pair_counts int64 [3] = pairs, same first choice,
+    shared expert)."""
+    T, k = topk_idx.shape
+    dev = topk_idx.device
+    if expert_counts is None:
+        expert_counts = torch.empty(n, dtype=torch.int64, device=dev)
+    if pair_counts is None:
+        pair_counts = torch.empty(3, dtype=torch.int64, device=dev)
+    st = _native.lib().moe_routing_stats(_ptr(topk_idx), T, k, n, int(seq_len), _ptr(expert_counts),
+                                         _ptr(pair_counts), _stream(stream))
+    check("moe_routing_stats", st)
+    return expert_counts, pair_counts

@@ -38,6 +38,7 @@ SIGNATURES = {
     "moe_rmsnorm": (_I, [_P, _I, _I, _F, _I, _P, _P]),
     "moe_layer_forward": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P,
                                _SZ, _P]),
+    "moe_routing_stats": (_I, [_P, _I, _I, _I, _I, _P, _P, _P]),
     "moe_check_device_error": (_I, [_P, _SZ, _P]),
     "moe_set_wait_limit_ns": (None, [ctypes.c_ulonglong]),
 }

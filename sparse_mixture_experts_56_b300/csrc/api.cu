@@ -273,6 +273,17 @@ moe_status moe_layer_forward(const void* x, const void* w_gate, const float* log
   return MOE_OK;
 }
 
+moe_status moe_routing_stats(const int32_t* topk_idx, int T, int k, int n, int seq_len,
+                             int64_t* expert_counts, int64_t* pair_counts, void* stream) {
+  if (!sizes_ok(T, 1, 1, n, k) || seq_len < 0) return MOE_ERR_INVALID_ARG;
+  if (!expert_counts || !pair_counts || (T > 0 && !topk_idx)) return MOE_ERR_INVALID_ARG;
+  if (((uintptr_t)expert_counts & 7u) || ((uintptr_t)pair_counts & 7u) ||
+      ((uintptr_t)topk_idx & 3u))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_routing_stats(topk_idx, T, k, n, seq_len, expert_counts, pair_counts,
+                                          (cudaStream_t)stream));
+}
+
 moe_status moe_check_device_error(void* ws, size_t ws_bytes, void* stream) {
   if (!ws || ws_bytes < kAlign) return MOE_ERR_WORKSPACE;
   cudaStream_t s = (cudaStream_t)stream;

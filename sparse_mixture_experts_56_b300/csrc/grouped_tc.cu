@@ -300,6 +300,13 @@ __global__ void __launch_bounds__(256, 1)
   tc_fence_after();
   const uint32_t tmem_base = sh.tmem_base;
   const int total = sh.total;
+  // Balanced static schedule: the fewest CTAs that still finish in the same number of tile
+  // rounds, so every working CTA gets the same number of tiles (+-1 only in the last round);
+  // the spare CTAs exit at once.  For weight-streaming (HBM-bound) launches this removes
+  // the tail round in which a few CTAs stream alone.
+  const int rounds = (total + (int)gridDim.x - 1) / (int)gridDim.x;
+  const int gstride = rounds > 0 ? (total + rounds - 1) / rounds : (int)gridDim.x;
+  const int first_tile = (int)blockIdx.x < gstride ? (int)blockIdx.x : total;
   const uint64_t limit = args.wait_ns;
 
   if (warp == 0 && lane == 0) {
@@ -310,7 +317,7 @@ __global__ void __launch_bounds__(256, 1)
     int stage = 0;
     uint32_t phase = 0, issued = 0, iphase = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+    for (int tile = first_tile; ok && tile < total; tile += gstride) {
       const Tile t = decode_tile(sh, n, args.ntiles, tile);
       const int brow = t.e * args.ndim + t.nt * (MODE == kSwiGLU ? BN / 2 : BN);
       for (int kb = 0; kb < KB; ++kb) {
@@ -343,7 +350,7 @@ __global__ void __launch_bounds__(256, 1)
     int stage = 0, acc = 0;
     uint32_t phase = 0, acc_phase = 0;
     bool ok = true, any_mma = false;
-    for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+    for (int tile = first_tile; ok && tile < total; tile += gstride) {
       if (!wait_phase(smem_u32(&sh.tempty[acc]), acc_phase ^ 1u, abort, limit)) {
         raise_abort(abort, args.status);
         break;
@@ -388,7 +395,7 @@ __global__ void __launch_bounds__(256, 1)
     const int r = q * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+    for (int tile = first_tile; tile < total; tile += gstride) {
       const Tile t = decode_tile(sh, n, args.ntiles, tile);
       int ok = 1;
       if (lane == 0) {

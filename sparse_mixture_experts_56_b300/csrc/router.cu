@@ -5,10 +5,11 @@
 //   kept experts get weight, and those weights sum to 1).
 // Also the row-wise RMSNorm used by stacked layers (not part of the pages' layer).
 //
-// One warp per token.  The token's row of x is read once (16-byte loads); W_g (d x n,
-// 64 KB for 4096 x 8 bf16) stays hot in L1/L2.  Products accumulate in fp32 per lane,
-// then a butterfly reduction gives every lane all n logits.  Lane 0 selects the top K
-// (ties -> lower index, descending order) and normalises exp(l - l_max) over them.
+// One warp per token (for batches of at most 1024 tokens, one block per token, its 8 warps
+// splitting the row).  The token's row of x is read once (16-byte loads); W_g (d x n, 64 KB
+// for 4096 x 8 bf16) stays hot in L1/L2.  Products accumulate in fp32 per lane, then a
+// butterfly reduction gives every lane all n logits.  Lane 0 selects the top K (ties ->
+// lower index, descending order) and normalises exp(l - l_max) over them.
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -153,6 +154,70 @@ __global__ void __launch_bounds__(256) router_bf16_n8_kernel(const bf16* __restr
   }
 }
 
+// Small batches (too few tokens to fill the GPU with one warp each): one block per token.
+// The 8 warps split the row of x into 2048-element slabs, reduce within the warp, and meet
+// in shared memory; warp 0 adds the 8 partial sums per expert in a fixed order.
+__global__ void __launch_bounds__(256) router_bf16_n8_block_kernel(const bf16* __restrict__ x,
+                                                                   const bf16* __restrict__ wg,
+                                                                   const float* __restrict__ bias,
+                                                                   int Tn, int d, int k,
+                                                                   int32_t* __restrict__ idx,
+                                                                   float* __restrict__ w,
+                                                                   float* __restrict__ logits) {
+  __shared__ float part[8][8];  // [warp][expert]
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int t = blockIdx.x; t < Tn; t += gridDim.x) {
+    float acc[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+    const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)t * d);
+#pragma unroll 2
+    for (int i0 = threadIdx.x * 8; i0 < d; i0 += 2048) {
+      const uint4 xv = __ldg(xr + (i0 >> 3));
+      const __nv_bfloat162* xp = reinterpret_cast<const __nv_bfloat162*>(&xv);
+      const uint4* wr = reinterpret_cast<const uint4*>(wg + (size_t)i0 * 8);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float2 xf = __bfloat1622float2(xp[j >> 1]);
+        const float xs = (j & 1) ? xf.y : xf.x;
+        const uint4 wv = __ldg(wr + j);
+        const __nv_bfloat162* wp = reinterpret_cast<const __nv_bfloat162*>(&wv);
+#pragma unroll
+        for (int e2 = 0; e2 < 4; ++e2) {
+          const float2 wf = __bfloat1622float2(wp[e2]);
+          acc[2 * e2] = fmaf(xs, wf.x, acc[2 * e2]);
+          acc[2 * e2 + 1] = fmaf(xs, wf.y, acc[2 * e2 + 1]);
+        }
+      }
+    }
+    warp_allreduce<8>(acc);
+    if (lane == 0) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) part[warp][e] = acc[e];
+    }
+    __syncthreads();
+    if (warp == 0) {
+      float l[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        float v = 0.f;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) v += part[q][e];
+        l[e] = bias ? v + bias[e] : v;
+      }
+      if (logits && lane < 8) {
+        float v = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          if (e == lane) v = l[e];
+        logits[(size_t)t * 8 + lane] = v;
+      }
+      if (lane == 0) select_and_write<8>(l, 8, k, idx + (size_t)t * k, w + (size_t)t * k);
+    }
+    __syncthreads();
+  }
+}
+
 template <typename T>
 __global__ void __launch_bounds__(256) rmsnorm_kernel(const T* __restrict__ h, int Tn, int d,
                                                       float eps, T* __restrict__ x) {
@@ -211,6 +276,9 @@ __global__ void __launch_bounds__(256) rmsnorm_bf16_vec_kernel(const bf16* __res
   }
 }
 
+// Up to this many tokens the router gives each token a whole block (8 warps over d).
+constexpr int kRouterBlockPerTokenMax = 1024;
+
 int grid_for_warps(long long warps_needed) {
   const long long blocks = (warps_needed + 7) / 8;
   const long long cap = (long long)device_sm_count() * 16;
@@ -224,7 +292,10 @@ cudaError_t launch_router_topk(const void* x, const void* wg, const float* bias,
                                cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   const int grid = grid_for_warps(T);
-  if (dtype == MOE_BF16 && n == 8 && d % 256 == 0) {
+  if (dtype == MOE_BF16 && n == 8 && d % 256 == 0 && T <= kRouterBlockPerTokenMax) {
+    router_bf16_n8_block_kernel<<<T, 256, 0, s>>>((const bf16*)x, (const bf16*)wg, bias, T, d, k,
+                                                   idx, w, logits);
+  } else if (dtype == MOE_BF16 && n == 8 && d % 256 == 0) {
     router_bf16_n8_kernel<<<grid, 256, 0, s>>>((const bf16*)x, (const bf16*)wg, bias, T, d, k, idx,
                                                 w, logits);
   } else if (dtype == MOE_BF16) {

@@ -93,6 +93,13 @@ def test_host_validation_rejects_before_launch(lib):
     # rmsnorm: aliasing and negative eps
     assert lib.moe_rmsnorm(fake, 4, 64, 1e-5, 1, fake, nul) == INVALID
     assert lib.moe_rmsnorm(fake, 4, 64, -1.0, 1, ctypes.c_void_p(8192), nul) == INVALID
+    # routing statistics: bad sizes, missing outputs, misaligned counters, then T == 0 is
+    # still a launch (it zeroes the outputs), so only the rejections are checked here
+    assert lib.moe_routing_stats(fake, 4, 2, 8, -1, fake, fake, nul) == INVALID
+    assert lib.moe_routing_stats(fake, 4, 9, 8, 0, fake, fake, nul) == INVALID
+    assert lib.moe_routing_stats(fake, 4, 2, 8, 0, nul, fake, nul) == INVALID
+    assert lib.moe_routing_stats(nul, 4, 2, 8, 0, fake, fake, nul) == INVALID
+    assert lib.moe_routing_stats(fake, 4, 2, 8, 0, ctypes.c_void_p(4100), fake, nul) == INVALID
     assert lib.moe_check_device_error(nul, 0, nul) == WORKSPACE
     lib.moe_set_wait_limit_ns(0)
 

@@ -233,6 +233,22 @@ moe_status moe_check_device_error(void* ws, size_t ws_bytes, void* stream);
  */
 void moe_set_wait_limit_ns(unsigned long long ns);
 
+/*
+ * Which form of the tensor-core expert GEMMs the bf16 calls use (process-wide; takes effect
+ * at the next launch):
+ *   MOE_TC_FORM_AUTO    (default) the down-projection (w2) in the CTA-pair form (tcgen05
+ *                       cta_group::2, 256-row tiles over two SMs) when the experts average
+ *                       at least 256 rows, i.e. T*k >= 256*n; everything else in the
+ *                       single-CTA form (128-row tiles)
+ *   MOE_TC_FORM_SINGLE  always the single-CTA form
+ *   MOE_TC_FORM_PAIR    always the CTA-pair form (where the device can co-schedule pairs)
+ * Both forms compute the same results up to the fp32 accumulation order inside a tile
+ * (which is the same: both accumulate K in ascending order), so outputs are identical.
+ * Returns MOE_ERR_INVALID_ARG for any other value.
+ */
+enum { MOE_TC_FORM_AUTO = 0, MOE_TC_FORM_SINGLE = 1, MOE_TC_FORM_PAIR = 2 };
+moe_status moe_set_tc_form(int form);
+
 #ifdef __cplusplus
 }
 #endif

@@ -14,13 +14,15 @@ from typing import Optional, Tuple
 import torch
 
 from . import _native
-from ._native import MOE_BF16, MOE_F32, MoEError, check
+from ._native import (MOE_BF16, MOE_F32, MOE_TC_FORM_AUTO, MOE_TC_FORM_PAIR, MOE_TC_FORM_SINGLE,
+                      MoEError, check)
 
 __all__ = [
     "MOE_F32", "MOE_BF16", "MoEError", "dtype_code", "moe_workspace_size", "workspace",
     "moe_router_topk", "moe_permute", "moe_permute_noalloc", "moe_grouped_swiglu", "moe_expert_up", "moe_expert_down",
     "moe_combine", "moe_rmsnorm", "moe_routing_stats",
-    "moe_layer_forward", "moe_check_device_error", "moe_set_wait_limit_ns", "moe_version",
+    "moe_layer_forward", "moe_check_device_error", "moe_set_wait_limit_ns", "moe_set_tc_form",
+    "MOE_TC_FORM_AUTO", "MOE_TC_FORM_SINGLE", "MOE_TC_FORM_PAIR", "moe_version",
     "library_path",
 ]
 
@@ -74,6 +76,11 @@ def workspace(T: int, d: int, f: int, n: int, k: int, dtype, device="cuda") -> t
 
 def moe_set_wait_limit_ns(ns: int) -> None:
     _native.lib().moe_set_wait_limit_ns(int(ns))
+
+
+def moe_set_tc_form(form: int) -> None:
+    """Selects the tensor-core GEMM form: MOE_TC_FORM_AUTO, _SINGLE or _PAIR."""
+    check("moe_set_tc_form", _native.lib().moe_set_tc_form(int(form)))
 
 
 def moe_check_device_error(ws: torch.Tensor, stream=None) -> int:

@@ -14,6 +14,10 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoe.so")
 MOE_F32 = 0
 MOE_BF16 = 1
 
+MOE_TC_FORM_AUTO = 0
+MOE_TC_FORM_SINGLE = 1
+MOE_TC_FORM_PAIR = 2
+
 STATUS_NAMES = {
     0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",
     4: "MOE_ERR_CUDA", 5: "MOE_ERR_TIMEOUT", 6: "MOE_ERR_DEVICE_INDEX",
@@ -41,6 +45,7 @@ SIGNATURES = {
     "moe_routing_stats": (_I, [_P, _I, _I, _I, _I, _P, _P, _P]),
     "moe_check_device_error": (_I, [_P, _SZ, _P]),
     "moe_set_wait_limit_ns": (None, [ctypes.c_ulonglong]),
+    "moe_set_tc_form": (_I, [_I]),
 }
 
 _lib = None

@@ -302,4 +302,11 @@ moe_status moe_check_device_error(void* ws, size_t ws_bytes, void* stream) {
 
 void moe_set_wait_limit_ns(unsigned long long ns) { g_wait_ns.store(ns ? ns : kDefaultWaitNs); }
 
+moe_status moe_set_tc_form(int form) {
+  if (form != MOE_TC_FORM_AUTO && form != MOE_TC_FORM_SINGLE && form != MOE_TC_FORM_PAIR)
+    return MOE_ERR_INVALID_ARG;
+  set_tc_form(form);
+  return MOE_OK;
+}
+
 }  // extern "C"

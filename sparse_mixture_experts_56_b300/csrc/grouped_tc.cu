@@ -5,17 +5,27 @@
 // (xyznot.com summary), Método: each expert is a SwiGLU network of intermediate size 14336;
 // ja.news.hada.io, 実装と推論効率: experts receive variable numbers of tokens).
 //
-// Design (one persistent CTA per SM, 256 threads):
-//   warp 0      TMA producer: A tile [128 x 64] + B tile [256 x 64] per stage, 128-byte
-//               swizzle, into a 4-stage shared-memory ring (48 KB per stage).
-//   warp 1      MMA issuer: tcgen05.mma.cta_group::1.kind::f16, M=128 N=256 K=16, four per
-//               stage, into one of two TMEM accumulators (2 x 256 columns = all 512).
+// Design (persistent, one CTA per SM, 256 threads, warp-specialised):
+//   warp 0      TMA producer: A tile [128 x 64] + B tile [rows x 64] per stage, 128-byte
+//               swizzle, into a shared-memory ring.
+//   warp 1      MMA issuer: tcgen05.mma.kind::f16, N=256 K=16, four per stage, into one of two
+//               TMEM accumulators (2 x 256 columns = all 512).
 //   warp 2      allocates / frees the 512 TMEM columns.
 //   warps 4-7   epilogue: tcgen05.ld 32x32b (warp w reads TMEM lanes 32*(w-4)...), then
 //               GEMM1: SiLU(a)⊙b -> bf16 h;  GEMM2: -> bf16 y_perm.  Rows beyond the
 //               expert's count are computed but never stored.
-// For GEMM1 the B tile stacks 128 rows of w1_e over the same 128 rows of w3_e, so one
-// N=256 MMA fills both halves of the accumulator that the SwiGLU epilogue pairs up.
+// Two forms share this code:
+//   single CTA  (cta_group::1) M=128 tiles; each stage holds A [128 x 64] and all 256 B rows
+//               (48 KB, 4 stages).  Used for small expert groups (decode), where the kernel
+//               streams weights and the smaller tile wastes less of each MMA, and for GEMM1.
+//   CTA pair    (cta_group::2, clusters of 2) M=256 tiles: each CTA loads its own 128 rows of
+//               A and HALF of the 256 B rows (32 KB per stage, 6 stages); the even CTA issues
+//               one MMA that reads both CTAs' shared memory and writes each CTA's 128 rows of
+//               the accumulator into its own TMEM.  Per FLOP every SM moves a third less data
+//               from L2 into shared memory.  Used for GEMM2 on large expert groups.
+// For GEMM1 the 256 accumulator columns pair 128 rows of w1_e with the same 128 rows of w3_e
+// (single CTA: both in one stage; pair: w1 in the even CTA, w3 in the odd one), so the SwiGLU
+// epilogue finds a and b in columns c and 128 + c of the same TMEM lane.
 // Work list: tiles (expert, m-tile, n-tile) enumerated on the device from expert_offsets
 // (no host synchronisation); within an expert, groups of 16 m-tiles sweep all n-tiles so
 // that the weight tiles of concurrently running CTAs are shared through L2.
@@ -23,9 +33,11 @@
 // Every wait is bounded (globaltimer).  A wait that runs past the limit raises the CTA's
 // abort flag and sets the timeout bit of the device status word; every role then stops,
 // the producer waits (bounded) for its copies in flight, the MMA warp waits for its MMAs,
-// and the TMEM columns are freed before the CTA exits.
+// and the TMEM columns are freed before the CTA exits.  In the pair form a CTA that gives up
+// makes its peer's waits run out too; both meet at the final cluster barrier.
 #include <cuda.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "moe_internal.cuh"
@@ -33,25 +45,35 @@
 namespace moe {
 namespace {
 
-constexpr int BM = 128;                 // tile rows (tokens)  = UMMA M
+constexpr int BM = 128;                 // accumulator rows per CTA (TMEM lanes)
 constexpr int BK = 64;                  // K per stage: one 128-byte swizzle atom of bf16
-constexpr int BN = 256;                 // B rows per stage    = UMMA N = accumulator columns
+constexpr int BN = 256;                 // UMMA N = accumulator columns
 constexpr int UMMA_K = 16;
-constexpr int STAGES = 4;
 constexpr int ACC = 2;                  // TMEM accumulators
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int GROUP_M = 16;
-constexpr uint32_t A_BYTES = BM * BK * 2;
-constexpr uint32_t B_BYTES = BN * BK * 2;
-constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr uint64_t kDrainNs = 200ull * 1000 * 1000;
-
-// instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A bf16 (7-9 = 1), B bf16
-// (10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 at bits 17-22, M >> 4 at bits 24-28.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
-                            ((uint32_t)(BM >> 4) << 24);
+constexpr uint64_t kPeerGraceNs = 1000ull * 1000;
 
 enum Mode { kSwiGLU = 0, kDown = 1 };
+
+// Geometry of the two forms.
+template <bool PAIR>
+struct Cfg {
+  static constexpr int kCtas = PAIR ? 2 : 1;
+  static constexpr int kTileM = BM * kCtas;            // rows of one tile
+  static constexpr int kBRows = BN / kCtas;            // B rows each CTA loads per stage
+  static constexpr int kStages = PAIR ? 6 : 4;
+  static constexpr uint32_t kABytes = BM * BK * 2;
+  static constexpr uint32_t kBBytes = kBRows * BK * 2;
+  static constexpr uint32_t kStageBytes = kABytes + kBBytes;
+  // instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A bf16 (7-9 = 1), B bf16
+  // (10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 at bits 17-22, M >> 4 at bits 24-28
+  // (M of the whole CTA pair in the pair form).
+  static constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
+                                     ((uint32_t)(BN >> 3) << 17) |
+                                     ((uint32_t)(kTileM >> 4) << 24);
+};
 
 struct TcArgs {
   const int32_t* offsets;
@@ -64,6 +86,7 @@ struct TcArgs {
   unsigned long long wait_ns;
 };
 
+template <int STAGES>
 struct Shared {
   uint64_t full[STAGES];
   uint64_t empty[STAGES];
@@ -78,7 +101,11 @@ struct Shared {
   int off[kMaxExperts + 1];
 };
 
-constexpr size_t kSmemBytes = 1024 + (size_t)STAGES * STAGE_BYTES + sizeof(Shared);
+template <bool PAIR>
+constexpr size_t smem_bytes() {
+  return 1024 + (size_t)Cfg<PAIR>::kStages * Cfg<PAIR>::kStageBytes +
+         sizeof(Shared<Cfg<PAIR>::kStages>);
+}
 
 // ------------------------------------------------------------------------------------------
 // PTX wrappers
@@ -90,6 +117,21 @@ __device__ __forceinline__ uint64_t gtimer() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
+}
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Address, in the cluster's shared window, of the same shared variable in CTA `rank`.
+__device__ __forceinline__ uint32_t peer_addr(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+               ::: "memory");
 }
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
@@ -111,12 +153,27 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
+// Arrive on an mbarrier of another CTA of the cluster (address from peer_addr).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
+               : "memory");
+}
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                             int c0, int c1) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
       "l"((uint64_t)map), "r"(bar), "r"(c0), "r"(c1)
+      : "memory");
+}
+// Pair form: the copy lands in this CTA's shared memory and its bytes are counted on an
+// mbarrier that may live in either CTA of the pair (`bar_cluster` from peer_addr).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map,
+                                                 uint32_t bar_cluster, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"((uint64_t)map), "r"(bar_cluster), "r"(c0), "r"(c1)
       : "memory");
 }
 __device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
@@ -133,18 +190,75 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   return (uint64_t)((saddr & 0x3FFFFu) >> 4) | (1ull << 16) | ((uint64_t)(1024 >> 4) << 32) |
          (1ull << 46) | (2ull << 61);
 }
+template <bool PAIR>
 __device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
                                           uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
-      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
-      : "memory");
+  if constexpr (PAIR)
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
+        "l"(adesc), "l"(bdesc), "r"(Cfg<true>::kIdesc), "r"(accumulate)
+        : "memory");
+  else
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
+        "l"(adesc), "l"(bdesc), "r"(Cfg<false>::kIdesc), "r"(accumulate)
+        : "memory");
 }
-__device__ __forceinline__ void umma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                   bar)
-               : "memory");
+// Arrives on `bar` once the MMAs issued so far by this thread are done: in the pair form on
+// the barrier at that offset in both CTAs.
+template <bool PAIR>
+__device__ __forceinline__ void umma_commit_all(uint32_t bar) {
+  if constexpr (PAIR)
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(bar),
+        "h"((uint16_t)0x3)
+        : "memory");
+  else
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+// Arrives on this CTA's `bar` only.
+template <bool PAIR>
+__device__ __forceinline__ void umma_commit_local(uint32_t bar) {
+  if constexpr (PAIR)
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+  else
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+template <bool PAIR>
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem) {
+  if constexpr (PAIR) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     dst_smem),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  } else {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     dst_smem),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+}
+template <bool PAIR>
+__device__ __forceinline__ void tmem_dealloc(uint32_t base) {
+  if constexpr (PAIR)
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(base),
+                 "r"(TMEM_COLS)
+                 : "memory");
+  else
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(base),
+                 "r"(TMEM_COLS)
+                 : "memory");
 }
 
 #define MOE_R32(r)                                                                               \
@@ -203,24 +317,31 @@ __device__ __noinline__ bool drain_phase(uint32_t bar, uint32_t parity, uint64_t
     if (gtimer() - t0 > limit_ns) return false;
   }
 }
+__device__ __noinline__ void spin_ns(uint64_t ns) {
+  const uint64_t t0 = gtimer();
+  while (gtimer() - t0 < ns) {
+  }
+}
 
 struct Tile {
   int e, mt, nt, row0, rows;
 };
 
-__device__ __forceinline__ Tile decode_tile(const Shared& sh, int n, int ntiles, int tile) {
+template <int TILE_M>
+__device__ __forceinline__ Tile decode_tile(const int* tile_base, const int* mtiles,
+                                            const int* off, int n, int ntiles, int tile) {
   int e = 0;
-  while (e + 1 < n && sh.tile_base[e + 1] <= tile) ++e;
-  const int u = tile - sh.tile_base[e];
+  while (e + 1 < n && tile_base[e + 1] <= tile) ++e;
+  const int u = tile - tile_base[e];
   const int per_group = GROUP_M * ntiles;
   const int g = u / per_group, r = u - g * per_group;
-  const int gsz = min(GROUP_M, sh.mtiles[e] - g * GROUP_M);
+  const int gsz = min(GROUP_M, mtiles[e] - g * GROUP_M);
   Tile t;
   t.e = e;
   t.mt = g * GROUP_M + r % gsz;
   t.nt = r / gsz;
-  t.row0 = sh.off[e] + t.mt * BM;
-  t.rows = min(BM, sh.off[e + 1] - sh.off[e] - t.mt * BM);
+  t.row0 = off[e] + t.mt * TILE_M;
+  t.rows = min(TILE_M, off[e + 1] - off[e] - t.mt * TILE_M);
   return t;
 }
 
@@ -245,28 +366,33 @@ __device__ __forceinline__ void store_row32(bf16* dst, const float (&v)[32]) {
 // ------------------------------------------------------------------------------------------
 // the kernel
 // ------------------------------------------------------------------------------------------
-template <int MODE>
+template <int MODE, bool PAIR>
 __global__ void __launch_bounds__(256, 1)
     grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB0,
                            const __grid_constant__ CUtensorMap tmB1, const TcArgs args) {
+  using C = Cfg<PAIR>;
+  constexpr int STAGES = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t* sA = smem;                              // STAGES x 16 KB
-  uint8_t* sB = smem + STAGES * A_BYTES;           // STAGES x 32 KB
-  Shared& sh = *reinterpret_cast<Shared*>(smem + STAGES * STAGE_BYTES);
+  uint8_t* sA = smem;                                  // STAGES x 16 KB
+  uint8_t* sB = smem + STAGES * C::kABytes;            // STAGES x B_BYTES
+  Shared<STAGES>& sh = *reinterpret_cast<Shared<STAGES>*>(smem + STAGES * C::kStageBytes);
   volatile int* abort = &sh.abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n = args.n;
   const int KB = args.kdim / BK;
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;   // 0 = the CTA that issues the MMAs
+  const int unit = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int units = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
 
   if (threadIdx.x == 0) {
     int acc = 0;
     for (int e = 0; e < n; ++e) {
       const int o0 = args.offsets[e], o1 = args.offsets[e + 1];
-      const int mt = (o1 - o0 + BM - 1) / BM;
+      const int mt = (o1 - o0 + C::kTileM - 1) / C::kTileM;
       sh.off[e] = o0;
       sh.mtiles[e] = mt;
       sh.tile_base[e] = acc;
@@ -282,32 +408,29 @@ __global__ void __launch_bounds__(256, 1)
     }
     for (int a = 0; a < ACC; ++a) {
       mbar_init(smem_u32(&sh.tfull[a]), 1);
-      mbar_init(smem_u32(&sh.tempty[a]), 4);
+      mbar_init(smem_u32(&sh.tempty[a]), 4 * C::kCtas);   // the epilogue warps of every CTA
     }
     mbar_init(smem_u32(&sh.drain), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
-  if (warp == 2) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_u32(&sh.tmem_base)),
-                 "r"(TMEM_COLS)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-  }
+  if (warp == 2) tmem_alloc<PAIR>(smem_u32(&sh.tmem_base));
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR)
+    cluster_sync_all();   // the peer's barriers are initialised before anyone signals them
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = sh.tmem_base;
   const int total = sh.total;
-  // Balanced static schedule: the fewest CTAs that still finish in the same number of tile
-  // rounds, so every working CTA gets the same number of tiles (+-1 only in the last round);
-  // the spare CTAs exit at once.  For weight-streaming (HBM-bound) launches this removes
-  // the tail round in which a few CTAs stream alone.
-  const int rounds = (total + (int)gridDim.x - 1) / (int)gridDim.x;
-  const int gstride = rounds > 0 ? (total + rounds - 1) / rounds : (int)gridDim.x;
-  const int first_tile = (int)blockIdx.x < gstride ? (int)blockIdx.x : total;
   const uint64_t limit = args.wait_ns;
+  // Balanced static schedule: the fewest CTAs (pairs) that still finish in the same number
+  // of tile rounds, so every working unit gets the same number of tiles (+-1 only in the
+  // last round); the spare units exit at once.  For weight-streaming (HBM-bound) launches
+  // this removes the tail round in which a few CTAs stream alone.
+  const int rounds = (total + units - 1) / units;
+  const int gstride = rounds > 0 ? (total + rounds - 1) / rounds : units;
+  const int first_tile = unit < gstride ? unit : total;
 
   if (warp == 0 && lane == 0) {
     // ---------------------------------------------------------------- TMA producer
@@ -318,8 +441,14 @@ __global__ void __launch_bounds__(256, 1)
     uint32_t phase = 0, issued = 0, iphase = 0;
     bool ok = true;
     for (int tile = first_tile; ok && tile < total; tile += gstride) {
-      const Tile t = decode_tile(sh, n, args.ntiles, tile);
-      const int brow = t.e * args.ndim + t.nt * (MODE == kSwiGLU ? BN / 2 : BN);
+      const Tile t = decode_tile<C::kTileM>(sh.tile_base, sh.mtiles, sh.off, n, args.ntiles, tile);
+      const int arow = t.row0 + (int)rank * BM;
+      // first B row of this CTA's share: GEMM1 takes 128 rows of w1 (and of w3), GEMM2 256
+      // rows of w2, split between the two CTAs of a pair
+      const int brow = MODE == kSwiGLU
+                           ? t.e * args.ndim + t.nt * (BN / 2)
+                           : t.e * args.ndim + t.nt * BN + (int)rank * C::kBRows;
+      const CUtensorMap* bmap = (MODE == kSwiGLU && PAIR && rank == 1) ? &tmB1 : &tmB0;
       for (int kb = 0; kb < KB; ++kb) {
         if (!wait_phase(smem_u32(&sh.empty[stage]), phase ^ 1u, abort, limit)) {
           raise_abort(abort, args.status);
@@ -327,11 +456,21 @@ __global__ void __launch_bounds__(256, 1)
           break;
         }
         const uint32_t fb = smem_u32(&sh.full[stage]);
-        mbar_expect_tx(fb, STAGE_BYTES);
-        tma_load_2d(smem_u32(sA + stage * A_BYTES), &tmA, fb, kb * BK, t.row0);
-        tma_load_2d(smem_u32(sB + stage * B_BYTES), &tmB0, fb, kb * BK, brow);
-        if (MODE == kSwiGLU)
-          tma_load_2d(smem_u32(sB + stage * B_BYTES + B_BYTES / 2), &tmB1, fb, kb * BK, brow);
+        const uint32_t a_dst = smem_u32(sA + stage * C::kABytes);
+        const uint32_t b_dst = smem_u32(sB + stage * C::kBBytes);
+        if constexpr (PAIR) {
+          // both CTAs' bytes land on the even CTA's barrier, which the MMA issuer waits on
+          if (rank == 0) mbar_expect_tx(fb, 2 * C::kStageBytes);
+          const uint32_t fb0 = peer_addr(fb, 0);
+          tma_load_2d_pair(a_dst, &tmA, fb0, kb * BK, arow);
+          tma_load_2d_pair(b_dst, bmap, fb0, kb * BK, brow);
+        } else {
+          mbar_expect_tx(fb, C::kStageBytes);
+          tma_load_2d(a_dst, &tmA, fb, kb * BK, arow);
+          tma_load_2d(b_dst, &tmB0, fb, kb * BK, brow);
+          if (MODE == kSwiGLU)
+            tma_load_2d(b_dst + C::kBBytes / 2, &tmB1, fb, kb * BK, brow);
+        }
         issued |= 1u << stage;
         iphase = (iphase & ~(1u << stage)) | (phase << stage);
         if (++stage == STAGES) {
@@ -341,11 +480,17 @@ __global__ void __launch_bounds__(256, 1)
       }
     }
     // every copy issued must have landed before the CTA may exit
-    for (int s = 0; s < STAGES; ++s)
-      if ((issued >> s) & 1u)
-        if (!drain_phase(smem_u32(&sh.full[s]), (iphase >> s) & 1u, kDrainNs))
-          atomicOr(args.status, kDevErrTimeout);
-  } else if (warp == 1 && lane == 0) {
+    if (!PAIR || rank == 0) {
+      for (int s = 0; s < STAGES; ++s)
+        if ((issued >> s) & 1u)
+          if (!drain_phase(smem_u32(&sh.full[s]), (iphase >> s) & 1u, kDrainNs))
+            atomicOr(args.status, kDevErrTimeout);
+    } else if (issued && *abort) {
+      // the odd CTA's copies are counted on the even CTA's barriers; after an abort the
+      // even CTA may not wait for them, so give them time to land
+      spin_ns(kPeerGraceNs);
+    }
+  } else if (warp == 1 && lane == 0 && (!PAIR || rank == 0)) {
     // ---------------------------------------------------------------- MMA issuer
     int stage = 0, acc = 0;
     uint32_t phase = 0, acc_phase = 0;
@@ -364,21 +509,21 @@ __global__ void __launch_bounds__(256, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t a0 = smem_u32(sA + stage * A_BYTES);
-        const uint32_t b0 = smem_u32(sB + stage * B_BYTES);
+        const uint32_t a0 = smem_u32(sA + stage * C::kABytes);
+        const uint32_t b0 = smem_u32(sB + stage * C::kBBytes);
 #pragma unroll
         for (int kk = 0; kk < BK / UMMA_K; ++kk)
-          umma_bf16(d_tmem, sw128_desc(a0 + kk * UMMA_K * 2), sw128_desc(b0 + kk * UMMA_K * 2),
-                    (kb | kk) != 0 ? 1u : 0u);
+          umma_bf16<PAIR>(d_tmem, sw128_desc(a0 + kk * UMMA_K * 2),
+                          sw128_desc(b0 + kk * UMMA_K * 2), (kb | kk) != 0 ? 1u : 0u);
         any_mma = true;
-        umma_commit(smem_u32(&sh.empty[stage]));
+        umma_commit_all<PAIR>(smem_u32(&sh.empty[stage]));
         if (++stage == STAGES) {
           stage = 0;
           phase ^= 1u;
         }
       }
       if (!ok) break;
-      umma_commit(smem_u32(&sh.tfull[acc]));
+      umma_commit_all<PAIR>(smem_u32(&sh.tfull[acc]));
       if (++acc == ACC) {
         acc = 0;
         acc_phase ^= 1u;
@@ -386,7 +531,7 @@ __global__ void __launch_bounds__(256, 1)
     }
     // all MMAs issued by this thread must finish before the TMEM columns are freed
     if (any_mma) {
-      umma_commit(smem_u32(&sh.drain));
+      umma_commit_local<PAIR>(smem_u32(&sh.drain));
       if (!drain_phase(smem_u32(&sh.drain), 0, kDrainNs)) atomicOr(args.status, kDevErrTimeout);
     }
   } else if (warp >= 4) {
@@ -396,7 +541,7 @@ __global__ void __launch_bounds__(256, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = first_tile; tile < total; tile += gstride) {
-      const Tile t = decode_tile(sh, n, args.ntiles, tile);
+      const Tile t = decode_tile<C::kTileM>(sh.tile_base, sh.mtiles, sh.off, n, args.ntiles, tile);
       int ok = 1;
       if (lane == 0) {
         ok = wait_phase(smem_u32(&sh.tfull[acc]), acc_phase, abort, limit) ? 1 : 0;
@@ -405,12 +550,15 @@ __global__ void __launch_bounds__(256, 1)
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc_fence_after();
-      const bool row_ok = r < t.rows;
+      const int row = (int)rank * BM + r;   // row of the tile held in this TMEM lane
+      const bool row_ok = row < t.rows;
       const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
-      const uint32_t tempty = smem_u32(&sh.tempty[acc]);
+      const uint32_t tempty_local = smem_u32(&sh.tempty[acc]);
+      // the even CTA's MMA issuer waits for the epilogue warps of both CTAs
+      const uint32_t tempty = PAIR ? peer_addr(tempty_local, 0) : tempty_local;
       if (MODE == kSwiGLU) {
         const int col0 = t.nt * (BN / 2);
-        bf16* orow = args.out + (size_t)(t.row0 + r) * args.ndim + col0;
+        bf16* orow = args.out + (size_t)(t.row0 + row) * args.ndim + col0;
 #pragma unroll 1
         for (int c = 0; c < BN / 64; ++c) {
           uint32_t a[32], b[32];
@@ -421,7 +569,12 @@ __global__ void __launch_bounds__(256, 1)
           if (c == BN / 64 - 1) {
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(tempty);
+            if (lane == 0) {
+              if (PAIR)
+                mbar_arrive_cluster(tempty);
+              else
+                mbar_arrive(tempty);
+            }
           }
           if (row_ok && col0 + c * 32 < args.ndim) {
             float v[32];
@@ -436,7 +589,7 @@ __global__ void __launch_bounds__(256, 1)
         }
       } else {
         const int col0 = t.nt * BN;
-        bf16* orow = args.out + (size_t)(t.row0 + r) * args.ndim + col0;
+        bf16* orow = args.out + (size_t)(t.row0 + row) * args.ndim + col0;
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           uint32_t a[32];
@@ -445,7 +598,12 @@ __global__ void __launch_bounds__(256, 1)
           if (c == BN / 32 - 1) {
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(tempty);
+            if (lane == 0) {
+              if (PAIR)
+                mbar_arrive_cluster(tempty);
+              else
+                mbar_arrive(tempty);
+            }
           }
           if (row_ok && col0 + c * 32 < args.ndim) {
             float v[32];
@@ -464,12 +622,13 @@ __global__ void __launch_bounds__(256, 1)
 
   __syncwarp();
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR)
+    cluster_sync_all();   // neither CTA leaves while the other may still touch its memory
+  else
+    __syncthreads();
   if (warp == 2) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
-                 "r"(TMEM_COLS)
-                 : "memory");
+    tmem_dealloc<PAIR>(tmem_base);
   }
 }
 
@@ -508,25 +667,106 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int MODE>
+template <int MODE, bool PAIR>
 cudaError_t set_smem_attr() {
   static cudaError_t err = cudaErrorNotReady;
   static std::once_flag once;
   std::call_once(once, [] {
-    err = cudaFuncSetAttribute(grouped_gemm_tc_kernel<MODE>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    err = cudaFuncSetAttribute(grouped_gemm_tc_kernel<MODE, PAIR>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)smem_bytes<PAIR>());
   });
   return err;
 }
 
+// Clusters of two that can be resident at once (0 if the pair form cannot run here).
+template <int MODE>
+int max_pairs() {
+  static int cache[64];
+  static bool done[64] = {false};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!done[dev]) {
+    int clusters = 0;
+    if (set_smem_attr<MODE, true>() == cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 2;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.gridDim = dim3(2 * device_sm_count(), 1, 1);
+      cfg.blockDim = dim3(256, 1, 1);
+      cfg.dynamicSmemBytes = smem_bytes<true>();
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      if (cudaOccupancyMaxActiveClusters(&clusters, grouped_gemm_tc_kernel<MODE, true>, &cfg) !=
+          cudaSuccess)
+        clusters = 0;
+      (void)cudaGetLastError();
+    }
+    cache[dev] = clusters;
+    done[dev] = true;
+  }
+  return cache[dev];
+}
+
+std::atomic<int> g_tc_form{MOE_TC_FORM_AUTO};
+
+// Unless a form was forced with moe_set_tc_form: the pair form for GEMM2 (w2) when the
+// experts hold on average at least one full 256-row tile; the single form otherwise and for
+// GEMM1.  Measured on B300 at the prefill sizes (T = 4096 and 16384, d = 4096, f = 14336,
+// clocks held down by the power cap): GEMM2 runs 3-5 % faster as pairs; GEMM1 runs 1-2 %
+// slower, its 256-row tiles wasting more rows on the experts' ragged last tiles while its
+// single-CTA form already keeps up with the L2.
+template <int MODE>
+inline bool want_pair(int A, int n) {
+  const int form = g_tc_form.load(std::memory_order_relaxed);
+  if (form == MOE_TC_FORM_SINGLE) return false;
+  if (form == MOE_TC_FORM_PAIR) return true;
+  return MODE == kDown && (long long)A >= 256ll * n;
+}
+
+template <int MODE>
+cudaError_t launch_gemm(const CUtensorMap& mA, const CUtensorMap& mB0, const CUtensorMap& mB1,
+                        const TcArgs& a, int A, cudaStream_t s) {
+  const int sms = device_sm_count();
+  const int pairs = want_pair<MODE>(A, a.n) ? max_pairs<MODE>() : 0;
+  if (pairs > 0) {
+    const long long tiles = ((long long)(A + 255) / 256 + a.n) * a.ntiles;
+    const int units = (int)(tiles < pairs ? tiles : pairs);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2 * units, 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.dynamicSmemBytes = smem_bytes<true>();
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, grouped_gemm_tc_kernel<MODE, true>, mA, mB0, mB1, a);
+  }
+  cudaError_t e = set_smem_attr<MODE, false>();
+  if (e != cudaSuccess) return e;
+  const long long tiles = ((long long)(A + BM - 1) / BM + a.n) * a.ntiles;
+  grouped_gemm_tc_kernel<MODE, false><<<(int)(tiles < sms ? tiles : sms), 256,
+                                        smem_bytes<false>(), s>>>(mA, mB0, mB1, a);
+  return cudaGetLastError();
+}
+
 }  // namespace
+
+void set_tc_form(int form) { g_tc_form.store(form, std::memory_order_relaxed); }
 
 cudaError_t launch_up_tc(const bf16* x_perm, const int32_t* offsets, const bf16* w1, const bf16* w3,
                          int A, int d, int f, int n, bf16* h, uint32_t* status,
                          unsigned long long wait_ns, cudaStream_t s) {
   if (A == 0) return cudaSuccess;
-  cudaError_t e = set_smem_attr<kSwiGLU>();
-  if (e != cudaSuccess) return e;
   CUtensorMap mA, mW1, mW3;
   if (!make_map(&mA, x_perm, (uint64_t)A, (uint64_t)d, BM) ||
       !make_map(&mW1, w1, (uint64_t)n * f, (uint64_t)d, BN / 2) ||
@@ -541,22 +781,18 @@ cudaError_t launch_up_tc(const bf16* x_perm, const int32_t* offsets, const bf16*
   a.out = h;
   a.status = status;
   a.wait_ns = wait_ns;
-  const long long tiles = ((long long)(A + BM - 1) / BM + n) * a.ntiles;
-  const int sms = device_sm_count();
-  grouped_gemm_tc_kernel<kSwiGLU><<<(int)(tiles < sms ? tiles : sms), 256, kSmemBytes, s>>>(
-      mA, mW1, mW3, a);
-  return cudaGetLastError();
+  return launch_gemm<kSwiGLU>(mA, mW1, mW3, a, A, s);
 }
 
 cudaError_t launch_down_tc(const bf16* h, const int32_t* offsets, const bf16* w2, int A, int d,
                            int f, int n, bf16* y_perm, uint32_t* status, unsigned long long wait_ns,
                            cudaStream_t s) {
   if (A == 0) return cudaSuccess;
-  cudaError_t e = set_smem_attr<kDown>();
-  if (e != cudaSuccess) return e;
+  // the pair form loads 128 of the 256 rows of a w2 tile per CTA, the single form all 256
+  const uint32_t brows = want_pair<kDown>(A, n) && max_pairs<kDown>() > 0 ? BN / 2 : BN;
   CUtensorMap mA, mW2;
   if (!make_map(&mA, h, (uint64_t)A, (uint64_t)f, BM) ||
-      !make_map(&mW2, w2, (uint64_t)n * d, (uint64_t)f, BN))
+      !make_map(&mW2, w2, (uint64_t)n * d, (uint64_t)f, brows))
     return cudaErrorInvalidValue;
   TcArgs a;
   a.offsets = offsets;
@@ -567,11 +803,7 @@ cudaError_t launch_down_tc(const bf16* h, const int32_t* offsets, const bf16* w2
   a.out = y_perm;
   a.status = status;
   a.wait_ns = wait_ns;
-  const long long tiles = ((long long)(A + BM - 1) / BM + n) * a.ntiles;
-  const int sms = device_sm_count();
-  grouped_gemm_tc_kernel<kDown><<<(int)(tiles < sms ? tiles : sms), 256, kSmemBytes, s>>>(
-      mA, mW2, mW2, a);
-  return cudaGetLastError();
+  return launch_gemm<kDown>(mA, mW2, mW2, a, A, s);
 }
 
 }  // namespace moe

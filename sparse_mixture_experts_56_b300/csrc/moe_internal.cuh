@@ -69,6 +69,9 @@ cudaError_t launch_down_tc(const bf16* h, const int32_t* offsets, const bf16* w2
                            int f, int n, bf16* y_perm, uint32_t* status, unsigned long long wait_ns,
                            cudaStream_t s);
 
+// Which tensor-core GEMM form the launchers pick (MOE_TC_FORM_*; process-wide).
+void set_tc_form(int form);
+
 // Routing statistics of one layer (counts [n], pair_counts [3]: pairs, same first, shared).
 cudaError_t launch_routing_stats(const int32_t* idx, int T, int k, int n, int seq_len,
                                  int64_t* counts, int64_t* pair_counts, cudaStream_t s);

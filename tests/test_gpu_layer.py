@@ -39,6 +39,13 @@ LAYER_CASES = {
     "tc-n32-k2": (500, 128, 128, 32, 2, "bf16", False),
     "tc-t1": (1, 256, 256, 8, 2, "bf16", False),
     "simt-bf16-d200": (64, 200, 136, 8, 2, "bf16", False),     # not a multiple of 64
+    # CTA-pair tensor-core form (chosen when the experts average >= 256 rows): 256-row tiles
+    # split over two CTAs, ragged last tiles in both CTAs of a pair
+    "pair-t2048-d256-f384": (2048, 256, 384, 8, 2, "bf16", False),
+    "pair-t1500-d384-f320-skew": (1500, 384, 320, 8, 2, "bf16", True),   # partial n-tiles
+    "pair-n1-k1-t700": (700, 256, 256, 1, 1, "bf16", False),            # 3 tiles, 188-row tail
+    "pair-n2-k1-t600": (600, 128, 192, 2, 1, "bf16", False),
+    "pair-n32-k2-t4200": (4200, 128, 128, 32, 2, "bf16", False),
     "simt-fp32-n4": (45, 96, 80, 4, 2, "f32", True),
 }
 
@@ -78,7 +85,8 @@ def test_layer_forward_matches_oracle(moe, name):
     assert_close_rel(to_numpy_f32(y), yref, TOL[w.dtype])
 
 
-@pytest.mark.parametrize("name", ["tc-t300-d256-f384-skew", "tiny-fp32-t64", "simt-bf16-d200"])
+@pytest.mark.parametrize("name", ["tc-t300-d256-f384-skew", "tiny-fp32-t64", "simt-bf16-d200",
+                                  "pair-t1500-d384-f320-skew", "pair-n1-k1-t700"])
 def test_grouped_swiglu_rows(moe, name):
     """y_perm rows are the unweighted expert outputs E_e(x_t), grouped as the oracle groups."""
     w = _workload(name)
@@ -170,6 +178,65 @@ def test_timeout_path_reports_and_recovers(moe):
     assert st in (0, 5)   # 5 = MOE_ERR_TIMEOUT (0 only if every first wait already succeeded)
     y = moe.moe_layer_forward(g["x"], g["wg"], g["w1"], g["w3"], g["w2"], w.k, ws)
     assert moe.moe_check_device_error(ws) == 0
+    f = f32_inputs(inp, w)
+    yref = oracle.moe_layer(f["x"], f["wg"], f["w1"], f["w3"], f["w2"], w.k)
+    lref = oracle.router_logits(f["x"], f["wg"])
+    keep = ~oracle.near_tie_tokens(lref, w.k)[0]
+    assert_close_rel(to_numpy_f32(y)[keep], yref[keep], TOL["bf16"])
+
+
+@pytest.mark.parametrize("name", ["tc-t77-d128-f192", "tc-t640-d384-f320-skew", "pair-t1500-d384-f320-skew",
+                                  "pair-n1-k1-t700", "tc-t1"])
+def test_tc_forms_agree(moe, name):
+    """The single-CTA and CTA-pair forms of the expert GEMMs, each forced on the same inputs,
+    give identical outputs (both accumulate K in the same order), and match the oracle."""
+    w = _workload(name)
+    inp = workloads.make_inputs(w)
+    g = _dev_inputs(inp, w)
+    bias = torch.from_numpy(inp["bias"]).to(DEV) if inp["bias"] is not None else None
+    ws = moe.workspace(w.T, w.d, w.f, w.n, w.k, torch.bfloat16, DEV)
+    idx = torch.empty((w.T, w.k), dtype=torch.int32, device=DEV)
+    ys = {}
+    try:
+        for form in (moe.MOE_TC_FORM_SINGLE, moe.MOE_TC_FORM_PAIR):
+            moe.moe_set_tc_form(form)
+            ys[form] = moe.moe_layer_forward(g["x"], g["wg"], g["w1"], g["w3"], g["w2"], w.k, ws,
+                                             logit_bias=bias, topk_idx_out=idx)
+            assert moe.moe_check_device_error(ws) == 0
+    finally:
+        moe.moe_set_tc_form(moe.MOE_TC_FORM_AUTO)
+    a, b = ys[moe.MOE_TC_FORM_SINGLE], ys[moe.MOE_TC_FORM_PAIR]
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16)), \
+        f"forms differ in {(a != b).sum().item()} elements"
+    f = f32_inputs(inp, w)
+    lref = oracle.router_logits(f["x"], f["wg"], inp["bias"])
+    gi = idx.cpu().numpy().astype(np.int64)
+    yref = oracle.moe_layer(f["x"], f["wg"], f["w1"], f["w3"], f["w2"], w.k, inp["bias"],
+                            idx=gi, w=gate_weights_for(gi, lref))
+    assert_close_rel(to_numpy_f32(b), yref, TOL[w.dtype])
+
+
+def test_timeout_path_of_the_pair_form(moe):
+    """The CTA-pair form under a 1 ns wait limit: both CTAs of every pair give up, meet at
+    their final cluster barrier, report MOE_ERR_TIMEOUT, and the next call is correct."""
+    name = "pair-t2048-d256-f384"
+    w = _workload(name)
+    inp = workloads.make_inputs(w)
+    g = _dev_inputs(inp, w)
+    ws = moe.workspace(w.T, w.d, w.f, w.n, w.k, torch.bfloat16, DEV)
+    moe.moe_set_tc_form(moe.MOE_TC_FORM_PAIR)
+    try:
+        try:
+            moe.moe_set_wait_limit_ns(1)
+            moe.moe_layer_forward(g["x"], g["wg"], g["w1"], g["w3"], g["w2"], w.k, ws)
+            st = moe.moe_check_device_error(ws)
+        finally:
+            moe.moe_set_wait_limit_ns(0)
+        assert st in (0, 5)
+        y = moe.moe_layer_forward(g["x"], g["wg"], g["w1"], g["w3"], g["w2"], w.k, ws)
+        assert moe.moe_check_device_error(ws) == 0
+    finally:
+        moe.moe_set_tc_form(moe.MOE_TC_FORM_AUTO)
     f = f32_inputs(inp, w)
     yref = oracle.moe_layer(f["x"], f["wg"], f["w1"], f["w3"], f["w2"], w.k)
     lref = oracle.router_logits(f["x"], f["wg"])

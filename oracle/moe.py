@@ -292,8 +292,8 @@ def routing_statistics(idx, n: int, seq_len: int = 0):
                  Table 5 in the routing analysis; xyznot.com, "Limitaciones": 28.4% at
                  layer 15 against 12.5% = 1/8 for random assignment);
       same_any   pairs whose K chosen experts have at least one expert in common (the
-                 pages name only the first-choice measure; this reading of "the same
-                 expert chosen again, first or second choice" is the plainest one).
+                 pages define only the first-choice measure; this extension to all K
+                 choices takes the plainest reading of "the same expert chosen again").
 
     ``seq_len`` > 0 splits the T tokens into sequences of that length (the last one may
     be shorter) and no pair crosses a sequence boundary; 0 means one sequence.

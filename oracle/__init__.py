@@ -13,5 +13,6 @@ from .moe import (  # noqa: F401
     router_logits, topk_select, topk_mask, masked_softmax, gate, gate_softmax_then_topk,
     silu, expert_swiglu, group_by_expert, moe_layer, moe_layer_dense, rmsnorm,
     stacked_layer, near_tie_tokens, param_counts, consecutive_same_expert_rate,
-    routing_statistics,
+    routing_statistics, sigmoid, silu_grad, softmax_backward, expert_swiglu_backward,
+    moe_layer_backward,
 )

@@ -314,3 +314,83 @@ def routing_statistics(idx, n: int, seq_len: int = 0):
     # any expert of token t among the experts of token t+1
     share = (a[:, :, None] == b[:, None, :]).any(axis=(1, 2))
     return counts, int(inside.sum()), same_first, int(np.count_nonzero(share))
+
+
+# ------------------------------------------------------------------------------------------
+# Backward of the layer (the chain rule applied to the forward definitions above)
+# ------------------------------------------------------------------------------------------
+def sigmoid(z) -> np.ndarray:
+    z = _f64(z)
+    out = np.empty_like(z)
+    pos = z >= 0
+    out[pos] = 1.0 / (1.0 + np.exp(-z[pos]))
+    ez = np.exp(z[~pos])
+    out[~pos] = ez / (1.0 + ez)
+    return out
+
+
+def silu_grad(z) -> np.ndarray:
+    """d/dz SiLU(z) = sigma(z) + z sigma(z) (1 - sigma(z))."""
+    z = _f64(z)
+    s = sigmoid(z)
+    return s * (1.0 + z * (1.0 - s))
+
+
+def softmax_backward(p, dp) -> np.ndarray:
+    """Vector-Jacobian product of the softmax over the last axis: for p = softmax(z) and
+    dL/dp = dp, dL/dz = p (dp - sum_j p_j dp_j)."""
+    p, dp = _f64(p), _f64(dp)
+    return p * (dp - np.sum(p * dp, axis=-1, keepdims=True))
+
+
+def expert_swiglu_backward(xs, do, w1_e, w3_e, w2_e):
+    """Backward of E(x) = w2 (SiLU(w1 x) ⊙ (w3 x)) for the rows of ``xs`` [m, d] given
+    dL/dE = ``do`` [m, d].  Returns (dxs [m,d], dw1 [f,d], dw3 [f,d], dw2 [d,f])."""
+    xs, do = _f64(xs), _f64(do)
+    w1_e, w3_e, w2_e = _f64(w1_e), _f64(w3_e), _f64(w2_e)
+    a, b = xs @ w1_e.T, xs @ w3_e.T
+    s = silu(a)
+    h = s * b
+    dh = do @ w2_e
+    da = dh * b * silu_grad(a)
+    db = dh * s
+    return da @ w1_e + db @ w3_e, da.T @ xs, db.T @ xs, do.T @ h
+
+
+def moe_layer_backward(x, wg, w1, w3, w2, k: int, dy, bias=None, *, idx=None):
+    """Gradients of the scalar L = <dy, y> for y = moe_layer(x, ...), by the chain rule through
+    the definitions of [G] / [CS] (the pages train the model but print no backward; the
+    derivative of the forward they define is the only reading).  TopK is piecewise constant,
+    so logits outside the kept set get no gradient; inside it the softmax Jacobian gives
+    dl_i = G_i (dG_i - sum_j G_j dG_j) with dG_i = <dy, E_i(x)>.
+
+    ``idx`` overrides the selection (one row per token).  Returns a dict of float64 arrays:
+    dx [T,d], dwg [d,n], dw1 [n,f,d], dw3 [n,f,d], dw2 [n,d,f], dbias [n], dlogits [T,n],
+    dgate [T,k] (dG of the kept experts, slot order of idx)."""
+    x, dy = _f64(x), _f64(dy)
+    wg, w1, w3, w2 = _f64(wg), _f64(w1), _f64(w3), _f64(w2)
+    T, d = x.shape
+    n, f, _ = w1.shape
+    l = router_logits(x, wg, bias)
+    gi = topk_select(l, k) if idx is None else np.asarray(idx, dtype=np.int64)
+    gw = masked_softmax(np.take_along_axis(l, gi, axis=1))        # G at the kept experts
+    dx = np.zeros_like(x)
+    dw1, dw3, dw2 = np.zeros_like(w1), np.zeros_like(w3), np.zeros_like(w2)
+    dgate = np.zeros((T, gi.shape[1]))
+    offsets, perm, _ = group_by_expert(gi, n)
+    kk = gi.shape[1]
+    for e in range(n):
+        sel = perm[offsets[e]:offsets[e + 1]]
+        if sel.size == 0:
+            continue                                              # no rows, zero gradient
+        t, slot = sel // kk, sel % kk
+        xs, g = x[t], dy[t]
+        dgate[t, slot] = np.sum(g * expert_swiglu(xs, w1[e], w3[e], w2[e]), axis=1)
+        dxs, dw1[e], dw3[e], dw2[e] = expert_swiglu_backward(
+            xs, gw[t, slot][:, None] * g, w1[e], w3[e], w2[e])    # dL/dE_i(x) = G_i dy
+        np.add.at(dx, t, dxs)
+    dl = np.zeros((T, n))
+    np.put_along_axis(dl, gi, softmax_backward(gw, dgate), axis=1)
+    dx += dl @ wg.T
+    return {"dx": dx, "dwg": x.T @ dl, "dw1": dw1, "dw3": dw3, "dw2": dw2,
+            "dbias": dl.sum(axis=0), "dlogits": dl, "dgate": dgate}

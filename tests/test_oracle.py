@@ -264,11 +264,108 @@ def check_routing_statistics(o):
         assert abs(fa / p - (1 - math.comb(n - k, k) / math.comb(n, k))) < 0.005
 
 
+def _bwd_case(seed, T, d, f, n, k, margin=1e-2, scale=0.4):
+    """Random layer whose TopK decisions all have a gap of at least ``margin`` (so small
+    perturbations do not flip a selection)."""
+    rng = np.random.default_rng(seed)
+    while True:
+        x = rng.standard_normal((T, d))
+        wg = rng.standard_normal((d, n))
+        bias = rng.standard_normal(n) * 0.1
+        l = np.sort(x @ wg + bias, axis=1)[:, ::-1]
+        if k == n or np.all(l[:, k - 1] - l[:, k] > margin):
+            break
+    w1 = rng.standard_normal((n, f, d)) * scale
+    w3 = rng.standard_normal((n, f, d)) * scale
+    w2 = rng.standard_normal((n, d, f)) * scale
+    dy = rng.standard_normal((T, d))
+    return x, wg, w1, w3, w2, bias, dy
+
+
+def check_backward_finite_differences(o):
+    """Every gradient entry against central differences of L = <dy, y> in fp64."""
+    x, wg, w1, w3, w2, bias, dy = _bwd_case(70, 5, 6, 7, 4, 2)
+    params = {"x": x, "wg": wg, "w1": w1, "w3": w3, "w2": w2, "bias": bias}
+
+    def loss(p):
+        return float(np.sum(dy * o.moe_layer(p["x"], p["wg"], p["w1"], p["w3"], p["w2"], 2,
+                                             p["bias"])))
+    g = o.moe_layer_backward(x, wg, w1, w3, w2, 2, dy, bias)
+    names = {"x": "dx", "wg": "dwg", "w1": "dw1", "w3": "dw3", "w2": "dw2", "bias": "dbias"}
+    eps = 1e-6
+    for name, arr in params.items():
+        num = np.zeros_like(arr)
+        for i in np.ndindex(arr.shape):
+            p = {kk: v.copy() for kk, v in params.items()}
+            p[name][i] += eps
+            lp = loss(p)
+            p[name][i] -= 2 * eps
+            num[i] = (lp - loss(p)) / (2 * eps)
+        np.testing.assert_allclose(g[names[name]], num, rtol=1e-6, atol=1e-7, err_msg=name)
+
+
+def _torch_moe(x, wg, bias, w1, w3, w2, idx):
+    """The layer restated with torch ops on a fixed selection, for autograd."""
+    l = x @ wg + bias
+    gw = torch.softmax(torch.gather(l, 1, idx), dim=1)
+    y = torch.zeros_like(x)
+    for slot in range(idx.shape[1]):
+        e = idx[:, slot]
+        a = torch.einsum("td,tfd->tf", x, w1[e])
+        b = torch.einsum("td,tfd->tf", x, w3[e])
+        o = torch.einsum("tf,tdf->td", F.silu(a) * b, w2[e])
+        y = y + gw[:, slot:slot + 1] * o
+    return y
+
+
+def check_backward_autograd(o):
+    """The whole backward against torch autograd of a torch restatement of the forward."""
+    for seed, (T, d, f, n, k) in [(71, (40, 16, 24, 8, 2)), (72, (23, 8, 12, 5, 3)),
+                                  (73, (17, 8, 8, 6, 1))]:
+        x, wg, w1, w3, w2, bias, dy = _bwd_case(seed, T, d, f, n, k, margin=1e-6)
+        g = o.moe_layer_backward(x, wg, w1, w3, w2, k, dy, bias)
+        idx = torch.from_numpy(o.topk_select(x @ wg + bias, k))
+        ts = [torch.from_numpy(a).requires_grad_(True) for a in (x, wg, bias, w1, w3, w2)]
+        y = _torch_moe(*ts, idx)
+        (y * torch.from_numpy(dy)).sum().backward()
+        for name, t in zip(("dx", "dwg", "dbias", "dw1", "dw3", "dw2"), ts):
+            np.testing.assert_allclose(g[name], t.grad.numpy(), rtol=1e-10, atol=1e-11,
+                                       err_msg=name)
+
+
+def check_backward_special_cases(o):
+    # K = 1: the gate is identically 1, so the router gets no gradient
+    x, wg, w1, w3, w2, bias, dy = _bwd_case(74, 9, 8, 8, 4, 1)
+    g = o.moe_layer_backward(x, wg, w1, w3, w2, 1, dy, bias)
+    assert np.all(g["dlogits"] == 0) and np.all(g["dwg"] == 0)
+    # the softmax Jacobian keeps the logit gradient of every token summing to zero
+    x, wg, w1, w3, w2, bias, dy = _bwd_case(75, 30, 8, 8, 8, 3)
+    g = o.moe_layer_backward(x, wg, w1, w3, w2, 3, dy, bias)
+    np.testing.assert_allclose(g["dlogits"].sum(axis=1), 0.0, atol=1e-12)
+    assert np.all(np.count_nonzero(g["dlogits"], axis=1) <= 3)
+    # one expert, K = 1: the backward of a plain SwiGLU FFN (torch autograd of F.linear)
+    x, wg, w1, w3, w2, bias, dy = _bwd_case(76, 12, 8, 10, 1, 1)
+    g = o.moe_layer_backward(x, wg, w1, w3, w2, 1, dy)
+    tx, t1, t3, t2 = (torch.from_numpy(a).requires_grad_(True) for a in (x, w1[0], w3[0], w2[0]))
+    yt = F.linear(F.silu(F.linear(tx, t1)) * F.linear(tx, t3), t2)
+    (yt * torch.from_numpy(dy)).sum().backward()
+    np.testing.assert_allclose(g["dx"], tx.grad.numpy(), rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(g["dw1"][0], t1.grad.numpy(), rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(g["dw3"][0], t3.grad.numpy(), rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(g["dw2"][0], t2.grad.numpy(), rtol=1e-11, atol=1e-12)
+    # SiLU'(z) against the symmetric difference of SiLU, and at 0 (= 1/2)
+    z = np.linspace(-30, 30, 601)
+    np.testing.assert_allclose(o.silu_grad(z), (o.silu(z + 1e-6) - o.silu(z - 1e-6)) / 2e-6,
+                               rtol=1e-6, atol=1e-8)
+    assert o.silu_grad(np.array([0.0]))[0] == 0.5
+
+
 CHECKS = [check_worked_example, check_gate_invariants, check_topk_bruteforce,
           check_softmax_order_equivalence, check_single_expert_is_plain_ffn,
           check_k_equals_n_is_dense_softmax_mixture, check_sparse_equals_dense, check_grouping,
           check_silu, check_bias_enters_before_topk, check_rmsnorm, check_param_counts,
-          check_locality_metric, check_routing_statistics]
+          check_locality_metric, check_routing_statistics, check_backward_finite_differences,
+          check_backward_autograd, check_backward_special_cases]
 
 
 @pytest.mark.parametrize("check", CHECKS, ids=lambda c: c.__name__[6:])
@@ -356,6 +453,27 @@ def _mut_stats_slotwise_any(idx, n, seq_len=0):
     return c, p, f1, int(np.count_nonzero((e[:-1] == e[1:]).any(axis=1)[inside]))
 
 
+_ORIG_SWIGLU_BWD = moe_oracle.expert_swiglu_backward
+
+
+def _mut_silu_grad_sigmoid_only(z):
+    return moe_oracle.sigmoid(z)
+
+
+def _mut_softmax_bwd_no_centering(p, dp):
+    return np.asarray(p, dtype=np.float64) * np.asarray(dp, dtype=np.float64)
+
+
+def _mut_swiglu_bwd_dw2_transposed(xs, do, w1_e, w3_e, w2_e):
+    dxs, dw1, dw3, dw2 = _ORIG_SWIGLU_BWD(xs, do, w1_e, w3_e, w2_e)
+    return dxs, dw1, dw3, dw2.reshape(dw2.shape[1], dw2.shape[0]).T.reshape(dw2.shape)
+
+
+def _mut_swiglu_bwd_swapped_branches(xs, do, w1_e, w3_e, w2_e):
+    dxs, dw1, dw3, dw2 = _ORIG_SWIGLU_BWD(xs, do, w1_e, w3_e, w2_e)
+    return dxs, dw3, dw1, dw2
+
+
 MUTATIONS = {
     "silu->sigmoid": ("silu", _mut_sigmoid_for_silu),
     "swap w1/w3": ("expert_swiglu", _mut_swap_w1_w3),
@@ -369,6 +487,10 @@ MUTATIONS = {
     "rmsnorm without sqrt": ("rmsnorm", _mut_rms_no_sqrt),
     "pairs cross sequences": ("routing_statistics", _mut_stats_cross_sequences),
     "either-choice slot by slot": ("routing_statistics", _mut_stats_slotwise_any),
+    "SiLU' = sigmoid": ("silu_grad", _mut_silu_grad_sigmoid_only),
+    "softmax backward without centering": ("softmax_backward", _mut_softmax_bwd_no_centering),
+    "dw2 layout mix-up": ("expert_swiglu_backward", _mut_swiglu_bwd_dw2_transposed),
+    "dw1/dw3 swapped": ("expert_swiglu_backward", _mut_swiglu_bwd_swapped_branches),
 }
 
 

@@ -200,6 +200,35 @@ moe_status moe_layer_forward(const void* x, const void* w_gate, const float* log
                              size_t ws_bytes, void* stream);
 
 /*
+ * Backward of the layer y = MoE(x) (without residual; with y = r + MoE(x) the residual's
+ * gradient is dy itself): the gradients of L = <dy, y> by the chain rule through the pages'
+ * definition ("Mixtral of Experts", Método, eqs. G and y; blog.csdn.net MOE数学公式 §2).
+ * TopK is piecewise constant, so only the K kept logits of each token get gradient, through
+ * the softmax over them:  dl_k = G_k (dG_k - sum_j G_j dG_j),  dG_k = <dy, E_{e_k}(x)>.
+ * The routing is recomputed from x, w_gate and logit_bias with the forward's kernels (the
+ * same selection and gates as moe_layer_forward on the same inputs).
+ *   x, dy           [T, d] bf16         inputs of the forward / gradient of its output
+ *   w_gate [d, n], w1, w3 [n, f, d], w2 [n, d, f] bf16;  logit_bias [n] fp32 nullable
+ *   dx              [T, d] bf16 out     fp32 accumulation, one rounding
+ *   dw_gate         [d, n] fp32 out
+ *   dlogit_bias     [n] fp32 out, nullable
+ *   dw1, dw3        [n, f, d] bf16 out; dw2 [n, d, f] bf16 out (fp32 accumulation over the
+ *                   expert's rows in TMEM, one rounding; experts without rows get zeros)
+ *   ws, ws_bytes    at least moe_backward_workspace_size(T, d, f, n, k, dtype) bytes, its
+ *                   first 256 bytes zeroed as for every workspace (status word)
+ * Every output is overwritten (not accumulated into).  Only MOE_BF16 with d % 64 == 0 and
+ * f % 64 == 0 (the tensor-core path) is implemented; other shapes or fp32 return
+ * MOE_ERR_UNSUPPORTED.  The expert GEMMs run on tcgen05 in an expert-padded row order
+ * (every expert's rows padded with zero rows to a multiple of 128).
+ */
+size_t moe_backward_workspace_size(int T, int d, int f, int n, int k, int dtype);
+moe_status moe_layer_backward(const void* x, const void* w_gate, const float* logit_bias,
+                              const void* w1, const void* w3, const void* w2, const void* dy,
+                              int T, int d, int f, int n, int k, int dtype, void* dx,
+                              float* dw_gate, float* dlogit_bias, void* dw1, void* dw3, void* dw2,
+                              void* ws, size_t ws_bytes, void* stream);
+
+/*
  * Routing statistics of one layer from its TopK selections (newsflash.city digest,
  * "路径分析", Table 5: how often consecutive tokens are sent to the same expert;
  * "Mixtral of Experts" (xyznot.com summary), "Limitaciones": 28.4% first-choice repetition

@@ -20,7 +20,8 @@ from ._native import (MOE_BF16, MOE_F32, MOE_TC_FORM_AUTO, MOE_TC_FORM_PAIR, MOE
 __all__ = [
     "MOE_F32", "MOE_BF16", "MoEError", "dtype_code", "moe_workspace_size", "workspace",
     "moe_router_topk", "moe_permute", "moe_permute_noalloc", "moe_grouped_swiglu", "moe_expert_up", "moe_expert_down",
-    "moe_combine", "moe_rmsnorm", "moe_routing_stats",
+    "moe_combine", "moe_rmsnorm", "moe_routing_stats", "moe_backward_workspace_size",
+    "backward_workspace", "moe_layer_backward",
     "moe_layer_forward", "moe_check_device_error", "moe_set_wait_limit_ns", "moe_set_tc_form",
     "MOE_TC_FORM_AUTO", "MOE_TC_FORM_SINGLE", "MOE_TC_FORM_PAIR", "moe_version",
     "library_path",
@@ -237,3 +238,46 @@ def moe_routing_stats(topk_idx: torch.Tensor, n: int, seq_len: int = 0, *,
                                          _ptr(pair_counts), _stream(stream))
     check("moe_routing_stats", st)
     return expert_counts, pair_counts
+
+
+def moe_backward_workspace_size(T: int, d: int, f: int, n: int, k: int, dtype) -> int:
+    code = dtype if isinstance(dtype, int) else dtype_code(dtype)
+    return int(_native.lib().moe_backward_workspace_size(T, d, f, n, k, code))
+
+
+def backward_workspace(T: int, d: int, f: int, n: int, k: int, dtype=torch.bfloat16,
+                       device="cuda") -> torch.Tensor:
+    """A zeroed workspace of moe_backward_workspace_size bytes."""
+    size = moe_backward_workspace_size(T, d, f, n, k, dtype)
+    if size == 0:
+        raise ValueError("invalid or unsupported sizes")
+    return torch.zeros(size, dtype=torch.uint8, device=device)
+
+
+def moe_layer_backward(x: torch.Tensor, w_gate: torch.Tensor, w1: torch.Tensor, w3: torch.Tensor,
+                       w2: torch.Tensor, k: int, dy: torch.Tensor, ws: torch.Tensor, *,
+                       logit_bias: Optional[torch.Tensor] = None, want_dbias: bool = False,
+                       dx: Optional[torch.Tensor] = None, dw_gate: Optional[torch.Tensor] = None,
+                       dw1: Optional[torch.Tensor] = None, dw3: Optional[torch.Tensor] = None,
+                       dw2: Optional[torch.Tensor] = None,
+                       dlogit_bias: Optional[torch.Tensor] = None, stream=None):
+    """Gradients of <dy, MoE(x)>: returns dict dx, dw_gate, dw1, dw3, dw2 (and dlogit_bias)."""
+    T, d = x.shape
+    n, f, _ = w1.shape
+    dev = x.device
+    dx = torch.empty_like(x) if dx is None else dx
+    dw_gate = torch.empty((d, n), dtype=torch.float32, device=dev) if dw_gate is None else dw_gate
+    dw1 = torch.empty_like(w1) if dw1 is None else dw1
+    dw3 = torch.empty_like(w3) if dw3 is None else dw3
+    dw2 = torch.empty_like(w2) if dw2 is None else dw2
+    if want_dbias and dlogit_bias is None:
+        dlogit_bias = torch.empty(n, dtype=torch.float32, device=dev)
+    st = _native.lib().moe_layer_backward(
+        _ptr(x), _ptr(w_gate), _ptr(logit_bias), _ptr(w1), _ptr(w3), _ptr(w2), _ptr(dy), T, d, f,
+        n, k, dtype_code(x.dtype), _ptr(dx), _ptr(dw_gate), _ptr(dlogit_bias), _ptr(dw1),
+        _ptr(dw3), _ptr(dw2), _ptr(ws), ws.numel(), _stream(stream))
+    check("moe_layer_backward", st)
+    out = {"dx": dx, "dw_gate": dw_gate, "dw1": dw1, "dw3": dw3, "dw2": dw2}
+    if dlogit_bias is not None:
+        out["dlogit_bias"] = dlogit_bias
+    return out

@@ -43,6 +43,9 @@ SIGNATURES = {
     "moe_layer_forward": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P,
                                _SZ, _P]),
     "moe_routing_stats": (_I, [_P, _I, _I, _I, _I, _P, _P, _P]),
+    "moe_backward_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
+    "moe_layer_backward": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P,
+                                _P, _P, _P, _SZ, _P]),
     "moe_check_device_error": (_I, [_P, _SZ, _P]),
     "moe_set_wait_limit_ns": (None, [ctypes.c_ulonglong]),
     "moe_set_tc_form": (_I, [_I]),

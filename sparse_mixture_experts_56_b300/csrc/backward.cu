@@ -1,0 +1,247 @@
+// Backward of the layer y = sum_k G_k E_{e_k}(x), G = Softmax(TopK(x W_g + b)) ("Mixtral of
+// Experts" (xyznot.com summary), Método, eqs. G and y; blog.csdn.net MOE数学公式 §2): the
+// chain rule through the definitions, for L = <dy, y>.  TopK is piecewise constant, so only
+// the kept logits receive gradient; the softmax over them gives
+//     dl_k = G_k (dG_k - sum_j G_j dG_j),   dG_k = <dy, E_{e_k}(x)> = <w2ᵀ dy, h_k>.
+// The experts' part runs on the tensor cores (grouped_tc.cu) in an expert-padded row layout:
+// expert e's rows occupy [poff[e], poff[e+1]), a multiple of 128 rows, the padding rows being
+// zero, so that no 128-row tile and no 64-row reduction block spans two experts.  This file
+// holds the steps around those GEMMs:
+//   pad_offsets   poff from the grouping's offsets
+//   gather_bwd    x_pad, g_pad (rows of x and dy in padded expert order) and each row's gate G
+//   router_bwd    per token: dG_k (sum of the GEMM epilogue's partial dot products, fixed
+//                 order), dl over the kept experts, dx = sum_k dx_pad[q_k] + dl W_gᵀ
+//   dwg_partial / dwg_reduce   dW_g = xᵀ dl and d(bias) = sum_t dl_t, in fixed order
+#include "moe_internal.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kRowAlign = 128;
+constexpr int kDwgChunk = 256;   // tokens per partial sum of dW_g
+
+__global__ void pad_offsets_kernel(const int32_t* __restrict__ off, int n,
+                                   int32_t* __restrict__ poff) {
+  if (threadIdx.x == 0 && blockIdx.x == 0) {
+    int acc = 0;
+    for (int e = 0; e < n; ++e) {
+      poff[e] = acc;
+      const int m = off[e + 1] - off[e];
+      acc += (m + kRowAlign - 1) / kRowAlign * kRowAlign;
+    }
+    poff[n] = acc;
+  }
+}
+
+// One block per padded row q (grid-stride).  Rows past poff[n] are left alone.
+__global__ void __launch_bounds__(256) gather_bwd_kernel(
+    const uint4* __restrict__ x, const uint4* __restrict__ dy, const int32_t* __restrict__ off,
+    const int32_t* __restrict__ poff, const int32_t* __restrict__ perm,
+    const float* __restrict__ topk_w, int n, int k, int rows_max, int row_vecs,
+    uint4* __restrict__ x_pad, uint4* __restrict__ g_pad, float* __restrict__ wq) {
+  __shared__ int s_poff[kMaxExperts + 1], s_off[kMaxExperts + 1];
+  for (int i = threadIdx.x; i <= n; i += blockDim.x) {
+    s_poff[i] = poff[i];
+    s_off[i] = off[i];
+  }
+  __syncthreads();
+  for (int q = blockIdx.x; q < rows_max && q < s_poff[n]; q += gridDim.x) {
+    int e = 0;
+    while (e + 1 < n && s_poff[e + 1] <= q) ++e;
+    const int j = q - s_poff[e];
+    uint4* xd = x_pad + (size_t)q * row_vecs;
+    uint4* gd = g_pad + (size_t)q * row_vecs;
+    if (j < s_off[e + 1] - s_off[e]) {
+      const int a = __ldg(perm + s_off[e] + j);
+      const int t = a / k;
+      if (threadIdx.x == 0) wq[q] = __ldg(topk_w + a);
+      const uint4* xs = x + (size_t)t * row_vecs;
+      const uint4* gs = dy + (size_t)t * row_vecs;
+      for (int c = threadIdx.x; c < row_vecs; c += blockDim.x) {
+        xd[c] = __ldg(xs + c);
+        gd[c] = __ldg(gs + c);
+      }
+    } else {
+      if (threadIdx.x == 0) wq[q] = 0.f;
+      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+      for (int c = threadIdx.x; c < row_vecs; c += blockDim.x) {
+        xd[c] = z;
+        gd[c] = z;
+      }
+    }
+  }
+}
+
+// One warp per token.  dx[t] = sum_k dx_pad[q_k] + sum_k dl_k W_g[:, e_k]; dl [T, n] holds
+// the logit gradient (zero outside the kept experts) for the dW_g reduction.
+template <int KMAX>
+__global__ void __launch_bounds__(256) router_bwd_kernel(
+    const int32_t* __restrict__ idx, const float* __restrict__ topk_w,
+    const int32_t* __restrict__ off, const int32_t* __restrict__ poff,
+    const int32_t* __restrict__ inv_perm, const float* __restrict__ dwp, int ntiles,
+    const bf16* __restrict__ dx_pad, const bf16* __restrict__ wg, int T, int d, int n, int k,
+    bf16* __restrict__ dx, float* __restrict__ dl) {
+  const int lane = threadIdx.x & 31;
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += warps) {
+    int es[KMAX], qs[KMAX];
+    float gate[KMAX], dG[KMAX];
+    float sdot = 0.f;
+#pragma unroll
+    for (int s = 0; s < KMAX; ++s) {
+      if (s < k) {
+        const int a = t * k + s;
+        const int e = __ldg(idx + a);
+        es[s] = e;
+        qs[s] = __ldg(poff + e) + (__ldg(inv_perm + a) - __ldg(off + e));
+        gate[s] = __ldg(topk_w + a);
+        // sum of the column-tile partials of <dw2ᵀ dy, h>: lane-strided, then a fixed tree
+        float v = 0.f;
+        for (int j = lane; j < ntiles; j += 32) v += __ldg(dwp + (size_t)qs[s] * ntiles + j);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        dG[s] = v;
+        sdot = fmaf(gate[s], v, sdot);
+      }
+    }
+    float dls[KMAX];
+#pragma unroll
+    for (int s = 0; s < KMAX; ++s)
+      if (s < k) dls[s] = gate[s] * (dG[s] - sdot);
+    // logit gradient row (zeros outside the kept experts)
+    for (int e = lane; e < n; e += 32) {
+      float v = 0.f;
+#pragma unroll
+      for (int s = 0; s < KMAX; ++s)
+        if (s < k && es[s] == e) v = dls[s];
+      dl[(size_t)t * n + e] = v;
+    }
+    // dx row, 8 columns per lane and step
+    for (int c0 = lane * 8; c0 < d; c0 += 256) {
+      float acc[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+#pragma unroll
+      for (int s = 0; s < KMAX; ++s) {
+        if (s < k) {
+          const uint4 u = __ldg(reinterpret_cast<const uint4*>(dx_pad + (size_t)qs[s] * d + c0));
+          const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float2 f2 = __bfloat1622float2(p[j]);
+            acc[2 * j] += f2.x;
+            acc[2 * j + 1] += f2.y;
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            acc[j] = fmaf(dls[s], __bfloat162float(wg[(size_t)(c0 + j) * n + es[s]]), acc[j]);
+        }
+      }
+      uint4 o;
+      __nv_bfloat162* op = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) op[j] = __floats2bfloat162_rn(acc[2 * j], acc[2 * j + 1]);
+      *reinterpret_cast<uint4*>(dx + (size_t)t * d + c0) = o;
+    }
+  }
+}
+
+// part[c][i][e] = sum over the tokens of chunk c of x[t, i] dl[t, e]; column i == d stands
+// for the logit bias (x = 1).  Block: 256 columns x one chunk of tokens.
+__global__ void __launch_bounds__(256) dwg_partial_kernel(const bf16* __restrict__ x,
+                                                          const float* __restrict__ dl, int T,
+                                                          int d, int n,
+                                                          float* __restrict__ part) {
+  __shared__ float s_dl[kDwgChunk * kMaxExperts];
+  const int c = blockIdx.y;
+  const int t0 = c * kDwgChunk;
+  const int tn = min(kDwgChunk, T - t0);
+  for (int i = threadIdx.x; i < tn * n; i += blockDim.x) s_dl[i] = dl[(size_t)t0 * n + i];
+  __syncthreads();
+  const int col = blockIdx.x * blockDim.x + threadIdx.x;
+  if (col > d) return;
+  float acc[kMaxExperts];
+  for (int e = 0; e < n; ++e) acc[e] = 0.f;
+  for (int tt = 0; tt < tn; ++tt) {
+    const float xv = col < d ? __bfloat162float(x[(size_t)(t0 + tt) * d + col]) : 1.0f;
+    for (int e = 0; e < n; ++e) acc[e] = fmaf(xv, s_dl[tt * n + e], acc[e]);
+  }
+  float* out = part + ((size_t)c * (d + 1) + col) * n;
+  for (int e = 0; e < n; ++e) out[e] = acc[e];
+}
+
+__global__ void __launch_bounds__(256) dwg_reduce_kernel(const float* __restrict__ part,
+                                                         int chunks, int d, int n,
+                                                         float* __restrict__ dwg,
+                                                         float* __restrict__ dbias) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;   // flat (column, expert)
+  if (i >= (d + 1) * n) return;
+  float v = 0.f;
+  for (int c = 0; c < chunks; ++c) v += part[(size_t)c * (d + 1) * n + i];
+  if (i < d * n)
+    dwg[i] = v;
+  else if (dbias)
+    dbias[i - d * n] = v;
+}
+
+}  // namespace
+
+int bwd_rows_max(long long A, int n) {
+  const long long r = A + (long long)(kRowAlign - 1) * n;
+  return (int)((r + kRowAlign - 1) / kRowAlign * kRowAlign);
+}
+
+int bwd_dwg_chunks(int T) { return (T + kDwgChunk - 1) / kDwgChunk; }
+
+cudaError_t launch_pad_offsets(const int32_t* off, int n, int32_t* poff, cudaStream_t s) {
+  pad_offsets_kernel<<<1, 32, 0, s>>>(off, n, poff);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_bwd(const bf16* x, const bf16* dy, const int32_t* off,
+                              const int32_t* poff, const int32_t* perm, const float* topk_w,
+                              int n, int k, int rows_max, int d, bf16* x_pad, bf16* g_pad,
+                              float* wq, cudaStream_t s) {
+  if (rows_max == 0) return cudaSuccess;
+  const int cap = device_sm_count() * 8;
+  gather_bwd_kernel<<<rows_max < cap ? rows_max : cap, 256, 0, s>>>(
+      (const uint4*)x, (const uint4*)dy, off, poff, perm, topk_w, n, k, rows_max, d / 8,
+      (uint4*)x_pad, (uint4*)g_pad, wq);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_router_bwd(const int32_t* idx, const float* topk_w, const int32_t* off,
+                              const int32_t* poff, const int32_t* inv_perm, const float* dwp,
+                              int ntiles, const bf16* dx_pad, const bf16* wg, int T, int d, int n,
+                              int k, bf16* dx, float* dl, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  const long long blocks = ((long long)T + 7) / 8;
+  const long long cap = (long long)device_sm_count() * 16;
+  const int grid = (int)(blocks < cap ? blocks : cap);
+  if (k <= 2)
+    router_bwd_kernel<2><<<grid, 256, 0, s>>>(idx, topk_w, off, poff, inv_perm, dwp, ntiles,
+                                              dx_pad, wg, T, d, n, k, dx, dl);
+  else if (k <= 8)
+    router_bwd_kernel<8><<<grid, 256, 0, s>>>(idx, topk_w, off, poff, inv_perm, dwp, ntiles,
+                                              dx_pad, wg, T, d, n, k, dx, dl);
+  else
+    router_bwd_kernel<kMaxExperts><<<grid, 256, 0, s>>>(idx, topk_w, off, poff, inv_perm, dwp,
+                                                        ntiles, dx_pad, wg, T, d, n, k, dx, dl);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dwg(const bf16* x, const float* dl, int T, int d, int n, float* part,
+                       float* dwg, float* dbias, cudaStream_t s) {
+  const int chunks = bwd_dwg_chunks(T);
+  if (chunks > 0) {
+    dim3 grid((d + 1 + 255) / 256, chunks);
+    dwg_partial_kernel<<<grid, 256, 0, s>>>(x, dl, T, d, n, part);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  const int outs = (d + 1) * n;
+  dwg_reduce_kernel<<<(outs + 255) / 256, 256, 0, s>>>(part, chunks, d, n, dwg, dbias);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

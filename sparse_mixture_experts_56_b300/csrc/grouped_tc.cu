@@ -55,7 +55,21 @@ constexpr int GROUP_M = 16;
 constexpr uint64_t kDrainNs = 200ull * 1000 * 1000;
 constexpr uint64_t kPeerGraceNs = 1000ull * 1000;
 
-enum Mode { kSwiGLU = 0, kDown = 1 };
+// Forward:  kSwiGLU  h = SiLU(x w1ᵀ) ⊙ (x w3ᵀ)          A = x rows,  B = w1|w3 (K-major)
+//           kDown    y_perm = h w2ᵀ                     A = h rows,  B = w2 (K-major)
+// Backward (rows in the expert-padded layout, every expert's segment a multiple of 128 rows):
+//           kStoreAB [a | b] = x [w1 | w3]ᵀ, stored      A = x rows,  B = w1|w3 (K-major)
+//           kDh      dh' = g w2 (g = dL/dy rows); the epilogue forms h, the gate gradient
+//                    partial <dh', h>, and the gate-scaled da, db, G·h
+//                                                        A = g rows,  B = w2 (MN-major)
+//           kDgradX  dx = da w1 + db w3                  A = da|db,   B = w1|w3 (MN-major)
+//           kWgrad   dW = Pᵀ Q over an expert's rows     A = P, B = Q (both MN-major)
+enum Mode { kSwiGLU = 0, kDown = 1, kStoreAB = 2, kDh = 3, kDgradX = 4, kWgrad = 5 };
+
+// Which operands sit in shared memory MN-major (the contiguous global dimension is M or N
+// rather than the reduction dimension K).
+constexpr bool a_mn(int mode) { return mode == kWgrad; }
+constexpr bool b_mn(int mode) { return mode == kDh || mode == kDgradX || mode == kWgrad; }
 
 // Geometry of the two forms.
 template <bool PAIR>
@@ -67,23 +81,38 @@ struct Cfg {
   static constexpr uint32_t kABytes = BM * BK * 2;
   static constexpr uint32_t kBBytes = kBRows * BK * 2;
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;
-  // instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A bf16 (7-9 = 1), B bf16
-  // (10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 at bits 17-22, M >> 4 at bits 24-28
-  // (M of the whole CTA pair in the pair form).
-  static constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
-                                     ((uint32_t)(BN >> 3) << 17) |
-                                     ((uint32_t)(kTileM >> 4) << 24);
 };
 
+// Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A bf16 (7-9 = 1), B bf16 (10-12 =
+// 1), A / B MN-major (bit 15 / 16), N >> 3 at bits 17-22, M >> 4 at bits 24-28 (M of the whole
+// CTA pair in the pair form).
+template <int MODE, bool PAIR>
+constexpr uint32_t instr_desc() {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn(MODE) ? 1u : 0u) << 15) |
+         ((b_mn(MODE) ? 1u : 0u) << 16) | ((uint32_t)(BN >> 3) << 17) |
+         ((uint32_t)(Cfg<PAIR>::kTileM >> 4) << 24);
+}
+
 struct TcArgs {
-  const int32_t* offsets;
+  const int32_t* offsets;  // rows of each expert: [offsets[e], offsets[e+1])
   int n;
-  int kdim;   // reduction length: d (GEMM1) or f (GEMM2)
-  int ndim;   // output columns: f (GEMM1) or d (GEMM2)
+  int kdim;   // reduction length (not used by kWgrad, whose K is the expert's row count)
+  int ndim;   // output columns
   int ntiles; // n-tiles per expert
-  bf16* out;  // [A, ndim]
+  bf16* out;  // main output
   uint32_t* status;
   unsigned long long wait_ns;
+  // backward only
+  int brows;          // kDh / kDgradX: rows of one expert's B matrix in its 2-D view (d or f)
+  int kb_split;       // kDgradX: k-blocks taken from (da, w1) before switching to (db, w3)
+  int mdim;           // kWgrad: rows of the weight gradient (M)
+  int mtiles_w;       // kWgrad: 128-row tiles of M
+  const bf16* ab;     // kDh: [rows, 2 ndim] recomputed a | b
+  const float* wq;    // kDh: gate weight of every row (0 on padding rows)
+  float* dwp;         // kDh: [rows, ntiles] partial sums of <dh', h>
+  bf16* da;           // kDh outputs [rows, ndim]
+  bf16* db;
+  bf16* hw;
 };
 
 template <int STAGES>
@@ -190,20 +219,36 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   return (uint64_t)((saddr & 0x3FFFFu) >> 4) | (1ull << 16) | ((uint64_t)(1024 >> 4) << 32) |
          (1ull << 46) | (2ull << 61);
 }
-template <bool PAIR>
+// MN-major, 128-byte swizzle: each TMA box is 64 K-rows of 64 contiguous M/N elements (8 KB);
+// boxes for successive 64-element M/N chunks sit 8 KB apart (leading byte offset), 8-row K
+// groups 1024 bytes apart (stride byte offset).
+constexpr uint32_t kMnChunkBytes = 64 * 64 * 2;
+__device__ __forceinline__ uint64_t sw128_mn_desc(uint32_t saddr) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)(kMnChunkBytes >> 4) << 16) |
+         ((uint64_t)(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61);
+}
+// Descriptor of the 16-deep K slice kk of an operand tile at `base`.
+template <bool MN>
+__device__ __forceinline__ uint64_t slice_desc(uint32_t base, int kk) {
+  if constexpr (MN)
+    return sw128_mn_desc(base + (uint32_t)kk * 16 * 128);   // 16 K-rows of 128 bytes
+  else
+    return sw128_desc(base + (uint32_t)kk * UMMA_K * 2);     // 32 bytes along the swizzled row
+}
+template <int MODE, bool PAIR>
 __device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
                                           uint32_t accumulate) {
   if constexpr (PAIR)
     asm volatile(
         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
         " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
-        "l"(adesc), "l"(bdesc), "r"(Cfg<true>::kIdesc), "r"(accumulate)
+        "l"(adesc), "l"(bdesc), "r"(instr_desc<MODE, true>()), "r"(accumulate)
         : "memory");
   else
     asm volatile(
         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
         " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
-        "l"(adesc), "l"(bdesc), "r"(Cfg<false>::kIdesc), "r"(accumulate)
+        "l"(adesc), "l"(bdesc), "r"(instr_desc<MODE, false>()), "r"(accumulate)
         : "memory");
 }
 // Arrives on `bar` once the MMAs issued so far by this thread are done: in the pair form on
@@ -324,10 +369,12 @@ __device__ __noinline__ void spin_ns(uint64_t ns) {
 }
 
 struct Tile {
-  int e, mt, nt, row0, rows;
+  int e, mt, nt;
+  int row0;   // first A row (token-row modes) / first K row of the expert (kWgrad)
+  int rows;   // valid rows of the tile (token-row modes) / K rows of the expert (kWgrad)
 };
 
-template <int TILE_M>
+template <int MODE, int TILE_M>
 __device__ __forceinline__ Tile decode_tile(const int* tile_base, const int* mtiles,
                                             const int* off, int n, int ntiles, int tile) {
   int e = 0;
@@ -340,8 +387,13 @@ __device__ __forceinline__ Tile decode_tile(const int* tile_base, const int* mti
   t.e = e;
   t.mt = g * GROUP_M + r % gsz;
   t.nt = r / gsz;
-  t.row0 = off[e] + t.mt * TILE_M;
-  t.rows = min(TILE_M, off[e + 1] - off[e] - t.mt * TILE_M);
+  if (MODE == kWgrad) {
+    t.row0 = off[e];
+    t.rows = off[e + 1] - off[e];
+  } else {
+    t.row0 = off[e] + t.mt * TILE_M;
+    t.rows = min(TILE_M, off[e + 1] - off[e] - t.mt * TILE_M);
+  }
   return t;
 }
 
@@ -363,16 +415,35 @@ __device__ __forceinline__ void store_row32(bf16* dst, const float (&v)[32]) {
   }
 }
 
+__device__ __forceinline__ void load_row32(const bf16* src, float (&v)[32]) {
+  const uint4* q = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint4 u = __ldg(q + j);
+    const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __bfloat1622float2(p[i]);
+      v[8 * j + 2 * i] = f.x;
+      v[8 * j + 2 * i + 1] = f.y;
+    }
+  }
+}
+
+__device__ __forceinline__ float sigmoidf_(float z) { return 1.0f / (1.0f + __expf(-z)); }
+
 // ------------------------------------------------------------------------------------------
 // the kernel
 // ------------------------------------------------------------------------------------------
 template <int MODE, bool PAIR>
 __global__ void __launch_bounds__(256, 1)
     grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
+                           const __grid_constant__ CUtensorMap tmA2,
                            const __grid_constant__ CUtensorMap tmB0,
                            const __grid_constant__ CUtensorMap tmB1, const TcArgs args) {
   using C = Cfg<PAIR>;
   constexpr int STAGES = C::kStages;
+  static_assert(!PAIR || MODE == kSwiGLU || MODE == kDown, "the pair form serves the forward");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -392,7 +463,7 @@ __global__ void __launch_bounds__(256, 1)
     int acc = 0;
     for (int e = 0; e < n; ++e) {
       const int o0 = args.offsets[e], o1 = args.offsets[e + 1];
-      const int mt = (o1 - o0 + C::kTileM - 1) / C::kTileM;
+      const int mt = MODE == kWgrad ? args.mtiles_w : (o1 - o0 + C::kTileM - 1) / C::kTileM;
       sh.off[e] = o0;
       sh.mtiles[e] = mt;
       sh.tile_base[e] = acc;
@@ -435,21 +506,24 @@ __global__ void __launch_bounds__(256, 1)
   if (warp == 0 && lane == 0) {
     // ---------------------------------------------------------------- TMA producer
     prefetch_map(&tmA);
+    if (MODE == kDgradX) prefetch_map(&tmA2);
     prefetch_map(&tmB0);
-    if (MODE == kSwiGLU) prefetch_map(&tmB1);
+    if (MODE == kSwiGLU || MODE == kStoreAB || MODE == kDgradX) prefetch_map(&tmB1);
     int stage = 0;
     uint32_t phase = 0, issued = 0, iphase = 0;
     bool ok = true;
     for (int tile = first_tile; ok && tile < total; tile += gstride) {
-      const Tile t = decode_tile<C::kTileM>(sh.tile_base, sh.mtiles, sh.off, n, args.ntiles, tile);
+      const Tile t =
+          decode_tile<MODE, C::kTileM>(sh.tile_base, sh.mtiles, sh.off, n, args.ntiles, tile);
       const int arow = t.row0 + (int)rank * BM;
       // first B row of this CTA's share: GEMM1 takes 128 rows of w1 (and of w3), GEMM2 256
       // rows of w2, split between the two CTAs of a pair
-      const int brow = MODE == kSwiGLU
+      const int brow = (MODE == kSwiGLU || MODE == kStoreAB)
                            ? t.e * args.ndim + t.nt * (BN / 2)
                            : t.e * args.ndim + t.nt * BN + (int)rank * C::kBRows;
       const CUtensorMap* bmap = (MODE == kSwiGLU && PAIR && rank == 1) ? &tmB1 : &tmB0;
-      for (int kb = 0; kb < KB; ++kb) {
+      const int kbs = MODE == kWgrad ? t.rows / BK : KB;
+      for (int kb = 0; kb < kbs; ++kb) {
         if (!wait_phase(smem_u32(&sh.empty[stage]), phase ^ 1u, abort, limit)) {
           raise_abort(abort, args.status);
           ok = false;
@@ -466,10 +540,39 @@ __global__ void __launch_bounds__(256, 1)
           tma_load_2d_pair(b_dst, bmap, fb0, kb * BK, brow);
         } else {
           mbar_expect_tx(fb, C::kStageBytes);
-          tma_load_2d(a_dst, &tmA, fb, kb * BK, arow);
-          tma_load_2d(b_dst, &tmB0, fb, kb * BK, brow);
-          if (MODE == kSwiGLU)
-            tma_load_2d(b_dst + C::kBBytes / 2, &tmB1, fb, kb * BK, brow);
+          // A: 128 rows x 64 K (K-major), or for kWgrad 64 K-rows x 2 chunks of 64 M columns
+          if constexpr (MODE == kWgrad) {
+            tma_load_2d(a_dst, &tmA, fb, t.mt * BM, t.row0 + kb * BK);
+            tma_load_2d(a_dst + kMnChunkBytes, &tmA, fb, t.mt * BM + 64, t.row0 + kb * BK);
+          } else if constexpr (MODE == kDgradX) {
+            if (kb < args.kb_split)
+              tma_load_2d(a_dst, &tmA, fb, kb * BK, arow);
+            else
+              tma_load_2d(a_dst, &tmA2, fb, (kb - args.kb_split) * BK, arow);
+          } else {
+            tma_load_2d(a_dst, &tmA, fb, kb * BK, arow);
+          }
+          // B: K-major rows, or MN-major 64 K-rows x 4 chunks of 64 N columns
+          if constexpr (b_mn(MODE)) {
+            const CUtensorMap* bm = &tmB0;
+            int krow;
+            if constexpr (MODE == kWgrad) {
+              krow = t.row0 + kb * BK;
+            } else if constexpr (MODE == kDgradX) {
+              const bool second = kb >= args.kb_split;
+              bm = second ? &tmB1 : &tmB0;
+              krow = t.e * args.brows + (second ? kb - args.kb_split : kb) * BK;
+            } else {
+              krow = t.e * args.brows + kb * BK;
+            }
+#pragma unroll
+            for (int i = 0; i < BN / 64; ++i)
+              tma_load_2d(b_dst + i * kMnChunkBytes, bm, fb, t.nt * BN + 64 * i, krow);
+          } else {
+            tma_load_2d(b_dst, &tmB0, fb, kb * BK, brow);
+            if (MODE == kSwiGLU || MODE == kStoreAB)
+              tma_load_2d(b_dst + C::kBBytes / 2, &tmB1, fb, kb * BK, brow);
+          }
         }
         issued |= 1u << stage;
         iphase = (iphase & ~(1u << stage)) | (phase << stage);
@@ -496,13 +599,19 @@ __global__ void __launch_bounds__(256, 1)
     uint32_t phase = 0, acc_phase = 0;
     bool ok = true, any_mma = false;
     for (int tile = first_tile; ok && tile < total; tile += gstride) {
+      int kbs = KB;
+      if (MODE == kWgrad) {
+        const Tile t =
+            decode_tile<MODE, C::kTileM>(sh.tile_base, sh.mtiles, sh.off, n, args.ntiles, tile);
+        kbs = t.rows / BK;
+      }
       if (!wait_phase(smem_u32(&sh.tempty[acc]), acc_phase ^ 1u, abort, limit)) {
         raise_abort(abort, args.status);
         break;
       }
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-      for (int kb = 0; kb < KB; ++kb) {
+      for (int kb = 0; kb < kbs; ++kb) {
         if (!wait_phase(smem_u32(&sh.full[stage]), phase, abort, limit)) {
           raise_abort(abort, args.status);
           ok = false;
@@ -513,8 +622,8 @@ __global__ void __launch_bounds__(256, 1)
         const uint32_t b0 = smem_u32(sB + stage * C::kBBytes);
 #pragma unroll
         for (int kk = 0; kk < BK / UMMA_K; ++kk)
-          umma_bf16<PAIR>(d_tmem, sw128_desc(a0 + kk * UMMA_K * 2),
-                          sw128_desc(b0 + kk * UMMA_K * 2), (kb | kk) != 0 ? 1u : 0u);
+          umma_bf16<MODE, PAIR>(d_tmem, slice_desc<a_mn(MODE)>(a0, kk),
+                                slice_desc<b_mn(MODE)>(b0, kk), (kb | kk) != 0 ? 1u : 0u);
         any_mma = true;
         umma_commit_all<PAIR>(smem_u32(&sh.empty[stage]));
         if (++stage == STAGES) {
@@ -523,6 +632,8 @@ __global__ void __launch_bounds__(256, 1)
         }
       }
       if (!ok) break;
+      // (a weight-gradient tile of an expert without rows has no MMA: the commit still
+      // arrives, and the epilogue writes zeros)
       umma_commit_all<PAIR>(smem_u32(&sh.tfull[acc]));
       if (++acc == ACC) {
         acc = 0;
@@ -541,7 +652,8 @@ __global__ void __launch_bounds__(256, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = first_tile; tile < total; tile += gstride) {
-      const Tile t = decode_tile<C::kTileM>(sh.tile_base, sh.mtiles, sh.off, n, args.ntiles, tile);
+      const Tile t =
+          decode_tile<MODE, C::kTileM>(sh.tile_base, sh.mtiles, sh.off, n, args.ntiles, tile);
       int ok = 1;
       if (lane == 0) {
         ok = wait_phase(smem_u32(&sh.tfull[acc]), acc_phase, abort, limit) ? 1 : 0;
@@ -551,14 +663,24 @@ __global__ void __launch_bounds__(256, 1)
       if (!ok) break;
       tc_fence_after();
       const int row = (int)rank * BM + r;   // row of the tile held in this TMEM lane
-      const bool row_ok = row < t.rows;
+      const bool row_ok = MODE == kWgrad ? t.mt * BM + r < args.mdim : row < t.rows;
       const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
       const uint32_t tempty_local = smem_u32(&sh.tempty[acc]);
       // the even CTA's MMA issuer waits for the epilogue warps of both CTAs
       const uint32_t tempty = PAIR ? peer_addr(tempty_local, 0) : tempty_local;
-      if (MODE == kSwiGLU) {
+      auto release_acc = [&]() {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (PAIR)
+            mbar_arrive_cluster(tempty);
+          else
+            mbar_arrive(tempty);
+        }
+      };
+      if constexpr (MODE == kSwiGLU || MODE == kStoreAB) {
         const int col0 = t.nt * (BN / 2);
-        bf16* orow = args.out + (size_t)(t.row0 + row) * args.ndim + col0;
+        const size_t grow = (size_t)(t.row0 + row);
 #pragma unroll 1
         for (int c = 0; c < BN / 64; ++c) {
           uint32_t a[32], b[32];
@@ -566,49 +688,85 @@ __global__ void __launch_bounds__(256, 1)
           tmem_ld32(tb + BN / 2 + c * 32, b);
           tmem_wait(a);
           tmem_wait(b);
-          if (c == BN / 64 - 1) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-              if (PAIR)
-                mbar_arrive_cluster(tempty);
-              else
-                mbar_arrive(tempty);
-            }
-          }
+          if (c == BN / 64 - 1) release_acc();
           if (row_ok && col0 + c * 32 < args.ndim) {
             float v[32];
+            if constexpr (MODE == kSwiGLU) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const float av = __uint_as_float(a[j]);
-              const float bv = __uint_as_float(b[j]);
-              v[j] = av / (1.0f + __expf(-av)) * bv;
+              for (int j = 0; j < 32; ++j) {
+                const float av = __uint_as_float(a[j]);
+                const float bv = __uint_as_float(b[j]);
+                v[j] = av / (1.0f + __expf(-av)) * bv;
+              }
+              store_row32(args.out + grow * args.ndim + col0 + c * 32, v);
+            } else {
+              // [a | b] row of 2 * ndim columns
+              bf16* o = args.out + grow * 2 * args.ndim + col0 + c * 32;
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(a[j]);
+              store_row32(o, v);
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(b[j]);
+              store_row32(o + args.ndim, v);
             }
-            store_row32(orow + c * 32, v);
           }
         }
-      } else {
+      } else if constexpr (MODE == kDh) {
+        // dh' = g w2 for 256 columns of f; with the recomputed a, b of the same columns:
+        //   h = SiLU(a) b,  partial <dh', h>,  da = G dh' b SiLU'(a),  db = G dh' SiLU(a),
+        //   hw = G h  (G = this row's gate weight, 0 on padding rows)
         const int col0 = t.nt * BN;
-        bf16* orow = args.out + (size_t)(t.row0 + row) * args.ndim + col0;
+        const size_t grow = (size_t)(t.row0 + row);
+        const float gate = args.wq[grow];
+        float dot = 0.f;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t dr[32];
+          tmem_ld32(tb + c * 32, dr);
+          tmem_wait(dr);
+          if (c == BN / 32 - 1) release_acc();
+          const int col = col0 + c * 32;
+          if (row_ok && col < args.ndim) {
+            float av[32], bv[32], o1[32], o2[32];
+            load_row32(args.ab + grow * 2 * args.ndim + col, av);
+            load_row32(args.ab + grow * 2 * args.ndim + args.ndim + col, bv);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const float dh = __uint_as_float(dr[j]);
+              const float sg = sigmoidf_(av[j]);
+              const float si = av[j] * sg;
+              const float h = si * bv[j];
+              dot = fmaf(dh, h, dot);
+              o1[j] = gate * dh * bv[j] * sg * (1.0f + av[j] * (1.0f - sg));
+              o2[j] = gate * dh * si;
+              bv[j] = gate * h;
+            }
+            const size_t oo = grow * args.ndim + col;
+            store_row32(args.da + oo, o1);
+            store_row32(args.db + oo, o2);
+            store_row32(args.hw + oo, bv);
+          }
+        }
+        if (row_ok) args.dwp[grow * args.ntiles + t.nt] = dot;
+      } else {
+        // kDown, kDgradX: rows of the tile; kWgrad: rows t.mt*128.. of expert e's gradient
+        const int col0 = t.nt * BN;
+        bf16* orow;
+        if constexpr (MODE == kWgrad)
+          orow = args.out + ((size_t)t.e * args.mdim + (size_t)(t.mt * BM + r)) * args.ndim + col0;
+        else
+          orow = args.out + (size_t)(t.row0 + row) * args.ndim + col0;
+        const bool empty_k = MODE == kWgrad && t.rows == 0;
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           uint32_t a[32];
           tmem_ld32(tb + c * 32, a);
           tmem_wait(a);
-          if (c == BN / 32 - 1) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-              if (PAIR)
-                mbar_arrive_cluster(tempty);
-              else
-                mbar_arrive(tempty);
-            }
-          }
+          if (c == BN / 32 - 1) release_acc();
           if (row_ok && col0 + c * 32 < args.ndim) {
             float v[32];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(a[j]);
+            for (int j = 0; j < 32; ++j) v[j] = empty_k ? 0.f : __uint_as_float(a[j]);
             store_row32(orow + c * 32, v);
           }
         }
@@ -729,10 +887,22 @@ inline bool want_pair(int A, int n) {
   return MODE == kDown && (long long)A >= 256ll * n;
 }
 
+// Single-CTA launch over at most `tiles` tiles.
+template <int MODE>
+cudaError_t launch_single(const CUtensorMap& mA, const CUtensorMap& mA2, const CUtensorMap& mB0,
+                          const CUtensorMap& mB1, const TcArgs& a, long long tiles,
+                          cudaStream_t s) {
+  cudaError_t e = set_smem_attr<MODE, false>();
+  if (e != cudaSuccess) return e;
+  const int sms = device_sm_count();
+  const int grid = (int)(tiles < sms ? (tiles > 0 ? tiles : 1) : sms);
+  grouped_gemm_tc_kernel<MODE, false><<<grid, 256, smem_bytes<false>(), s>>>(mA, mA2, mB0, mB1, a);
+  return cudaGetLastError();
+}
+
 template <int MODE>
 cudaError_t launch_gemm(const CUtensorMap& mA, const CUtensorMap& mB0, const CUtensorMap& mB1,
                         const TcArgs& a, int A, cudaStream_t s) {
-  const int sms = device_sm_count();
   const int pairs = want_pair<MODE>(A, a.n) ? max_pairs<MODE>() : 0;
   if (pairs > 0) {
     const long long tiles = ((long long)(A + 255) / 256 + a.n) * a.ntiles;
@@ -749,14 +919,10 @@ cudaError_t launch_gemm(const CUtensorMap& mA, const CUtensorMap& mB0, const CUt
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, grouped_gemm_tc_kernel<MODE, true>, mA, mB0, mB1, a);
+    return cudaLaunchKernelEx(&cfg, grouped_gemm_tc_kernel<MODE, true>, mA, mA, mB0, mB1, a);
   }
-  cudaError_t e = set_smem_attr<MODE, false>();
-  if (e != cudaSuccess) return e;
   const long long tiles = ((long long)(A + BM - 1) / BM + a.n) * a.ntiles;
-  grouped_gemm_tc_kernel<MODE, false><<<(int)(tiles < sms ? tiles : sms), 256,
-                                        smem_bytes<false>(), s>>>(mA, mB0, mB1, a);
-  return cudaGetLastError();
+  return launch_single<MODE>(mA, mA, mB0, mB1, a, tiles, s);
 }
 
 }  // namespace
@@ -772,7 +938,7 @@ cudaError_t launch_up_tc(const bf16* x_perm, const int32_t* offsets, const bf16*
       !make_map(&mW1, w1, (uint64_t)n * f, (uint64_t)d, BN / 2) ||
       !make_map(&mW3, w3, (uint64_t)n * f, (uint64_t)d, BN / 2))
     return cudaErrorInvalidValue;
-  TcArgs a;
+  TcArgs a = {};
   a.offsets = offsets;
   a.n = n;
   a.kdim = d;
@@ -794,7 +960,7 @@ cudaError_t launch_down_tc(const bf16* h, const int32_t* offsets, const bf16* w2
   if (!make_map(&mA, h, (uint64_t)A, (uint64_t)f, BM) ||
       !make_map(&mW2, w2, (uint64_t)n * d, (uint64_t)f, brows))
     return cudaErrorInvalidValue;
-  TcArgs a;
+  TcArgs a = {};
   a.offsets = offsets;
   a.n = n;
   a.kdim = f;
@@ -804,6 +970,106 @@ cudaError_t launch_down_tc(const bf16* h, const int32_t* offsets, const bf16* w2
   a.status = status;
   a.wait_ns = wait_ns;
   return launch_gemm<kDown>(mA, mW2, mW2, a, A, s);
+}
+
+// ------------------------------------------------------------------------------------------
+// backward launchers (rows in the expert-padded layout: every expert's segment of
+// `offsets` is a multiple of 128 rows; rows_max bounds the padded row count)
+// ------------------------------------------------------------------------------------------
+int bwd_dh_ntiles(int f) { return (f + BN - 1) / BN; }
+
+cudaError_t launch_bwd_store_ab(const bf16* x_pad, const int32_t* poff, const bf16* w1,
+                                const bf16* w3, int rows_max, int d, int f, int n, bf16* ab,
+                                uint32_t* status, unsigned long long wait_ns, cudaStream_t s) {
+  if (rows_max == 0) return cudaSuccess;
+  CUtensorMap mA, mW1, mW3;
+  if (!make_map(&mA, x_pad, (uint64_t)rows_max, (uint64_t)d, BM) ||
+      !make_map(&mW1, w1, (uint64_t)n * f, (uint64_t)d, BN / 2) ||
+      !make_map(&mW3, w3, (uint64_t)n * f, (uint64_t)d, BN / 2))
+    return cudaErrorInvalidValue;
+  TcArgs a = {};
+  a.offsets = poff;
+  a.n = n;
+  a.kdim = d;
+  a.ndim = f;
+  a.ntiles = (f + BN / 2 - 1) / (BN / 2);
+  a.out = ab;
+  a.status = status;
+  a.wait_ns = wait_ns;
+  return launch_single<kStoreAB>(mA, mA, mW1, mW3, a, (long long)(rows_max / BM) * a.ntiles, s);
+}
+
+cudaError_t launch_bwd_dh(const bf16* g_pad, const int32_t* poff, const bf16* w2, const bf16* ab,
+                          const float* wq, int rows_max, int d, int f, int n, float* dwp, bf16* da,
+                          bf16* db, bf16* hw, uint32_t* status, unsigned long long wait_ns,
+                          cudaStream_t s) {
+  if (rows_max == 0) return cudaSuccess;
+  CUtensorMap mA, mW2;
+  if (!make_map(&mA, g_pad, (uint64_t)rows_max, (uint64_t)d, BM) ||
+      !make_map(&mW2, w2, (uint64_t)n * d, (uint64_t)f, 64))
+    return cudaErrorInvalidValue;
+  TcArgs a = {};
+  a.offsets = poff;
+  a.n = n;
+  a.kdim = d;
+  a.ndim = f;
+  a.ntiles = bwd_dh_ntiles(f);
+  a.brows = d;
+  a.ab = ab;
+  a.wq = wq;
+  a.dwp = dwp;
+  a.da = da;
+  a.db = db;
+  a.hw = hw;
+  a.status = status;
+  a.wait_ns = wait_ns;
+  return launch_single<kDh>(mA, mA, mW2, mW2, a, (long long)(rows_max / BM) * a.ntiles, s);
+}
+
+cudaError_t launch_bwd_dgrad_x(const bf16* da, const bf16* db, const int32_t* poff, const bf16* w1,
+                               const bf16* w3, int rows_max, int d, int f, int n, bf16* dx_pad,
+                               uint32_t* status, unsigned long long wait_ns, cudaStream_t s) {
+  if (rows_max == 0) return cudaSuccess;
+  CUtensorMap mDa, mDb, mW1, mW3;
+  if (!make_map(&mDa, da, (uint64_t)rows_max, (uint64_t)f, BM) ||
+      !make_map(&mDb, db, (uint64_t)rows_max, (uint64_t)f, BM) ||
+      !make_map(&mW1, w1, (uint64_t)n * f, (uint64_t)d, 64) ||
+      !make_map(&mW3, w3, (uint64_t)n * f, (uint64_t)d, 64))
+    return cudaErrorInvalidValue;
+  TcArgs a = {};
+  a.offsets = poff;
+  a.n = n;
+  a.kdim = 2 * f;
+  a.kb_split = f / BK;
+  a.ndim = d;
+  a.ntiles = (d + BN - 1) / BN;
+  a.brows = f;
+  a.out = dx_pad;
+  a.status = status;
+  a.wait_ns = wait_ns;
+  return launch_single<kDgradX>(mDa, mDb, mW1, mW3, a, (long long)(rows_max / BM) * a.ntiles, s);
+}
+
+cudaError_t launch_bwd_wgrad(const bf16* P, const bf16* Q, const int32_t* poff, int rows_max,
+                             int M, int N, int n, bf16* dW, uint32_t* status,
+                             unsigned long long wait_ns, cudaStream_t s) {
+  CUtensorMap mP, mQ;
+  // rows_max >= 1 keeps the maps valid when no expert has rows (every tile then writes zeros)
+  const uint64_t rows = rows_max > 0 ? (uint64_t)rows_max : 1;
+  if (!make_map(&mP, P, rows, (uint64_t)M, 64) || !make_map(&mQ, Q, rows, (uint64_t)N, 64))
+    return cudaErrorInvalidValue;
+  TcArgs a = {};
+  a.offsets = poff;
+  a.n = n;
+  a.kdim = 0;
+  a.mdim = M;
+  a.mtiles_w = (M + BM - 1) / BM;
+  a.ndim = N;
+  a.ntiles = (N + BN - 1) / BN;
+  a.out = dW;
+  a.status = status;
+  a.wait_ns = wait_ns;
+  return launch_single<kWgrad>(mP, mP, mQ, mQ, a, (long long)n * a.mtiles_w * a.ntiles, s);
 }
 
 }  // namespace moe

@@ -69,6 +69,44 @@ cudaError_t launch_down_tc(const bf16* h, const int32_t* offsets, const bf16* w2
                            int f, int n, bf16* y_perm, uint32_t* status, unsigned long long wait_ns,
                            cudaStream_t s);
 
+// Backward on the tensor cores, rows in the expert-padded layout (segments of `poff` are
+// multiples of 128 rows; rows_max bounds the padded row count):
+//   store_ab: ab[q] = [x_pad[q] w1_eᵀ | x_pad[q] w3_eᵀ]                         [rows, 2f]
+//   dh:       dh' = g_pad[q] w2_e;  with a, b from ab and the row's gate G = wq[q]:
+//             dwp[q, j] = <dh', SiLU(a) b> over column tile j,  da = G dh' b SiLU'(a),
+//             db = G dh' SiLU(a),  hw = G SiLU(a) b                            [rows, f]
+//   dgrad_x:  dx_pad[q] = da[q] w1_e + db[q] w3_e                              [rows, d]
+//   wgrad:    dW_e = P_eᵀ Q_e over expert e's rows (P [rows, M], Q [rows, N]) [n, M, N]
+int bwd_dh_ntiles(int f);
+cudaError_t launch_bwd_store_ab(const bf16* x_pad, const int32_t* poff, const bf16* w1,
+                                const bf16* w3, int rows_max, int d, int f, int n, bf16* ab,
+                                uint32_t* status, unsigned long long wait_ns, cudaStream_t s);
+cudaError_t launch_bwd_dh(const bf16* g_pad, const int32_t* poff, const bf16* w2, const bf16* ab,
+                          const float* wq, int rows_max, int d, int f, int n, float* dwp, bf16* da,
+                          bf16* db, bf16* hw, uint32_t* status, unsigned long long wait_ns,
+                          cudaStream_t s);
+cudaError_t launch_bwd_dgrad_x(const bf16* da, const bf16* db, const int32_t* poff, const bf16* w1,
+                               const bf16* w3, int rows_max, int d, int f, int n, bf16* dx_pad,
+                               uint32_t* status, unsigned long long wait_ns, cudaStream_t s);
+cudaError_t launch_bwd_wgrad(const bf16* P, const bf16* Q, const int32_t* poff, int rows_max,
+                             int M, int N, int n, bf16* dW, uint32_t* status,
+                             unsigned long long wait_ns, cudaStream_t s);
+
+// Steps of the backward around the GEMMs (backward.cu).
+int bwd_rows_max(long long A, int n);
+int bwd_dwg_chunks(int T);
+cudaError_t launch_pad_offsets(const int32_t* off, int n, int32_t* poff, cudaStream_t s);
+cudaError_t launch_gather_bwd(const bf16* x, const bf16* dy, const int32_t* off,
+                              const int32_t* poff, const int32_t* perm, const float* topk_w,
+                              int n, int k, int rows_max, int d, bf16* x_pad, bf16* g_pad,
+                              float* wq, cudaStream_t s);
+cudaError_t launch_router_bwd(const int32_t* idx, const float* topk_w, const int32_t* off,
+                              const int32_t* poff, const int32_t* inv_perm, const float* dwp,
+                              int ntiles, const bf16* dx_pad, const bf16* wg, int T, int d, int n,
+                              int k, bf16* dx, float* dl, cudaStream_t s);
+cudaError_t launch_dwg(const bf16* x, const float* dl, int T, int d, int n, float* part,
+                       float* dwg, float* dbias, cudaStream_t s);
+
 // Which tensor-core GEMM form the launchers pick (MOE_TC_FORM_*; process-wide).
 void set_tc_form(int form);
 

@@ -35,7 +35,7 @@ __all__ = [
 _CHUNK = 1 << 24
 
 # tensor ids used in the seed sequence (stable: changing them changes every input)
-TENSOR_IDS = {"x": 0, "wg": 1, "w1": 2, "w3": 3, "w2": 4}
+TENSOR_IDS = {"x": 0, "wg": 1, "w1": 2, "w3": 3, "w2": 4, "dy": 5}
 
 
 @dataclasses.dataclass(frozen=True)
@@ -165,6 +165,8 @@ def make_inputs(w: Workload, seed: int = 0, layer: int = 0,
       w1 [n, f, d]   per-expert gate projection, out x in (K-major rows)
       w3 [n, f, d]   per-expert up projection, out x in
       w2 [n, d, f]   per-expert down projection, out x in
+      dy [T, d]      (only when asked for) gradient of the layer output, N(0, 1), for the
+                     backward
       bias [n] fp32  logit bias, or None
     ``x`` depends only on (seed, workload); weights also on ``layer``.
     """
@@ -180,6 +182,8 @@ def make_inputs(w: Workload, seed: int = 0, layer: int = 0,
         out["w3"] = _draw((w.n, w.f, w.d), 1.0 / np.sqrt(w.d), seed, w, layer, "w3", bf)
     if "w2" in tensors:
         out["w2"] = _draw((w.n, w.d, w.f), 1.0 / np.sqrt(w.f), seed, w, layer, "w2", bf)
+    if "dy" in tensors:
+        out["dy"] = _draw((w.T, w.d), 1.0, seed, w, layer, "dy", bf)
     out["bias"] = logit_bias_vector(w.n) if w.skew_bias else None
     return out
 

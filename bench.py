@@ -49,6 +49,8 @@ def parse():
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--pass", dest="which", default="forward", choices=["forward", "backward"],
+                   help="time the layer's forward (default) or its backward (moe_layer_backward)")
     return p.parse_args()
 
 
@@ -548,6 +550,118 @@ def routing_stats_report(moe, w, step, layer, layers, x, xn, hs, idx, off, strea
             "kernel_us_per_launch": us, "bytes_read_per_launch": T * k * 4}
 
 
+def backward_arm(args, w, dist):
+    """Times moe_layer_backward: one step = the gradients of <dy, MoE(x)> with respect to x,
+    W_g, the logit bias and every expert's w1, w3, w2 (routing recomputed inside the call)."""
+    import torch
+    import sparse_mixture_experts_56_b300 as moe
+
+    if w.dtype != "bf16" or w.layers != 1:
+        raise SystemExit("bench.py --pass backward: single-layer bf16 workloads only")
+    dev = torch.device("cuda", dist.local)
+    torch.cuda.set_device(dev)
+    moe._native.lib()
+    T, d, f, n, k = w.T, w.d, w.f, w.n, w.k
+    A = T * k
+    inp = workloads.make_inputs(w, seed=args.seed, tensors=("x", "wg", "w1", "w3", "w2", "dy"))
+    g = {t: to_dev(inp[t], w, dev) for t in ("x", "wg", "w1", "w3", "w2", "dy")}
+    bias = torch.from_numpy(inp["bias"]).to(dev) if inp["bias"] is not None else None
+    ws = moe.backward_workspace(T, d, f, n, k, torch.bfloat16, dev)
+    outs = {"dx": torch.empty_like(g["x"]), "dw_gate": torch.empty((d, n), dtype=torch.float32, device=dev),
+            "dw1": torch.empty_like(g["w1"]), "dw3": torch.empty_like(g["w3"]),
+            "dw2": torch.empty_like(g["w2"]), "dlogit_bias": torch.empty(n, dtype=torch.float32, device=dev)}
+    stream = torch.cuda.current_stream()
+
+    def step(xx=None, dyy=None):
+        moe.moe_layer_backward(g["x"] if xx is None else xx, g["wg"], g["w1"], g["w3"], g["w2"], k,
+                               g["dy"] if dyy is None else dyy, ws, logit_bias=bias, **outs)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    if moe.moe_check_device_error(ws) != 0:
+        raise SystemExit("device status set after warm-up")
+    sampler = ClockSampler(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    sampler.stop()
+    dist.barrier()
+    if moe.moe_check_device_error(ws) != 0:
+        raise SystemExit("device status set in the timed region")
+    ms = dist.max(e0.elapsed_time(e1)) / args.steps
+    # FLOPs of the expert GEMMs: recompute of a|b (4Adf), dy w2 (2Adf), dx (4Adf), three
+    # weight gradients (6Adf); the router's part is negligible
+    flops = 16.0 * A * d * f
+    pk, pk_kind = peaks()
+    tc_peak = float(pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    ach = flops / (ms / 1e3) / 1e12
+    line = {"metric": METRIC, "pass": "backward", "value": T * dist.world / (ms / 1e3),
+            "unit": "tokens/s", "n_gpus": dist.world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic (seeded Gaussian, Mixtral-shaped; dy ~ N(0,1))",
+            "config": {"workload": w.name, "T": T, "d_model": d, "d_ff": f, "n_experts": n, "top_k": k,
+                       "skewed_bias": w.skew_bias, "parallelism": f"replicas x{dist.world}",
+                       "l2": "no flush: per-step weights and gradients exceed the 126 MB L2"},
+            "tflops": flops * dist.world / (ms / 1e3) / 1e12,
+            "roofline": {"bound": "tensor", "achieved": ach, "peak": tc_peak, "unit": "TFLOP/s",
+                         "frac": ach / tc_peak, "traffic": None,
+                         "kernel": "moe_layer_backward (all launches of the call; 16*T*K*d*f FLOPs)",
+                         "peak_source": f"{pk_kind} (MEASURED_PEAKS.json)"},
+            "gpu_launches": 14 * args.steps, "clocks": sampler.summary()}
+    if not args.no_e2e:
+        x_pin = torch.from_numpy(np.ascontiguousarray(inp["x"]).view(np.int16)).view(torch.bfloat16).pin_memory()
+        dy_pin = torch.from_numpy(np.ascontiguousarray(inp["dy"]).view(np.int16)).view(torch.bfloat16).pin_memory()
+        dx_pin = torch.empty_like(x_pin).pin_memory()
+        dwg_pin = torch.empty((d, n), dtype=torch.float32).pin_memory()
+        xd, dyd = torch.empty_like(g["x"]), torch.empty_like(g["dy"])
+
+        def e2e_step():
+            xd.copy_(x_pin, non_blocking=True)
+            dyd.copy_(dy_pin, non_blocking=True)
+            step(xd, dyd)
+            dx_pin.copy_(outs["dx"], non_blocking=True)
+            dwg_pin.copy_(outs["dw_gate"], non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        em = dist.max(e0.elapsed_time(e1)) / args.steps
+        line["e2e"] = {"value": T * dist.world / (em / 1e3), "unit": "tokens/s",
+                       "h2d_bytes_per_step": 2 * T * d * 2, "d2h_bytes_per_step": T * d * 2 + d * n * 4,
+                       "ms_per_step": em, "api": "moe_layer_backward (dx and dW_g copied back)"}
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+        import oracle
+        f64 = {t: workloads.as_f32(inp[t], w).astype(np.float64) for t in ("x", "wg", "w1", "w3", "w2", "dy")}
+        rng = np.random.default_rng(99)
+        tok = oracle_sample_tokens(w, {2: 32, 3: 64, 4: 64}.get(w.wid, 32), rng)
+        t0 = time.perf_counter()
+        reps = 0
+        while True:
+            oracle.moe_layer_backward(f64["x"][tok], f64["wg"], f64["w1"], f64["w3"], f64["w2"], k,
+                                      f64["dy"][tok], inp["bias"])
+            reps += 1
+            el = time.perf_counter() - t0
+            if el >= 10.0 or el * (reps + 1) / reps > 30:
+                break
+        line["cpu_baseline"] = {"value": reps * len(tok) / el, "unit": "tokens/s", "cores": cpu_cores(),
+                                "kind": "oracle",
+                                "sample": f"backward of {len(tok)} of the {T} tokens x {reps} repetition(s), "
+                                          f"fp64 NumPy ({el:.1f} s)"}
+    if dist.rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     w = workloads.workload(args.workload)
@@ -558,7 +672,10 @@ def main():
     import torch
     dist.init("nccl" if torch.cuda.is_available() else "gloo")
     try:
-        ours_arm(args, w, dist)
+        if args.which == "backward":
+            backward_arm(args, w, dist)
+        else:
+            ours_arm(args, w, dist)
     finally:
         dist.close()
 

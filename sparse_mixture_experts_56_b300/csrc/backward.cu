@@ -18,7 +18,7 @@ namespace moe {
 namespace {
 
 constexpr int kRowAlign = 128;
-constexpr int kDwgChunk = 256;   // tokens per partial sum of dW_g
+constexpr int kDwgChunk = 128;   // tokens per partial sum of dW_g
 
 __global__ void pad_offsets_kernel(const int32_t* __restrict__ off, int n,
                                    int32_t* __restrict__ poff) {
@@ -132,9 +132,26 @@ __global__ void __launch_bounds__(256) router_bwd_kernel(
             acc[2 * j] += f2.x;
             acc[2 * j + 1] += f2.y;
           }
+          if (n == 8) {
+            // row c0 + j of W_g is 8 bf16 = one 16-byte load holding every expert
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            acc[j] = fmaf(dls[s], __bfloat162float(wg[(size_t)(c0 + j) * n + es[s]]), acc[j]);
+            for (int j = 0; j < 8; ++j) {
+              const uint4 wr = __ldg(reinterpret_cast<const uint4*>(wg + (size_t)(c0 + j) * 8));
+              const __nv_bfloat162* wp = reinterpret_cast<const __nv_bfloat162*>(&wr);
+              float wv = 0.f;
+#pragma unroll
+              for (int h = 0; h < 4; ++h) {
+                const float2 f2 = __bfloat1622float2(wp[h]);
+                if (es[s] == 2 * h) wv = f2.x;
+                if (es[s] == 2 * h + 1) wv = f2.y;
+              }
+              acc[j] = fmaf(dls[s], wv, acc[j]);
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              acc[j] = fmaf(dls[s], __bfloat162float(wg[(size_t)(c0 + j) * n + es[s]]), acc[j]);
+          }
         }
       }
       uint4 o;
@@ -168,6 +185,55 @@ __global__ void __launch_bounds__(256) dwg_partial_kernel(const bf16* __restrict
   }
   float* out = part + ((size_t)c * (d + 1) + col) * n;
   for (int e = 0; e < n; ++e) out[e] = acc[e];
+}
+
+// n == 8, d % 8 == 0: each thread owns 8 consecutive columns (one 16-byte load of x per
+// token) and all 8 experts; the first block of a chunk also sums the chunk's logit gradients
+// (the bias column, i == d).
+__global__ void __launch_bounds__(128) dwg_partial_n8_kernel(const bf16* __restrict__ x,
+                                                             const float* __restrict__ dl, int T,
+                                                             int d, float* __restrict__ part) {
+  __shared__ float s_dl[kDwgChunk * 8];
+  const int c = blockIdx.y;
+  const int t0 = c * kDwgChunk;
+  const int tn = min(kDwgChunk, T - t0);
+  for (int i = threadIdx.x; i < tn * 8; i += blockDim.x) s_dl[i] = dl[(size_t)t0 * 8 + i];
+  __syncthreads();
+  float* pc = part + (size_t)c * (d + 1) * 8;
+  if (blockIdx.x == 0 && threadIdx.x < 8) {
+    float v = 0.f;
+    for (int tt = 0; tt < tn; ++tt) v += s_dl[tt * 8 + threadIdx.x];
+    pc[(size_t)d * 8 + threadIdx.x] = v;
+  }
+  const int col0 = (blockIdx.x * blockDim.x + threadIdx.x) * 8;
+  if (col0 >= d) return;
+  float acc[8][8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[j][e] = 0.f;
+  for (int tt = 0; tt < tn; ++tt) {
+    const uint4 u = __ldg(reinterpret_cast<const uint4*>(x + (size_t)(t0 + tt) * d + col0));
+    const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&u);
+    float g[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) g[e] = s_dl[tt * 8 + e];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 xf = __bfloat1622float2(p[j]);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        acc[2 * j][e] = fmaf(xf.x, g[e], acc[2 * j][e]);
+        acc[2 * j + 1][e] = fmaf(xf.y, g[e], acc[2 * j + 1][e]);
+      }
+    }
+  }
+  float4* out = reinterpret_cast<float4*>(pc + (size_t)col0 * 8);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    out[2 * j] = make_float4(acc[j][0], acc[j][1], acc[j][2], acc[j][3]);
+    out[2 * j + 1] = make_float4(acc[j][4], acc[j][5], acc[j][6], acc[j][7]);
+  }
 }
 
 __global__ void __launch_bounds__(256) dwg_reduce_kernel(const float* __restrict__ part,
@@ -234,8 +300,13 @@ cudaError_t launch_dwg(const bf16* x, const float* dl, int T, int d, int n, floa
                        float* dwg, float* dbias, cudaStream_t s) {
   const int chunks = bwd_dwg_chunks(T);
   if (chunks > 0) {
-    dim3 grid((d + 1 + 255) / 256, chunks);
-    dwg_partial_kernel<<<grid, 256, 0, s>>>(x, dl, T, d, n, part);
+    if (n == 8 && d % 8 == 0) {
+      dim3 grid((d / 8 + 127) / 128, chunks);
+      dwg_partial_n8_kernel<<<grid, 128, 0, s>>>(x, dl, T, d, part);
+    } else {
+      dim3 grid((d + 1 + 255) / 256, chunks);
+      dwg_partial_kernel<<<grid, 256, 0, s>>>(x, dl, T, d, n, part);
+    }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

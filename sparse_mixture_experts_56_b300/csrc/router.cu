@@ -105,7 +105,10 @@ __global__ void __launch_bounds__(256) router_generic_kernel(const T* __restrict
 }
 
 // Fast path: bf16, n == 8, d % 256 == 0.  Each lane owns 8 consecutive elements of x per
-// 256-element slab: one 16-byte load of x and eight 16-byte loads of the matching W_g rows.
+// 256-element slab: eight 16-byte loads of the matching W_g rows, reused for the TPW tokens
+// the warp handles at once, and one 16-byte load of x per token.  Every lane accumulates its
+// elements in the same order whatever TPW is, so the logits do not depend on it.
+template <int TPW>
 __global__ void __launch_bounds__(256) router_bf16_n8_kernel(const bf16* __restrict__ x,
                                                              const bf16* __restrict__ wg,
                                                              const float* __restrict__ bias,
@@ -115,42 +118,56 @@ __global__ void __launch_bounds__(256) router_bf16_n8_kernel(const bf16* __restr
                                                              float* __restrict__ logits) {
   const int lane = threadIdx.x & 31;
   const int warps = (gridDim.x * blockDim.x) >> 5;
-  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < Tn; t += warps) {
-    float acc[8];
+  for (int t0 = ((blockIdx.x * blockDim.x + threadIdx.x) >> 5) * TPW; t0 < Tn;
+       t0 += warps * TPW) {
+    float acc[TPW][8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-    const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)t * d);
+    for (int j = 0; j < TPW; ++j)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[j][e] = 0.f;
     for (int i0 = lane * 8; i0 < d; i0 += 256) {
-      const uint4 xv = __ldg(xr + (i0 >> 3));
-      const __nv_bfloat162* xp = reinterpret_cast<const __nv_bfloat162*>(&xv);
       const uint4* wr = reinterpret_cast<const uint4*>(wg + (size_t)i0 * 8);
+      uint4 wv[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float2 xf = __bfloat1622float2(xp[j >> 1]);
-        const float xs = (j & 1) ? xf.y : xf.x;
-        const uint4 wv = __ldg(wr + j);
-        const __nv_bfloat162* wp = reinterpret_cast<const __nv_bfloat162*>(&wv);
+      for (int r = 0; r < 8; ++r) wv[r] = __ldg(wr + r);
 #pragma unroll
-        for (int e2 = 0; e2 < 4; ++e2) {
-          const float2 wf = __bfloat1622float2(wp[e2]);
-          acc[2 * e2] = fmaf(xs, wf.x, acc[2 * e2]);
-          acc[2 * e2 + 1] = fmaf(xs, wf.y, acc[2 * e2 + 1]);
+      for (int j = 0; j < TPW; ++j) {
+        if (t0 + j < Tn) {
+          const uint4 xv = __ldg(reinterpret_cast<const uint4*>(x + (size_t)(t0 + j) * d + i0));
+          const __nv_bfloat162* xp = reinterpret_cast<const __nv_bfloat162*>(&xv);
+#pragma unroll
+          for (int r = 0; r < 8; ++r) {
+            const float2 xf = __bfloat1622float2(xp[r >> 1]);
+            const float xs = (r & 1) ? xf.y : xf.x;
+            const __nv_bfloat162* wp = reinterpret_cast<const __nv_bfloat162*>(&wv[r]);
+#pragma unroll
+            for (int e2 = 0; e2 < 4; ++e2) {
+              const float2 wf = __bfloat1622float2(wp[e2]);
+              acc[j][2 * e2] = fmaf(xs, wf.x, acc[j][2 * e2]);
+              acc[j][2 * e2 + 1] = fmaf(xs, wf.y, acc[j][2 * e2 + 1]);
+            }
+          }
         }
       }
     }
-    warp_allreduce<8>(acc);
-    if (bias) {
 #pragma unroll
-      for (int e = 0; e < 8; ++e) acc[e] += bias[e];
-    }
-    if (logits && lane < 8) {
-      float v = 0.f;
+    for (int j = 0; j < TPW; ++j) {
+      const int t = t0 + j;
+      if (t >= Tn) break;
+      warp_allreduce<8>(acc[j]);
+      if (bias) {
 #pragma unroll
-      for (int e = 0; e < 8; ++e)
-        if (e == lane) v = acc[e];
-      logits[(size_t)t * 8 + lane] = v;
+        for (int e = 0; e < 8; ++e) acc[j][e] += bias[e];
+      }
+      if (logits && lane < 8) {
+        float v = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          if (e == lane) v = acc[j][e];
+        logits[(size_t)t * 8 + lane] = v;
+      }
+      if (lane == 0) select_and_write<8>(acc[j], 8, k, idx + (size_t)t * k, w + (size_t)t * k);
     }
-    if (lane == 0) select_and_write<8>(acc, 8, k, idx + (size_t)t * k, w + (size_t)t * k);
   }
 }
 
@@ -296,8 +313,9 @@ cudaError_t launch_router_topk(const void* x, const void* wg, const float* bias,
     router_bf16_n8_block_kernel<<<T, 256, 0, s>>>((const bf16*)x, (const bf16*)wg, bias, T, d, k,
                                                    idx, w, logits);
   } else if (dtype == MOE_BF16 && n == 8 && d % 256 == 0) {
-    router_bf16_n8_kernel<<<grid, 256, 0, s>>>((const bf16*)x, (const bf16*)wg, bias, T, d, k, idx,
-                                                w, logits);
+    // four tokens per warp share each W_g load
+    router_bf16_n8_kernel<4><<<grid_for_warps((T + 3) / 4), 256, 0, s>>>(
+        (const bf16*)x, (const bf16*)wg, bias, T, d, k, idx, w, logits);
   } else if (dtype == MOE_BF16) {
     if (n <= 8)
       router_generic_kernel<bf16, 8><<<grid, 256, 0, s>>>((const bf16*)x, (const bf16*)wg, bias, T,

@@ -90,3 +90,69 @@ def test_backward_is_deterministic(moe):
     for key in a:
         assert torch.equal(a[key].view(torch.uint8) if a[key].dtype != torch.float32 else a[key],
                            b[key].view(torch.uint8) if b[key].dtype != torch.float32 else b[key]), key
+
+
+def _f64(a, w):
+    return workloads.as_f32(a, w).astype(np.float64)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("wid", [2, 3])
+def test_full_size_backward(moe, wid):
+    """The Mixtral-shaped decode (T=32) and prefill (T=4096) workloads at full size, in the
+    launch configuration the benchmark times.  The oracle's steps run one expert at a time in
+    fp64: dG for every assignment (so dW_g and the bias gradient are compared whole), dx on a
+    token sample, and every expert's dW1, dW3, dW2 at decode / the largest and the smallest
+    expert's at prefill."""
+    w = workloads.workload(wid)
+    T, d, f, n, k = w.T, w.d, w.f, w.n, w.k
+    inp = workloads.make_inputs(w, tensors=("x", "wg", "w1", "w3", "w2", "dy"))
+    g = {t: to_device(inp[t], w, DEV) for t in ("x", "wg", "w1", "w3", "w2", "dy")}
+    ws = moe.backward_workspace(T, d, f, n, k, torch.bfloat16, DEV)
+    out = moe.moe_layer_backward(g["x"], g["wg"], g["w1"], g["w3"], g["w2"], k, g["dy"], ws,
+                                 want_dbias=True)
+    assert moe.moe_check_device_error(ws) == 0
+    idx, _, _ = moe.moe_router_topk(g["x"], g["wg"], k)
+    gi = idx.cpu().numpy().astype(np.int64)
+    del g
+    x, dy, wg = _f64(inp["x"], w), _f64(inp["dy"], w), _f64(inp["wg"], w)
+    lref = oracle.router_logits(x, wg)
+    check_selection(gi, lref, k)
+    gw = oracle.masked_softmax(np.take_along_axis(lref, gi, axis=1))
+    offsets, perm, _ = oracle.group_by_expert(gi, n)
+    counts = np.diff(offsets)
+    rng = np.random.default_rng(wid)
+    sample = np.unique(np.concatenate([[0, T - 1], rng.choice(T, size=min(T, 48), replace=False)]))
+    in_sample = np.zeros(T, dtype=bool)
+    in_sample[sample] = True
+    check_w = set(range(n)) if T <= 64 else {int(np.argmax(counts)), int(np.argmin(counts))}
+    dgate = np.zeros((T, k))
+    dx_ref = np.zeros((T, d))
+    tol = TOL["bf16"]
+    for e in range(n):
+        sel = perm[offsets[e]:offsets[e + 1]]
+        if sel.size == 0:
+            continue
+        t, slot = sel // k, sel % k
+        w1e, w3e, w2e = (_f64(inp[m][e], w) for m in ("w1", "w3", "w2"))
+        xs, ge = x[t], dy[t]
+        dgate[t, slot] = np.sum(ge * oracle.expert_swiglu(xs, w1e, w3e, w2e), axis=1)
+        do = gw[t, slot][:, None] * ge
+        if e in check_w:
+            dxs, dw1, dw3, dw2 = oracle.expert_swiglu_backward(xs, do, w1e, w3e, w2e)
+            assert_close_rel(to_numpy_f32(out["dw1"][e]), dw1, tol, f"dw1[{e}]")
+            assert_close_rel(to_numpy_f32(out["dw3"][e]), dw3, tol, f"dw3[{e}]")
+            assert_close_rel(to_numpy_f32(out["dw2"][e]), dw2, tol, f"dw2[{e}]")
+            np.add.at(dx_ref, t, dxs)
+        else:
+            m = in_sample[t]
+            if m.any():
+                dxs, _, _, _ = oracle.expert_swiglu_backward(xs[m], do[m], w1e, w3e, w2e)
+                np.add.at(dx_ref, t[m], dxs)
+        del w1e, w3e, w2e
+    dl = np.zeros((T, n))
+    np.put_along_axis(dl, gi, oracle.softmax_backward(gw, dgate), axis=1)
+    dx_ref += dl @ wg.T
+    assert_close_rel(to_numpy_f32(out["dx"])[sample], dx_ref[sample], tol, "dx (token sample)")
+    assert_close_rel(out["dw_gate"].cpu().numpy(), x.T @ dl, tol, "dw_gate")
+    assert_close_rel(out["dlogit_bias"].cpu().numpy(), dl.sum(axis=0), tol, "dlogit_bias")

@@ -207,19 +207,19 @@ moe_status moe_layer_forward(const void* x, const void* w_gate, const float* log
  * the softmax over them:  dl_k = G_k (dG_k - sum_j G_j dG_j),  dG_k = <dy, E_{e_k}(x)>.
  * The routing is recomputed from x, w_gate and logit_bias with the forward's kernels (the
  * same selection and gates as moe_layer_forward on the same inputs).
- *   x, dy           [T, d] bf16         inputs of the forward / gradient of its output
- *   w_gate [d, n], w1, w3 [n, f, d], w2 [n, d, f] bf16;  logit_bias [n] fp32 nullable
- *   dx              [T, d] bf16 out     fp32 accumulation, one rounding
+ *   x, dy           [T, d] dtype        inputs of the forward / gradient of its output
+ *   w_gate [d, n], w1, w3 [n, f, d], w2 [n, d, f] dtype;  logit_bias [n] fp32 nullable
+ *   dx              [T, d] dtype out    fp32 accumulation, one rounding
  *   dw_gate         [d, n] fp32 out
  *   dlogit_bias     [n] fp32 out, nullable
- *   dw1, dw3        [n, f, d] bf16 out; dw2 [n, d, f] bf16 out (fp32 accumulation over the
- *                   expert's rows in TMEM, one rounding; experts without rows get zeros)
+ *   dw1, dw3        [n, f, d] dtype out; dw2 [n, d, f] dtype out (fp32 accumulation over the
+ *                   expert's rows, one rounding; experts without rows get zeros)
  *   ws, ws_bytes    at least moe_backward_workspace_size(T, d, f, n, k, dtype) bytes, its
  *                   first 256 bytes zeroed as for every workspace (status word)
- * Every output is overwritten (not accumulated into).  Only MOE_BF16 with d % 64 == 0 and
- * f % 64 == 0 (the tensor-core path) is implemented; other shapes or fp32 return
- * MOE_ERR_UNSUPPORTED.  The expert GEMMs run on tcgen05 in an expert-padded row order
- * (every expert's rows padded with zero rows to a multiple of 128).
+ * Every output is overwritten (not accumulated into).  The expert GEMMs run in an
+ * expert-padded row order (every expert's rows padded with zero rows to a multiple of 128):
+ * on tcgen05 for MOE_BF16 with d % 64 == 0 and f % 64 == 0, otherwise on CUDA cores (fp32
+ * products; bf16 storage rounds the intermediates to bf16 as the tensor-core path does).
  */
 size_t moe_backward_workspace_size(int T, int d, int f, int n, int k, int dtype);
 moe_status moe_layer_backward(const void* x, const void* w_gate, const float* logit_bias,

@@ -58,12 +58,15 @@ struct BwdLayout {
   int rows_max, ntiles;
 };
 
-BwdLayout bwd_layout(long long T, long long d, long long f, int n, int k) {
-  const Layout L = layout(T, d, f, n, k, MOE_BF16);
+inline bool use_tc(int dtype, int d, int f);
+
+BwdLayout bwd_layout(long long T, long long d, long long f, int n, int k, int dtype) {
+  const Layout L = layout(T, d, f, n, k, dtype);
   BwdLayout B;
   const long long A = T * k;
+  const size_t esz = dtype == MOE_BF16 ? 2 : 4;
   B.rows_max = bwd_rows_max(A, n);
-  B.ntiles = bwd_dh_ntiles((int)f);
+  B.ntiles = use_tc(dtype, (int)d, (int)f) ? bwd_dh_ntiles((int)f) : bwd_simt_ntiles((int)f);
   const size_t R = (size_t)B.rows_max;
   size_t off = L.x_perm;   // everything before x_perm is shared with the forward layout
   auto take = [&](size_t bytes) {
@@ -73,13 +76,13 @@ BwdLayout bwd_layout(long long T, long long d, long long f, int n, int k) {
   };
   B.poff = take((size_t)(n + 1) * 4);
   B.wq = take(R * 4);
-  B.x_pad = take(R * d * 2);
-  B.g_pad = take(R * d * 2);
-  B.dx_pad = take(R * d * 2);
-  B.ab = take(R * 2 * f * 2);
-  B.da = take(R * f * 2);
-  B.db = take(R * f * 2);
-  B.hw = take(R * f * 2);
+  B.x_pad = take(R * d * esz);
+  B.g_pad = take(R * d * esz);
+  B.dx_pad = take(R * d * esz);
+  B.ab = take(R * 2 * f * esz);
+  B.da = take(R * f * esz);
+  B.db = take(R * f * esz);
+  B.hw = take(R * f * esz);
   B.dwp = take(R * B.ntiles * 4);
   B.dl = take((size_t)T * n * 4);
   B.part = take((size_t)bwd_dwg_chunks((int)T) * (d + 1) * n * 4);
@@ -310,8 +313,8 @@ moe_status moe_layer_forward(const void* x, const void* w_gate, const float* log
 }
 
 size_t moe_backward_workspace_size(int T, int d, int f, int n, int k, int dtype) {
-  if (dtype != MOE_BF16 || !sizes_ok(T, d, f, n, k)) return 0;
-  return bwd_layout(T, d, f, n, k).total;
+  if (!dtype_ok(dtype) || !sizes_ok(T, d, f, n, k)) return 0;
+  return bwd_layout(T, d, f, n, k, dtype).total;
 }
 
 moe_status moe_layer_backward(const void* x, const void* w_gate, const float* logit_bias,
@@ -320,17 +323,17 @@ moe_status moe_layer_backward(const void* x, const void* w_gate, const float* lo
                               float* dw_gate, float* dlogit_bias, void* dw1, void* dw3, void* dw2,
                               void* ws, size_t ws_bytes, void* stream) {
   if (!dtype_ok(dtype) || !sizes_ok(T, d, f, n, k)) return MOE_ERR_INVALID_ARG;
-  if (!use_tc(dtype, d, f)) return MOE_ERR_UNSUPPORTED;
   if (!w_gate || !w1 || !w3 || !w2 || !dw_gate || !dw1 || !dw3 || !dw2) return MOE_ERR_INVALID_ARG;
   if (T > 0 && (!x || !dy || !dx)) return MOE_ERR_INVALID_ARG;
   if (!aligned16(w_gate) || !aligned16(w1) || !aligned16(w3) || !aligned16(w2) ||
       !aligned16(dw1) || !aligned16(dw3) || !aligned16(dw2) || ((uintptr_t)dw_gate & 3u) ||
       (T > 0 && (!aligned16(x) || !aligned16(dy) || !aligned16(dx))))
     return MOE_ERR_INVALID_ARG;
-  const BwdLayout B = bwd_layout(T, d, f, n, k);
+  const BwdLayout B = bwd_layout(T, d, f, n, k, dtype);
   if (!ws || ws_bytes < B.total || !aligned16(ws)) return MOE_ERR_WORKSPACE;
   cudaStream_t s = (cudaStream_t)stream;
-  const size_t wbytes = (size_t)n * f * d * 2;
+  const size_t esz = dtype == MOE_BF16 ? 2 : 4;
+  const size_t wbytes = (size_t)n * f * d * esz;
   if (T == 0) {
     // no tokens: every gradient is zero
     cudaError_t e = cudaMemsetAsync(dw1, 0, wbytes, s);
@@ -340,7 +343,7 @@ moe_status moe_layer_backward(const void* x, const void* w_gate, const float* lo
     if (e == cudaSuccess && dlogit_bias) e = cudaMemsetAsync(dlogit_bias, 0, (size_t)n * 4, s);
     return cuda_status(e);
   }
-  const Layout L = layout(T, d, f, n, k, MOE_BF16);
+  const Layout L = layout(T, d, f, n, k, dtype);
   char* base = static_cast<char*>(ws);
   int32_t* idx = reinterpret_cast<int32_t*>(base + L.idx);
   float* w = reinterpret_cast<float*>(base + L.w);
@@ -349,6 +352,7 @@ moe_status moe_layer_backward(const void* x, const void* w_gate, const float* lo
   int32_t* inv_perm = reinterpret_cast<int32_t*>(base + L.inv_perm);
   int32_t* poff = reinterpret_cast<int32_t*>(base + B.poff);
   float* wq = reinterpret_cast<float*>(base + B.wq);
+  // padded expert-ordered buffers in the storage dtype (bf16 on the tensor-core path)
   bf16* x_pad = reinterpret_cast<bf16*>(base + B.x_pad);
   bf16* g_pad = reinterpret_cast<bf16*>(base + B.g_pad);
   bf16* dx_pad = reinterpret_cast<bf16*>(base + B.dx_pad);
@@ -370,26 +374,32 @@ moe_status moe_layer_backward(const void* x, const void* w_gate, const float* lo
                        reinterpret_cast<int32_t*>(base + L.scratch), st, s);
   if (e == cudaSuccess) e = launch_pad_offsets(offsets, n, poff, s);
   if (e == cudaSuccess)
-    e = launch_gather_bwd((const bf16*)x, (const bf16*)dy, offsets, poff, perm, w, n, k, R, d,
-                          x_pad, g_pad, wq, s);
-  // experts: recompute a | b, then dh' = dy w2 with the SwiGLU backward in its epilogue
-  if (e == cudaSuccess)
-    e = launch_bwd_store_ab(x_pad, poff, (const bf16*)w1, (const bf16*)w3, R, d, f, n, ab, st, wn,
-                            s);
-  if (e == cudaSuccess)
-    e = launch_bwd_dh(g_pad, poff, (const bf16*)w2, ab, wq, R, d, f, n, dwp, da, db, hw, st, wn, s);
-  if (e == cudaSuccess)
-    e = launch_bwd_dgrad_x(da, db, poff, (const bf16*)w1, (const bf16*)w3, R, d, f, n, dx_pad, st,
-                           wn, s);
-  // weight gradients: dW1_e = da_eᵀ x_e, dW3_e = db_eᵀ x_e, dW2_e = dy_eᵀ (G h)_e
-  if (e == cudaSuccess) e = launch_bwd_wgrad(da, x_pad, poff, R, f, d, n, (bf16*)dw1, st, wn, s);
-  if (e == cudaSuccess) e = launch_bwd_wgrad(db, x_pad, poff, R, f, d, n, (bf16*)dw3, st, wn, s);
-  if (e == cudaSuccess) e = launch_bwd_wgrad(g_pad, hw, poff, R, d, f, n, (bf16*)dw2, st, wn, s);
+    e = launch_gather_bwd(x, dy, offsets, poff, perm, w, n, k, R, (size_t)d * esz, x_pad, g_pad,
+                          wq, s);
+  if (use_tc(dtype, d, f)) {
+    // experts: recompute a | b, then dh' = dy w2 with the SwiGLU backward in its epilogue
+    if (e == cudaSuccess)
+      e = launch_bwd_store_ab(x_pad, poff, (const bf16*)w1, (const bf16*)w3, R, d, f, n, ab, st,
+                              wn, s);
+    if (e == cudaSuccess)
+      e = launch_bwd_dh(g_pad, poff, (const bf16*)w2, ab, wq, R, d, f, n, dwp, da, db, hw, st, wn,
+                        s);
+    if (e == cudaSuccess)
+      e = launch_bwd_dgrad_x(da, db, poff, (const bf16*)w1, (const bf16*)w3, R, d, f, n, dx_pad,
+                             st, wn, s);
+    // weight gradients: dW1_e = da_eᵀ x_e, dW3_e = db_eᵀ x_e, dW2_e = dy_eᵀ (G h)_e
+    if (e == cudaSuccess) e = launch_bwd_wgrad(da, x_pad, poff, R, f, d, n, (bf16*)dw1, st, wn, s);
+    if (e == cudaSuccess) e = launch_bwd_wgrad(db, x_pad, poff, R, f, d, n, (bf16*)dw3, st, wn, s);
+    if (e == cudaSuccess) e = launch_bwd_wgrad(g_pad, hw, poff, R, d, f, n, (bf16*)dw2, st, wn, s);
+  } else if (e == cudaSuccess) {
+    e = launch_bwd_experts_simt(x_pad, g_pad, poff, w1, w3, w2, wq, R, d, f, n, dtype, ab, dwp, da,
+                                db, hw, dx_pad, dw1, dw3, dw2, s);
+  }
   // router: gate and logit gradients, dx, then dW_g and the bias gradient
   if (e == cudaSuccess)
-    e = launch_router_bwd(idx, w, offsets, poff, inv_perm, dwp, B.ntiles, dx_pad,
-                          (const bf16*)w_gate, T, d, n, k, (bf16*)dx, dl, s);
-  if (e == cudaSuccess) e = launch_dwg((const bf16*)x, dl, T, d, n, part, dw_gate, dlogit_bias, s);
+    e = launch_router_bwd(idx, w, offsets, poff, inv_perm, dwp, B.ntiles, dx_pad, w_gate, T, d, n,
+                          k, dtype, dx, dl, s);
+  if (e == cudaSuccess) e = launch_dwg(x, dl, T, d, n, dtype, part, dw_gate, dlogit_bias, s);
   return cuda_status(e);
 }
 

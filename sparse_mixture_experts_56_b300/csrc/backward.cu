@@ -12,6 +12,8 @@
 //   router_bwd    per token: dG_k (sum of the GEMM epilogue's partial dot products, fixed
 //                 order), dl over the kept experts, dx = sum_k dx_pad[q_k] + dl W_gᵀ
 //   dwg_partial / dwg_reduce   dW_g = xᵀ dl and d(bias) = sum_t dl_t, in fixed order
+#include <string.h>
+
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -33,12 +35,14 @@ __global__ void pad_offsets_kernel(const int32_t* __restrict__ off, int n,
   }
 }
 
-// One block per padded row q (grid-stride).  Rows past poff[n] are left alone.
+// One block per padded row q (grid-stride).  Rows past poff[n] are left alone.  V is the copy
+// unit (16, 4 or 2 bytes, whichever divides the row).
+template <typename V>
 __global__ void __launch_bounds__(256) gather_bwd_kernel(
-    const uint4* __restrict__ x, const uint4* __restrict__ dy, const int32_t* __restrict__ off,
+    const V* __restrict__ x, const V* __restrict__ dy, const int32_t* __restrict__ off,
     const int32_t* __restrict__ poff, const int32_t* __restrict__ perm,
     const float* __restrict__ topk_w, int n, int k, int rows_max, int row_vecs,
-    uint4* __restrict__ x_pad, uint4* __restrict__ g_pad, float* __restrict__ wq) {
+    V* __restrict__ x_pad, V* __restrict__ g_pad, float* __restrict__ wq) {
   __shared__ int s_poff[kMaxExperts + 1], s_off[kMaxExperts + 1];
   for (int i = threadIdx.x; i <= n; i += blockDim.x) {
     s_poff[i] = poff[i];
@@ -49,21 +53,22 @@ __global__ void __launch_bounds__(256) gather_bwd_kernel(
     int e = 0;
     while (e + 1 < n && s_poff[e + 1] <= q) ++e;
     const int j = q - s_poff[e];
-    uint4* xd = x_pad + (size_t)q * row_vecs;
-    uint4* gd = g_pad + (size_t)q * row_vecs;
+    V* xd = x_pad + (size_t)q * row_vecs;
+    V* gd = g_pad + (size_t)q * row_vecs;
     if (j < s_off[e + 1] - s_off[e]) {
       const int a = __ldg(perm + s_off[e] + j);
       const int t = a / k;
       if (threadIdx.x == 0) wq[q] = __ldg(topk_w + a);
-      const uint4* xs = x + (size_t)t * row_vecs;
-      const uint4* gs = dy + (size_t)t * row_vecs;
+      const V* xs = x + (size_t)t * row_vecs;
+      const V* gs = dy + (size_t)t * row_vecs;
       for (int c = threadIdx.x; c < row_vecs; c += blockDim.x) {
         xd[c] = __ldg(xs + c);
         gd[c] = __ldg(gs + c);
       }
     } else {
       if (threadIdx.x == 0) wq[q] = 0.f;
-      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+      V z;
+      memset(&z, 0, sizeof(V));
       for (int c = threadIdx.x; c < row_vecs; c += blockDim.x) {
         xd[c] = z;
         gd[c] = z;
@@ -163,16 +168,71 @@ __global__ void __launch_bounds__(256) router_bwd_kernel(
   }
 }
 
+// Generic form (any storage dtype, any d): one warp per token, one column per lane and step.
+template <typename T, int KMAX>
+__global__ void __launch_bounds__(256) router_bwd_generic_kernel(
+    const int32_t* __restrict__ idx, const float* __restrict__ topk_w,
+    const int32_t* __restrict__ off, const int32_t* __restrict__ poff,
+    const int32_t* __restrict__ inv_perm, const float* __restrict__ dwp, int ntiles,
+    const T* __restrict__ dx_pad, const T* __restrict__ wg, int Tn, int d, int n, int k,
+    T* __restrict__ dx, float* __restrict__ dl) {
+  const int lane = threadIdx.x & 31;
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < Tn; t += warps) {
+    int es[KMAX], qs[KMAX];
+    float gate[KMAX], dG[KMAX];
+    float sdot = 0.f;
+#pragma unroll
+    for (int s = 0; s < KMAX; ++s) {
+      if (s < k) {
+        const int a = t * k + s;
+        const int e = __ldg(idx + a);
+        es[s] = e;
+        qs[s] = __ldg(poff + e) + (__ldg(inv_perm + a) - __ldg(off + e));
+        gate[s] = __ldg(topk_w + a);
+        float v = 0.f;
+        for (int j = lane; j < ntiles; j += 32) v += __ldg(dwp + (size_t)qs[s] * ntiles + j);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        dG[s] = v;
+        sdot = fmaf(gate[s], v, sdot);
+      }
+    }
+    float dls[KMAX];
+#pragma unroll
+    for (int s = 0; s < KMAX; ++s)
+      if (s < k) dls[s] = gate[s] * (dG[s] - sdot);
+    for (int e = lane; e < n; e += 32) {
+      float v = 0.f;
+#pragma unroll
+      for (int s = 0; s < KMAX; ++s)
+        if (s < k && es[s] == e) v = dls[s];
+      dl[(size_t)t * n + e] = v;
+    }
+    for (int c = lane; c < d; c += 32) {
+      float acc = 0.f;
+#pragma unroll
+      for (int s = 0; s < KMAX; ++s)
+        if (s < k) {
+          acc += to_f32(dx_pad[(size_t)qs[s] * d + c]);
+          acc = fmaf(dls[s], to_f32(wg[(size_t)c * n + es[s]]), acc);
+        }
+      dx[(size_t)t * d + c] = from_f32<T>(acc);
+    }
+  }
+}
+
 // part[c][i][e] = sum over the tokens of chunk c of x[t, i] dl[t, e]; column i == d stands
 // for the logit bias (x = 1).  Block: 256 columns x one chunk of tokens.
-__global__ void __launch_bounds__(256) dwg_partial_kernel(const bf16* __restrict__ x,
-                                                          const float* __restrict__ dl, int T,
+template <typename X>
+__global__ void __launch_bounds__(256) dwg_partial_kernel(const X* __restrict__ x,
+                                                          const float* __restrict__ dl, int Tn,
                                                           int d, int n,
                                                           float* __restrict__ part) {
   __shared__ float s_dl[kDwgChunk * kMaxExperts];
   const int c = blockIdx.y;
   const int t0 = c * kDwgChunk;
-  const int tn = min(kDwgChunk, T - t0);
+  const int tn = min(kDwgChunk, Tn - t0);
   for (int i = threadIdx.x; i < tn * n; i += blockDim.x) s_dl[i] = dl[(size_t)t0 * n + i];
   __syncthreads();
   const int col = blockIdx.x * blockDim.x + threadIdx.x;
@@ -180,7 +240,7 @@ __global__ void __launch_bounds__(256) dwg_partial_kernel(const bf16* __restrict
   float acc[kMaxExperts];
   for (int e = 0; e < n; ++e) acc[e] = 0.f;
   for (int tt = 0; tt < tn; ++tt) {
-    const float xv = col < d ? __bfloat162float(x[(size_t)(t0 + tt) * d + col]) : 1.0f;
+    const float xv = col < d ? to_f32(x[(size_t)(t0 + tt) * d + col]) : 1.0f;
     for (int e = 0; e < n; ++e) acc[e] = fmaf(xv, s_dl[tt * n + e], acc[e]);
   }
   float* out = part + ((size_t)c * (d + 1) + col) * n;
@@ -264,26 +324,61 @@ cudaError_t launch_pad_offsets(const int32_t* off, int n, int32_t* poff, cudaStr
   return cudaGetLastError();
 }
 
-cudaError_t launch_gather_bwd(const bf16* x, const bf16* dy, const int32_t* off,
+cudaError_t launch_gather_bwd(const void* x, const void* dy, const int32_t* off,
                               const int32_t* poff, const int32_t* perm, const float* topk_w,
-                              int n, int k, int rows_max, int d, bf16* x_pad, bf16* g_pad,
-                              float* wq, cudaStream_t s) {
+                              int n, int k, int rows_max, size_t row_bytes, void* x_pad,
+                              void* g_pad, float* wq, cudaStream_t s) {
   if (rows_max == 0) return cudaSuccess;
   const int cap = device_sm_count() * 8;
-  gather_bwd_kernel<<<rows_max < cap ? rows_max : cap, 256, 0, s>>>(
-      (const uint4*)x, (const uint4*)dy, off, poff, perm, topk_w, n, k, rows_max, d / 8,
-      (uint4*)x_pad, (uint4*)g_pad, wq);
+  const int grid = rows_max < cap ? rows_max : cap;
+  if (row_bytes % 16 == 0)
+    gather_bwd_kernel<uint4><<<grid, 256, 0, s>>>(
+        (const uint4*)x, (const uint4*)dy, off, poff, perm, topk_w, n, k, rows_max,
+        (int)(row_bytes / 16), (uint4*)x_pad, (uint4*)g_pad, wq);
+  else if (row_bytes % 4 == 0)
+    gather_bwd_kernel<uint32_t><<<grid, 256, 0, s>>>(
+        (const uint32_t*)x, (const uint32_t*)dy, off, poff, perm, topk_w, n, k, rows_max,
+        (int)(row_bytes / 4), (uint32_t*)x_pad, (uint32_t*)g_pad, wq);
+  else
+    gather_bwd_kernel<uint16_t><<<grid, 256, 0, s>>>(
+        (const uint16_t*)x, (const uint16_t*)dy, off, poff, perm, topk_w, n, k, rows_max,
+        (int)(row_bytes / 2), (uint16_t*)x_pad, (uint16_t*)g_pad, wq);
   return cudaGetLastError();
 }
 
 cudaError_t launch_router_bwd(const int32_t* idx, const float* topk_w, const int32_t* off,
                               const int32_t* poff, const int32_t* inv_perm, const float* dwp,
-                              int ntiles, const bf16* dx_pad, const bf16* wg, int T, int d, int n,
-                              int k, bf16* dx, float* dl, cudaStream_t s) {
+                              int ntiles, const void* dx_pad_v, const void* wg_v, int T, int d,
+                              int n, int k, int dtype, void* dx_v, float* dl, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   const long long blocks = ((long long)T + 7) / 8;
   const long long cap = (long long)device_sm_count() * 16;
   const int grid = (int)(blocks < cap ? blocks : cap);
+  if (dtype != MOE_BF16 || d % 8 != 0) {
+    if (dtype == MOE_BF16) {
+      if (k <= 2)
+        router_bwd_generic_kernel<bf16, 2><<<grid, 256, 0, s>>>(
+            idx, topk_w, off, poff, inv_perm, dwp, ntiles, (const bf16*)dx_pad_v,
+            (const bf16*)wg_v, T, d, n, k, (bf16*)dx_v, dl);
+      else
+        router_bwd_generic_kernel<bf16, kMaxExperts><<<grid, 256, 0, s>>>(
+            idx, topk_w, off, poff, inv_perm, dwp, ntiles, (const bf16*)dx_pad_v,
+            (const bf16*)wg_v, T, d, n, k, (bf16*)dx_v, dl);
+    } else {
+      if (k <= 2)
+        router_bwd_generic_kernel<float, 2><<<grid, 256, 0, s>>>(
+            idx, topk_w, off, poff, inv_perm, dwp, ntiles, (const float*)dx_pad_v,
+            (const float*)wg_v, T, d, n, k, (float*)dx_v, dl);
+      else
+        router_bwd_generic_kernel<float, kMaxExperts><<<grid, 256, 0, s>>>(
+            idx, topk_w, off, poff, inv_perm, dwp, ntiles, (const float*)dx_pad_v,
+            (const float*)wg_v, T, d, n, k, (float*)dx_v, dl);
+    }
+    return cudaGetLastError();
+  }
+  const bf16* dx_pad = (const bf16*)dx_pad_v;
+  const bf16* wg = (const bf16*)wg_v;
+  bf16* dx = (bf16*)dx_v;
   if (k <= 2)
     router_bwd_kernel<2><<<grid, 256, 0, s>>>(idx, topk_w, off, poff, inv_perm, dwp, ntiles,
                                               dx_pad, wg, T, d, n, k, dx, dl);
@@ -296,16 +391,19 @@ cudaError_t launch_router_bwd(const int32_t* idx, const float* topk_w, const int
   return cudaGetLastError();
 }
 
-cudaError_t launch_dwg(const bf16* x, const float* dl, int T, int d, int n, float* part,
-                       float* dwg, float* dbias, cudaStream_t s) {
+cudaError_t launch_dwg(const void* x, const float* dl, int T, int d, int n, int dtype,
+                       float* part, float* dwg, float* dbias, cudaStream_t s) {
   const int chunks = bwd_dwg_chunks(T);
   if (chunks > 0) {
-    if (n == 8 && d % 8 == 0) {
+    if (dtype == MOE_BF16 && n == 8 && d % 8 == 0) {
       dim3 grid((d / 8 + 127) / 128, chunks);
-      dwg_partial_n8_kernel<<<grid, 128, 0, s>>>(x, dl, T, d, part);
+      dwg_partial_n8_kernel<<<grid, 128, 0, s>>>((const bf16*)x, dl, T, d, part);
+    } else if (dtype == MOE_BF16) {
+      dim3 grid((d + 1 + 255) / 256, chunks);
+      dwg_partial_kernel<bf16><<<grid, 256, 0, s>>>((const bf16*)x, dl, T, d, n, part);
     } else {
       dim3 grid((d + 1 + 255) / 256, chunks);
-      dwg_partial_kernel<<<grid, 256, 0, s>>>(x, dl, T, d, n, part);
+      dwg_partial_kernel<float><<<grid, 256, 0, s>>>((const float*)x, dl, T, d, n, part);
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;

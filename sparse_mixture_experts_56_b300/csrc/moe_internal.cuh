@@ -96,16 +96,25 @@ cudaError_t launch_bwd_wgrad(const bf16* P, const bf16* Q, const int32_t* poff, 
 int bwd_rows_max(long long A, int n);
 int bwd_dwg_chunks(int T);
 cudaError_t launch_pad_offsets(const int32_t* off, int n, int32_t* poff, cudaStream_t s);
-cudaError_t launch_gather_bwd(const bf16* x, const bf16* dy, const int32_t* off,
+cudaError_t launch_gather_bwd(const void* x, const void* dy, const int32_t* off,
                               const int32_t* poff, const int32_t* perm, const float* topk_w,
-                              int n, int k, int rows_max, int d, bf16* x_pad, bf16* g_pad,
-                              float* wq, cudaStream_t s);
+                              int n, int k, int rows_max, size_t row_bytes, void* x_pad,
+                              void* g_pad, float* wq, cudaStream_t s);
 cudaError_t launch_router_bwd(const int32_t* idx, const float* topk_w, const int32_t* off,
                               const int32_t* poff, const int32_t* inv_perm, const float* dwp,
-                              int ntiles, const bf16* dx_pad, const bf16* wg, int T, int d, int n,
-                              int k, bf16* dx, float* dl, cudaStream_t s);
-cudaError_t launch_dwg(const bf16* x, const float* dl, int T, int d, int n, float* part,
-                       float* dwg, float* dbias, cudaStream_t s);
+                              int ntiles, const void* dx_pad, const void* wg, int T, int d, int n,
+                              int k, int dtype, void* dx, float* dl, cudaStream_t s);
+cudaError_t launch_dwg(const void* x, const float* dl, int T, int d, int n, int dtype,
+                       float* part, float* dwg, float* dbias, cudaStream_t s);
+// The backward's expert GEMMs on CUDA cores (fp32, or bf16 shapes outside the tensor-core
+// path): recompute, dy w2 with the SwiGLU backward, dx_pad, and the three weight gradients.
+int bwd_simt_ntiles(int f);
+cudaError_t launch_bwd_experts_simt(const void* x_pad, const void* g_pad, const int32_t* poff,
+                                    const void* w1, const void* w3, const void* w2,
+                                    const float* wq, int rows_max, int d, int f, int n, int dtype,
+                                    void* ab, float* dwp, void* da, void* db, void* hw,
+                                    void* dx_pad, void* dw1, void* dw3, void* dw2,
+                                    cudaStream_t s);
 
 // Which tensor-core GEMM form the launchers pick (MOE_TC_FORM_*; process-wide).
 void set_tc_form(int form);

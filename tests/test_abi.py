@@ -100,14 +100,13 @@ def test_host_validation_rejects_before_launch(lib):
     assert lib.moe_routing_stats(fake, 4, 2, 8, 0, nul, fake, nul) == INVALID
     assert lib.moe_routing_stats(nul, 4, 2, 8, 0, fake, fake, nul) == INVALID
     assert lib.moe_routing_stats(fake, 4, 2, 8, 0, ctypes.c_void_p(4100), fake, nul) == INVALID
-    # backward: fp32 and odd shapes are not implemented; workspace checked before launch
-    assert lib.moe_backward_workspace_size(64, 128, 256, 8, 2, 0) == 0
-    assert lib.moe_backward_workspace_size(64, 128, 256, 8, 2, 1) > \
+    # backward: sizes for both dtypes; bad dtype, workspace and missing pointers rejected
+    assert lib.moe_backward_workspace_size(64, 128, 256, 8, 2, 7) == 0
+    assert lib.moe_backward_workspace_size(64, 128, 256, 8, 2, 0) > \
+        lib.moe_backward_workspace_size(64, 128, 256, 8, 2, 1) > \
         lib.moe_workspace_size(64, 128, 256, 8, 2, 1) // 2
-    assert lib.moe_layer_backward(fake, fake, nul, fake, fake, fake, fake, 4, 64, 64, 8, 2, 0,
-                                  fake, fake, nul, fake, fake, fake, fake, 1 << 30, nul) == UNSUPPORTED
-    assert lib.moe_layer_backward(fake, fake, nul, fake, fake, fake, fake, 4, 96, 64, 8, 2, 1,
-                                  fake, fake, nul, fake, fake, fake, fake, 1 << 30, nul) == UNSUPPORTED
+    assert lib.moe_layer_backward(fake, fake, nul, fake, fake, fake, fake, 4, 64, 64, 8, 2, 5,
+                                  fake, fake, nul, fake, fake, fake, fake, 1 << 30, nul) == INVALID
     assert lib.moe_layer_backward(fake, fake, nul, fake, fake, fake, fake, 4, 64, 64, 8, 2, 1,
                                   fake, fake, nul, fake, fake, fake, fake, 16, nul) == WORKSPACE
     assert lib.moe_layer_backward(fake, fake, nul, fake, fake, fake, nul, 4, 64, 64, 8, 2, 1,

@@ -38,16 +38,23 @@ CASES = {
     "n32-k2-t500": (500, 128, 128, 32, 2, False),
     "t1": (1, 256, 256, 8, 2, False),
     "t1100-d512-f768": (1100, 512, 768, 8, 2, False),      # several 128-row tiles per expert
+    # CUDA-core path: fp32 storage (tolerance 1e-4), or bf16 shapes off the 64-multiple grid
+    "fp32-tiny-t64": (64, 128, 256, 8, 2, False, "f32"),   # the tiny fp32 workload's shape
+    "fp32-n4-t45-skew": (45, 96, 80, 4, 2, True, "f32"),
+    "fp32-k-equals-n-t20": (20, 40, 24, 3, 3, False, "f32"),
+    "simt-bf16-d200-f136": (64, 200, 136, 8, 2, False),
 }
 
 
 def _run(moe, name, wid):
-    T, d, f, n, k, skew = CASES[name]
-    w = workloads.custom(T, d, f, n, k, "bf16", wid=wid, skew_bias=skew)
+    T, d, f, n, k, skew, *dt = CASES[name]
+    dt = dt[0] if dt else "bf16"
+    w = workloads.custom(T, d, f, n, k, dt, wid=wid, skew_bias=skew)
     inp = workloads.make_inputs(w, tensors=("x", "wg", "w1", "w3", "w2", "dy"))
     g = {t: to_device(inp[t], w, DEV) for t in ("x", "wg", "w1", "w3", "w2", "dy")}
     bias = torch.from_numpy(inp["bias"]).to(DEV) if inp["bias"] is not None else None
-    ws = moe.backward_workspace(T, d, f, n, k, torch.bfloat16, DEV)
+    tdt = torch.bfloat16 if dt == "bf16" else torch.float32
+    ws = moe.backward_workspace(T, d, f, n, k, tdt, DEV)
     out = moe.moe_layer_backward(g["x"], g["wg"], g["w1"], g["w3"], g["w2"], k, g["dy"], ws,
                                  logit_bias=bias, want_dbias=True)
     assert moe.moe_check_device_error(ws) == 0
@@ -64,7 +71,7 @@ def test_backward_matches_oracle(moe, name):
     check_selection(gi, lref, w.k)
     ref = oracle.moe_layer_backward(f["x"], f["wg"], f["w1"], f["w3"], f["w2"], w.k, f["dy"],
                                     inp["bias"], idx=gi)
-    tol = TOL["bf16"]
+    tol = TOL[w.dtype]
     assert_close_rel(to_numpy_f32(out["dx"]), ref["dx"], tol, "dx")
     assert_close_rel(to_numpy_f32(out["dw1"]), ref["dw1"], tol, "dw1")
     assert_close_rel(to_numpy_f32(out["dw3"]), ref["dw3"], tol, "dw3")

@@ -10,6 +10,8 @@
 // for 4096 x 8 bf16) stays hot in L1/L2.  Products accumulate in fp32 per lane, then a
 // butterfly reduction gives every lane all n logits.  Lane 0 selects the top K (ties ->
 // lower index, descending order) and normalises exp(l - l_max) over them.
+#include <mutex>
+
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -171,6 +173,87 @@ __global__ void __launch_bounds__(256) router_bf16_n8_kernel(const bf16* __restr
   }
 }
 
+// Large batches: W_g (d x 8 bf16, 64 KB at d = 4096) is staged in shared memory once per
+// block, so the only global loads in the loop are the rows of x (unrolled so that 16 loads
+// of 16 bytes per lane are in flight).  Two tokens per warp share each read of W_g from
+// shared memory.  Each lane accumulates its elements in the same order as the kernel above,
+// so the logits are identical.
+constexpr int kRouterSmemTPW = 2;
+__global__ void __launch_bounds__(256) router_bf16_n8_smem_kernel(const bf16* __restrict__ x,
+                                                                  const bf16* __restrict__ wg,
+                                                                  const float* __restrict__ bias,
+                                                                  int Tn, int d, int k,
+                                                                  int32_t* __restrict__ idx,
+                                                                  float* __restrict__ w,
+                                                                  float* __restrict__ logits) {
+  // d rows of 8 bf16; row i sits in slot 8*(i/8) + ((i%8) ^ ((i/8)%8)), so that the eight
+  // lanes reading rows 8L + r (same r, consecutive L) hit eight different bank groups
+  extern __shared__ uint4 s_wg[];
+#pragma unroll 8
+  for (int i = threadIdx.x; i < d; i += blockDim.x)
+    s_wg[(i & ~7) | ((i ^ (i >> 3)) & 7)] = __ldg(reinterpret_cast<const uint4*>(wg) + i);
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  constexpr int TPW = kRouterSmemTPW;
+  for (int t0 = ((blockIdx.x * blockDim.x + threadIdx.x) >> 5) * TPW; t0 < Tn;
+       t0 += warps * TPW) {
+    float acc[TPW][8];
+#pragma unroll
+    for (int j = 0; j < TPW; ++j)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[j][e] = 0.f;
+    const int nt = Tn - t0 < TPW ? Tn - t0 : TPW;
+#pragma unroll 4
+    for (int i0 = lane * 8; i0 < d; i0 += 256) {
+      uint4 xv[TPW];
+#pragma unroll
+      for (int j = 0; j < TPW; ++j)
+        xv[j] = j < nt ? __ldg(reinterpret_cast<const uint4*>(x + (size_t)(t0 + j) * d + i0))
+                       : make_uint4(0u, 0u, 0u, 0u);
+      uint4 wr[8];
+#pragma unroll
+      for (int r = 0; r < 8; ++r) wr[r] = s_wg[i0 | ((r ^ (i0 >> 3)) & 7)];
+#pragma unroll
+      for (int j = 0; j < TPW; ++j) {
+        {
+          const __nv_bfloat162* xp = reinterpret_cast<const __nv_bfloat162*>(&xv[j]);
+#pragma unroll
+          for (int r = 0; r < 8; ++r) {
+            const float2 xf = __bfloat1622float2(xp[r >> 1]);
+            const float xs = (r & 1) ? xf.y : xf.x;
+            const __nv_bfloat162* wp = reinterpret_cast<const __nv_bfloat162*>(&wr[r]);
+#pragma unroll
+            for (int e2 = 0; e2 < 4; ++e2) {
+              const float2 wf = __bfloat1622float2(wp[e2]);
+              acc[j][2 * e2] = fmaf(xs, wf.x, acc[j][2 * e2]);
+              acc[j][2 * e2 + 1] = fmaf(xs, wf.y, acc[j][2 * e2 + 1]);
+            }
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < TPW; ++j) {
+      const int t = t0 + j;
+      if (t >= Tn) break;
+      warp_allreduce<8>(acc[j]);
+      if (bias) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[j][e] += bias[e];
+      }
+      if (logits && lane < 8) {
+        float v = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          if (e == lane) v = acc[j][e];
+        logits[(size_t)t * 8 + lane] = v;
+      }
+      if (lane == 0) select_and_write<8>(acc[j], 8, k, idx + (size_t)t * k, w + (size_t)t * k);
+    }
+  }
+}
+
 // Small batches (too few tokens to fill the GPU with one warp each): one block per token.
 // The 8 warps split the row of x into 2048-element slabs, reduce within the warp, and meet
 // in shared memory; warp 0 adds the 8 partial sums per expert in a fixed order.
@@ -296,6 +379,19 @@ __global__ void __launch_bounds__(256) rmsnorm_bf16_vec_kernel(const bf16* __res
 // Up to this many tokens the router gives each token a whole block (8 warps over d).
 constexpr int kRouterBlockPerTokenMax = 1024;
 
+// W_g rows staged in shared memory up to this d (16 bytes per row of 8 bf16).
+constexpr int kRouterSmemMaxD = 12288;
+
+cudaError_t router_smem_ready() {
+  static cudaError_t err = cudaErrorNotReady;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    err = cudaFuncSetAttribute(router_bf16_n8_smem_kernel,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, kRouterSmemMaxD * 16);
+  });
+  return err;
+}
+
 int grid_for_warps(long long warps_needed) {
   const long long blocks = (warps_needed + 7) / 8;
   const long long cap = (long long)device_sm_count() * 16;
@@ -312,6 +408,14 @@ cudaError_t launch_router_topk(const void* x, const void* wg, const float* bias,
   if (dtype == MOE_BF16 && n == 8 && d % 256 == 0 && T <= kRouterBlockPerTokenMax) {
     router_bf16_n8_block_kernel<<<T, 256, 0, s>>>((const bf16*)x, (const bf16*)wg, bias, T, d, k,
                                                    idx, w, logits);
+  } else if (dtype == MOE_BF16 && n == 8 && d % 256 == 0 && d <= kRouterSmemMaxD &&
+             router_smem_ready() == cudaSuccess) {
+    const long long warps_needed = (T + kRouterSmemTPW - 1) / kRouterSmemTPW;
+    long long blocks = (warps_needed + 7) / 8;
+    const long long cap = (long long)device_sm_count() * 3;
+    if (blocks > cap) blocks = cap;
+    router_bf16_n8_smem_kernel<<<(int)blocks, 256, (size_t)d * 16, s>>>(
+        (const bf16*)x, (const bf16*)wg, bias, T, d, k, idx, w, logits);
   } else if (dtype == MOE_BF16 && n == 8 && d % 256 == 0) {
     // four tokens per warp share each W_g load
     router_bf16_n8_kernel<4><<<grid_for_warps((T + 3) / 4), 256, 0, s>>>(

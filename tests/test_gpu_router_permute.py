@@ -38,6 +38,8 @@ ROUTER_CASES = [
     (33, 48, 1, 1, "f32", False),           # one expert
     (70, 256, 8, 1, "bf16", False),         # K = 1
     (1, 4096, 8, 2, "bf16", False),         # one token
+    (2000, 4096, 8, 2, "bf16", True),       # large batch: W_g staged in shared memory
+    (1025, 1280, 8, 2, "bf16", False),      # first large-batch size, d not a power of two
 ]
 
 

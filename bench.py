@@ -49,8 +49,9 @@ def parse():
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
-    p.add_argument("--pass", dest="which", default="forward", choices=["forward", "backward"],
-                   help="time the layer's forward (default) or its backward (moe_layer_backward)")
+    p.add_argument("--pass", dest="which", default="forward", choices=["forward", "backward", "train"],
+                   help="time the layer's forward (default), its backward (moe_layer_backward), "
+                        "or a training step (moe_layer_forward_train + moe_layer_backward_saved)")
     return p.parse_args()
 
 
@@ -552,7 +553,8 @@ def routing_stats_report(moe, w, step, layer, layers, x, xn, hs, idx, off, strea
 
 def backward_arm(args, w, dist):
     """Times moe_layer_backward: one step = the gradients of <dy, MoE(x)> with respect to x,
-    W_g, the logit bias and every expert's w1, w3, w2 (routing recomputed inside the call)."""
+    W_g, the logit bias and every expert's w1, w3, w2 (routing recomputed inside the call).
+    With --pass train a step is moe_layer_forward_train followed by moe_layer_backward_saved."""
     import torch
     import sparse_mixture_experts_56_b300 as moe
 
@@ -571,10 +573,29 @@ def backward_arm(args, w, dist):
             "dw1": torch.empty_like(g["w1"]), "dw3": torch.empty_like(g["w3"]),
             "dw2": torch.empty_like(g["w2"]), "dlogit_bias": torch.empty(n, dtype=torch.float32, device=dev)}
     stream = torch.cuda.current_stream()
+    train = args.which == "train"
+    if train:
+        fws = moe.workspace(T, d, f, n, k, torch.bfloat16, dev)
+        saved = moe.train_saved(T, d, f, n, k, torch.bfloat16, dev)
+        y = torch.empty_like(g["x"])
+        lib = moe._native.lib()
 
     def step(xx=None, dyy=None):
-        moe.moe_layer_backward(g["x"] if xx is None else xx, g["wg"], g["w1"], g["w3"], g["w2"], k,
-                               g["dy"] if dyy is None else dyy, ws, logit_bias=bias, **outs)
+        xx = g["x"] if xx is None else xx
+        dyy = g["dy"] if dyy is None else dyy
+        if not train:
+            moe.moe_layer_backward(xx, g["wg"], g["w1"], g["w3"], g["w2"], k, dyy, ws,
+                                   logit_bias=bias, **outs)
+            return
+        moe.moe_layer_forward_train(xx, g["wg"], g["w1"], g["w3"], g["w2"], k, fws, saved,
+                                    logit_bias=bias, y=y)
+        st = lib.moe_layer_backward_saved(
+            xx.data_ptr(), g["wg"].data_ptr(), g["w1"].data_ptr(), g["w3"].data_ptr(),
+            g["w2"].data_ptr(), dyy.data_ptr(), T, d, f, n, k, moe.MOE_BF16, saved.data_ptr(),
+            saved.numel(), outs["dx"].data_ptr(), outs["dw_gate"].data_ptr(),
+            outs["dlogit_bias"].data_ptr(), outs["dw1"].data_ptr(), outs["dw3"].data_ptr(),
+            outs["dw2"].data_ptr(), ws.data_ptr(), ws.numel(), stream.cuda_stream)
+        moe._native.check("moe_layer_backward_saved", st)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -596,12 +617,13 @@ def backward_arm(args, w, dist):
         raise SystemExit("device status set in the timed region")
     ms = dist.max(e0.elapsed_time(e1)) / args.steps
     # FLOPs of the expert GEMMs: recompute of a|b (4Adf), dy w2 (2Adf), dx (4Adf), three
-    # weight gradients (6Adf); the router's part is negligible
-    flops = 16.0 * A * d * f
+    # weight gradients (6Adf); a training step is the forward (6Adf) and the backward without
+    # the recompute (12Adf); the router's part is negligible
+    flops = (18.0 if train else 16.0) * A * d * f
     pk, pk_kind = peaks()
     tc_peak = float(pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     ach = flops / (ms / 1e3) / 1e12
-    line = {"metric": METRIC, "pass": "backward", "value": T * dist.world / (ms / 1e3),
+    line = {"metric": METRIC, "pass": args.which, "value": T * dist.world / (ms / 1e3),
             "unit": "tokens/s", "n_gpus": dist.world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic (seeded Gaussian, Mixtral-shaped; dy ~ N(0,1))",
@@ -611,10 +633,12 @@ def backward_arm(args, w, dist):
             "tflops": flops * dist.world / (ms / 1e3) / 1e12,
             "roofline": {"bound": "tensor", "achieved": ach, "peak": tc_peak, "unit": "TFLOP/s",
                          "frac": ach / tc_peak, "traffic": None,
-                         "kernel": "moe_layer_backward (all launches of the call; 16*T*K*d*f FLOPs)",
+                         "kernel": ("moe_layer_forward_train + moe_layer_backward_saved (all launches; "
+                                    "18*T*K*d*f FLOPs)") if train else
+                                   "moe_layer_backward (all launches of the call; 16*T*K*d*f FLOPs)",
                          "peak_source": f"{pk_kind} (MEASURED_PEAKS.json)"},
-            "gpu_launches": 14 * args.steps, "clocks": sampler.summary()}
-    if not args.no_e2e:
+            "gpu_launches": (21 if train else 14) * args.steps, "clocks": sampler.summary()}
+    if not args.no_e2e and not train:
         x_pin = torch.from_numpy(np.ascontiguousarray(inp["x"]).view(np.int16)).view(torch.bfloat16).pin_memory()
         dy_pin = torch.from_numpy(np.ascontiguousarray(inp["dy"]).view(np.int16)).view(torch.bfloat16).pin_memory()
         dx_pin = torch.empty_like(x_pin).pin_memory()
@@ -640,7 +664,7 @@ def backward_arm(args, w, dist):
         line["e2e"] = {"value": T * dist.world / (em / 1e3), "unit": "tokens/s",
                        "h2d_bytes_per_step": 2 * T * d * 2, "d2h_bytes_per_step": T * d * 2 + d * n * 4,
                        "ms_per_step": em, "api": "moe_layer_backward (dx and dW_g copied back)"}
-    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline and not train:
         import oracle
         f64 = {t: workloads.as_f32(inp[t], w).astype(np.float64) for t in ("x", "wg", "w1", "w3", "w2", "dy")}
         rng = np.random.default_rng(99)
@@ -672,7 +696,7 @@ def main():
     import torch
     dist.init("nccl" if torch.cuda.is_available() else "gloo")
     try:
-        if args.which == "backward":
+        if args.which in ("backward", "train"):
             backward_arm(args, w, dist)
         else:
             ours_arm(args, w, dist)

@@ -229,6 +229,34 @@ moe_status moe_layer_backward(const void* x, const void* w_gate, const float* lo
                               void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * Training pair: a forward that keeps what the backward needs, and the backward that uses it
+ * instead of recomputing the routing and the expert inputs a = x w1ᵀ, b = x w3ᵀ (the
+ * recompute is a quarter of moe_layer_backward's expert FLOPs).  Same results as
+ * moe_layer_forward / moe_layer_backward on the same inputs.
+ *   moe_train_saved_size   bytes of the `saved` buffer for these sizes (0 where the pair is
+ *                          not implemented: only MOE_BF16 with d % 64 == 0 and f % 64 == 0)
+ *   moe_layer_forward_train   moe_layer_forward (same arguments; no topk_idx_out /
+ *                          expert_offsets_out) that also fills `saved` (caller-owned device
+ *                          memory, 16-byte aligned): the routing (TopK indices and gates, the
+ *                          grouping) and a | b in bf16, rows in the expert-padded order
+ *   moe_layer_backward_saved  moe_layer_backward from `saved` (left unchanged, reusable) with
+ *                          the same x, weights and dy; no logit_bias (the routing is saved)
+ * Other dtypes or shapes return MOE_ERR_UNSUPPORTED.
+ */
+size_t moe_train_saved_size(int T, int d, int f, int n, int k, int dtype);
+moe_status moe_layer_forward_train(const void* x, const void* w_gate, const float* logit_bias,
+                                   const void* w1, const void* w3, const void* w2,
+                                   const void* residual, int T, int d, int f, int n, int k,
+                                   int dtype, void* y, void* saved, size_t saved_bytes, void* ws,
+                                   size_t ws_bytes, void* stream);
+moe_status moe_layer_backward_saved(const void* x, const void* w_gate, const void* w1,
+                                    const void* w3, const void* w2, const void* dy, int T, int d,
+                                    int f, int n, int k, int dtype, const void* saved,
+                                    size_t saved_bytes, void* dx, float* dw_gate,
+                                    float* dlogit_bias, void* dw1, void* dw3, void* dw2, void* ws,
+                                    size_t ws_bytes, void* stream);
+
+/*
  * Routing statistics of one layer from its TopK selections (newsflash.city digest,
  * "路径分析", Table 5: how often consecutive tokens are sent to the same expert;
  * "Mixtral of Experts" (xyznot.com summary), "Limitaciones": 28.4% first-choice repetition

@@ -21,7 +21,8 @@ __all__ = [
     "MOE_F32", "MOE_BF16", "MoEError", "dtype_code", "moe_workspace_size", "workspace",
     "moe_router_topk", "moe_permute", "moe_permute_noalloc", "moe_grouped_swiglu", "moe_expert_up", "moe_expert_down",
     "moe_combine", "moe_rmsnorm", "moe_routing_stats", "moe_backward_workspace_size",
-    "backward_workspace", "moe_layer_backward",
+    "backward_workspace", "moe_layer_backward", "moe_train_saved_size", "train_saved",
+    "moe_layer_forward_train", "moe_layer_backward_saved",
     "moe_layer_forward", "moe_check_device_error", "moe_set_wait_limit_ns", "moe_set_tc_form",
     "MOE_TC_FORM_AUTO", "MOE_TC_FORM_SINGLE", "MOE_TC_FORM_PAIR", "moe_version",
     "library_path",
@@ -280,4 +281,57 @@ def moe_layer_backward(x: torch.Tensor, w_gate: torch.Tensor, w1: torch.Tensor, 
     out = {"dx": dx, "dw_gate": dw_gate, "dw1": dw1, "dw3": dw3, "dw2": dw2}
     if dlogit_bias is not None:
         out["dlogit_bias"] = dlogit_bias
+    return out
+
+
+def moe_train_saved_size(T: int, d: int, f: int, n: int, k: int, dtype) -> int:
+    code = dtype if isinstance(dtype, int) else dtype_code(dtype)
+    return int(_native.lib().moe_train_saved_size(T, d, f, n, k, code))
+
+
+def train_saved(T: int, d: int, f: int, n: int, k: int, dtype=torch.bfloat16,
+                device="cuda") -> torch.Tensor:
+    """An uninitialised buffer of moe_train_saved_size bytes."""
+    size = moe_train_saved_size(T, d, f, n, k, dtype)
+    if size == 0:
+        raise ValueError("invalid or unsupported sizes")
+    return torch.empty(size, dtype=torch.uint8, device=device)
+
+
+def moe_layer_forward_train(x: torch.Tensor, w_gate: torch.Tensor, w1: torch.Tensor,
+                            w3: torch.Tensor, w2: torch.Tensor, k: int, ws: torch.Tensor,
+                            saved: torch.Tensor, *, logit_bias: Optional[torch.Tensor] = None,
+                            residual: Optional[torch.Tensor] = None,
+                            y: Optional[torch.Tensor] = None, stream=None):
+    """moe_layer_forward that also fills `saved` for moe_layer_backward_saved."""
+    T, d = x.shape
+    n, f, _ = w1.shape
+    if y is None:
+        y = torch.empty_like(x)
+    st = _native.lib().moe_layer_forward_train(
+        _ptr(x), _ptr(w_gate), _ptr(logit_bias), _ptr(w1), _ptr(w3), _ptr(w2), _ptr(residual), T,
+        d, f, n, k, dtype_code(x.dtype), _ptr(y), _ptr(saved), saved.numel(), _ptr(ws), ws.numel(),
+        _stream(stream))
+    check("moe_layer_forward_train", st)
+    return y
+
+
+def moe_layer_backward_saved(x: torch.Tensor, w_gate: torch.Tensor, w1: torch.Tensor,
+                             w3: torch.Tensor, w2: torch.Tensor, k: int, dy: torch.Tensor,
+                             saved: torch.Tensor, ws: torch.Tensor, *, want_dbias: bool = False,
+                             stream=None):
+    """moe_layer_backward from the buffer filled by moe_layer_forward_train."""
+    T, d = x.shape
+    n, f, _ = w1.shape
+    dev = x.device
+    out = {"dx": torch.empty_like(x), "dw_gate": torch.empty((d, n), dtype=torch.float32, device=dev),
+           "dw1": torch.empty_like(w1), "dw3": torch.empty_like(w3), "dw2": torch.empty_like(w2)}
+    if want_dbias:
+        out["dlogit_bias"] = torch.empty(n, dtype=torch.float32, device=dev)
+    st = _native.lib().moe_layer_backward_saved(
+        _ptr(x), _ptr(w_gate), _ptr(w1), _ptr(w3), _ptr(w2), _ptr(dy), T, d, f, n, k,
+        dtype_code(x.dtype), _ptr(saved), saved.numel(), _ptr(out["dx"]), _ptr(out["dw_gate"]),
+        _ptr(out.get("dlogit_bias")), _ptr(out["dw1"]), _ptr(out["dw3"]), _ptr(out["dw2"]),
+        _ptr(ws), ws.numel(), _stream(stream))
+    check("moe_layer_backward_saved", st)
     return out

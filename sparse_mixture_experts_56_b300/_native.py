@@ -44,6 +44,11 @@ SIGNATURES = {
                                _SZ, _P]),
     "moe_routing_stats": (_I, [_P, _I, _I, _I, _I, _P, _P, _P]),
     "moe_backward_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
+    "moe_train_saved_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
+    "moe_layer_forward_train": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _SZ,
+                                     _P, _SZ, _P]),
+    "moe_layer_backward_saved": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _SZ, _P,
+                                      _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_layer_backward": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P,
                                 _P, _P, _P, _SZ, _P]),
     "moe_check_device_error": (_I, [_P, _SZ, _P]),

@@ -147,6 +147,119 @@ moe_status grouped_impl(const void* x, const int32_t* perm, const int32_t* offse
   return down_impl(h, offsets, w2, T, d, f, n, k, dtype, y_perm, ws, s);
 }
 
+struct Routing {
+  int32_t *idx, *offsets, *perm, *inv_perm, *poff;
+  float* w;
+};
+
+// What moe_layer_forward_train keeps for moe_layer_backward_saved: the routing and the
+// expert inputs a = x w1ᵀ, b = x w3ᵀ (bf16) in the expert-padded row order.
+struct SavedLayout {
+  size_t idx, w, offsets, perm, inv_perm, poff, ab, total;
+};
+
+SavedLayout saved_layout(long long T, long long d, long long f, int n, int k) {
+  const long long A = T * k;
+  SavedLayout S;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off += align_up(bytes);
+    return at;
+  };
+  S.idx = take((size_t)A * 4);
+  S.w = take((size_t)A * 4);
+  S.offsets = take((size_t)(n + 1) * 4);
+  S.perm = take((size_t)A * 4);
+  S.inv_perm = take((size_t)A * 4);
+  S.poff = take((size_t)(n + 1) * 4);
+  S.ab = take((size_t)bwd_rows_max(A, n) * 2 * f * 2);
+  S.total = off;
+  (void)d;
+  return S;
+}
+
+moe_status check_backward_args(const void* x, const void* w_gate, const void* w1, const void* w3,
+                               const void* w2, const void* dy, int T, int d, int f, int n, int k,
+                               int dtype, const void* dx, const float* dw_gate, const void* dw1,
+                               const void* dw3, const void* dw2) {
+  if (!dtype_ok(dtype) || !sizes_ok(T, d, f, n, k)) return MOE_ERR_INVALID_ARG;
+  if (!w_gate || !w1 || !w3 || !w2 || !dw_gate || !dw1 || !dw3 || !dw2) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!x || !dy || !dx)) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(w_gate) || !aligned16(w1) || !aligned16(w3) || !aligned16(w2) ||
+      !aligned16(dw1) || !aligned16(dw3) || !aligned16(dw2) || ((uintptr_t)dw_gate & 3u) ||
+      (T > 0 && (!aligned16(x) || !aligned16(dy) || !aligned16(dx))))
+    return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+// No tokens: every gradient is zero.
+moe_status zero_grads(int d, int f, int n, int dtype, float* dw_gate, float* dlogit_bias, void* dw1,
+                      void* dw3, void* dw2, cudaStream_t s) {
+  const size_t wbytes = (size_t)n * f * d * (dtype == MOE_BF16 ? 2 : 4);
+  cudaError_t e = cudaMemsetAsync(dw1, 0, wbytes, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(dw3, 0, wbytes, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(dw2, 0, wbytes, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(dw_gate, 0, (size_t)d * n * 4, s);
+  if (e == cudaSuccess && dlogit_bias) e = cudaMemsetAsync(dlogit_bias, 0, (size_t)n * 4, s);
+  return cuda_status(e);
+}
+
+// The backward after the routing (and its padded offsets) exists: gather, the expert GEMMs
+// (recomputing a | b unless ab_saved holds them), the router's part and dW_g.
+moe_status backward_core(const void* x, const void* w_gate, const void* w1, const void* w3,
+                         const void* w2, const void* dy, int T, int d, int f, int n, int k,
+                         int dtype, void* dx, float* dw_gate, float* dlogit_bias, void* dw1,
+                         void* dw3, void* dw2, void* ws, const BwdLayout& B, const Routing& r,
+                         const bf16* ab_saved, cudaStream_t s) {
+  char* base = static_cast<char*>(ws);
+  const size_t esz = dtype == MOE_BF16 ? 2 : 4;
+  float* wq = reinterpret_cast<float*>(base + B.wq);
+  // padded expert-ordered buffers in the storage dtype (bf16 on the tensor-core path)
+  bf16* x_pad = reinterpret_cast<bf16*>(base + B.x_pad);
+  bf16* g_pad = reinterpret_cast<bf16*>(base + B.g_pad);
+  bf16* dx_pad = reinterpret_cast<bf16*>(base + B.dx_pad);
+  bf16* ab = reinterpret_cast<bf16*>(base + B.ab);
+  bf16* da = reinterpret_cast<bf16*>(base + B.da);
+  bf16* db = reinterpret_cast<bf16*>(base + B.db);
+  bf16* hw = reinterpret_cast<bf16*>(base + B.hw);
+  float* dwp = reinterpret_cast<float*>(base + B.dwp);
+  float* dl = reinterpret_cast<float*>(base + B.dl);
+  float* part = reinterpret_cast<float*>(base + B.part);
+  uint32_t* st = status_word(ws);
+  const unsigned long long wn = g_wait_ns.load();
+  const int R = B.rows_max;
+  const int32_t* poff = r.poff;
+  cudaError_t e = launch_gather_bwd(x, dy, r.offsets, poff, r.perm, r.w, n, k, R, (size_t)d * esz,
+                                    x_pad, g_pad, wq, s);
+  if (use_tc(dtype, d, f)) {
+    // experts: a | b (saved by the forward, or recomputed), then dh' = dy w2 with the SwiGLU
+    // backward in its epilogue
+    if (!ab_saved && e == cudaSuccess)
+      e = launch_bwd_store_ab(x_pad, poff, (const bf16*)w1, (const bf16*)w3, R, d, f, n, ab, st,
+                              wn, s);
+    if (e == cudaSuccess)
+      e = launch_bwd_dh(g_pad, poff, (const bf16*)w2, ab_saved ? ab_saved : ab, wq, R, d, f, n,
+                        dwp, da, db, hw, st, wn, s);
+    if (e == cudaSuccess)
+      e = launch_bwd_dgrad_x(da, db, poff, (const bf16*)w1, (const bf16*)w3, R, d, f, n, dx_pad,
+                             st, wn, s);
+    // weight gradients: dW1_e = da_eᵀ x_e, dW3_e = db_eᵀ x_e, dW2_e = dy_eᵀ (G h)_e
+    if (e == cudaSuccess) e = launch_bwd_wgrad(da, x_pad, poff, R, f, d, n, (bf16*)dw1, st, wn, s);
+    if (e == cudaSuccess) e = launch_bwd_wgrad(db, x_pad, poff, R, f, d, n, (bf16*)dw3, st, wn, s);
+    if (e == cudaSuccess) e = launch_bwd_wgrad(g_pad, hw, poff, R, d, f, n, (bf16*)dw2, st, wn, s);
+  } else if (e == cudaSuccess) {
+    e = launch_bwd_experts_simt(x_pad, g_pad, poff, w1, w3, w2, wq, R, d, f, n, dtype, ab, dwp, da,
+                                db, hw, dx_pad, dw1, dw3, dw2, s);
+  }
+  // router: gate and logit gradients, dx, then dW_g and the bias gradient
+  if (e == cudaSuccess)
+    e = launch_router_bwd(r.idx, r.w, r.offsets, poff, r.inv_perm, dwp, B.ntiles, dx_pad, w_gate,
+                          T, d, n, k, dtype, dx, dl, s);
+  if (e == cudaSuccess) e = launch_dwg(x, dl, T, d, n, dtype, part, dw_gate, dlogit_bias, s);
+  return cuda_status(e);
+}
+
 }  // namespace
 
 int device_sm_count() {
@@ -322,85 +435,112 @@ moe_status moe_layer_backward(const void* x, const void* w_gate, const float* lo
                               int T, int d, int f, int n, int k, int dtype, void* dx,
                               float* dw_gate, float* dlogit_bias, void* dw1, void* dw3, void* dw2,
                               void* ws, size_t ws_bytes, void* stream) {
-  if (!dtype_ok(dtype) || !sizes_ok(T, d, f, n, k)) return MOE_ERR_INVALID_ARG;
-  if (!w_gate || !w1 || !w3 || !w2 || !dw_gate || !dw1 || !dw3 || !dw2) return MOE_ERR_INVALID_ARG;
-  if (T > 0 && (!x || !dy || !dx)) return MOE_ERR_INVALID_ARG;
-  if (!aligned16(w_gate) || !aligned16(w1) || !aligned16(w3) || !aligned16(w2) ||
-      !aligned16(dw1) || !aligned16(dw3) || !aligned16(dw2) || ((uintptr_t)dw_gate & 3u) ||
-      (T > 0 && (!aligned16(x) || !aligned16(dy) || !aligned16(dx))))
-    return MOE_ERR_INVALID_ARG;
+  moe_status st = check_backward_args(x, w_gate, w1, w3, w2, dy, T, d, f, n, k, dtype, dx,
+                                      dw_gate, dw1, dw3, dw2);
+  if (st != MOE_OK) return st;
   const BwdLayout B = bwd_layout(T, d, f, n, k, dtype);
   if (!ws || ws_bytes < B.total || !aligned16(ws)) return MOE_ERR_WORKSPACE;
   cudaStream_t s = (cudaStream_t)stream;
-  const size_t esz = dtype == MOE_BF16 ? 2 : 4;
-  const size_t wbytes = (size_t)n * f * d * esz;
-  if (T == 0) {
-    // no tokens: every gradient is zero
-    cudaError_t e = cudaMemsetAsync(dw1, 0, wbytes, s);
-    if (e == cudaSuccess) e = cudaMemsetAsync(dw3, 0, wbytes, s);
-    if (e == cudaSuccess) e = cudaMemsetAsync(dw2, 0, wbytes, s);
-    if (e == cudaSuccess) e = cudaMemsetAsync(dw_gate, 0, (size_t)d * n * 4, s);
-    if (e == cudaSuccess && dlogit_bias) e = cudaMemsetAsync(dlogit_bias, 0, (size_t)n * 4, s);
-    return cuda_status(e);
-  }
+  if (T == 0) return zero_grads(d, f, n, dtype, dw_gate, dlogit_bias, dw1, dw3, dw2, s);
   const Layout L = layout(T, d, f, n, k, dtype);
   char* base = static_cast<char*>(ws);
-  int32_t* idx = reinterpret_cast<int32_t*>(base + L.idx);
-  float* w = reinterpret_cast<float*>(base + L.w);
-  int32_t* offsets = reinterpret_cast<int32_t*>(base + L.offsets);
-  int32_t* perm = reinterpret_cast<int32_t*>(base + L.perm);
-  int32_t* inv_perm = reinterpret_cast<int32_t*>(base + L.inv_perm);
-  int32_t* poff = reinterpret_cast<int32_t*>(base + B.poff);
-  float* wq = reinterpret_cast<float*>(base + B.wq);
-  // padded expert-ordered buffers in the storage dtype (bf16 on the tensor-core path)
-  bf16* x_pad = reinterpret_cast<bf16*>(base + B.x_pad);
-  bf16* g_pad = reinterpret_cast<bf16*>(base + B.g_pad);
-  bf16* dx_pad = reinterpret_cast<bf16*>(base + B.dx_pad);
-  bf16* ab = reinterpret_cast<bf16*>(base + B.ab);
-  bf16* da = reinterpret_cast<bf16*>(base + B.da);
-  bf16* db = reinterpret_cast<bf16*>(base + B.db);
-  bf16* hw = reinterpret_cast<bf16*>(base + B.hw);
-  float* dwp = reinterpret_cast<float*>(base + B.dwp);
-  float* dl = reinterpret_cast<float*>(base + B.dl);
-  float* part = reinterpret_cast<float*>(base + B.part);
-  uint32_t* st = status_word(ws);
-  const unsigned long long wn = g_wait_ns.load();
-  const int A = T * k, R = B.rows_max;
-
+  Routing r;
+  r.idx = reinterpret_cast<int32_t*>(base + L.idx);
+  r.w = reinterpret_cast<float*>(base + L.w);
+  r.offsets = reinterpret_cast<int32_t*>(base + L.offsets);
+  r.perm = reinterpret_cast<int32_t*>(base + L.perm);
+  r.inv_perm = reinterpret_cast<int32_t*>(base + L.inv_perm);
+  r.poff = reinterpret_cast<int32_t*>(base + B.poff);
   // the forward's routing, recomputed (same kernels, same inputs, same result)
+  cudaError_t e =
+      launch_router_topk(x, w_gate, logit_bias, T, d, n, k, dtype, r.idx, r.w, nullptr, s);
+  if (e == cudaSuccess)
+    e = launch_permute(r.idx, T * k, n, r.offsets, r.perm, r.inv_perm,
+                       reinterpret_cast<int32_t*>(base + L.scratch), status_word(ws), s);
+  if (e == cudaSuccess) e = launch_pad_offsets(r.offsets, n, r.poff, s);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  return backward_core(x, w_gate, w1, w3, w2, dy, T, d, f, n, k, dtype, dx, dw_gate, dlogit_bias,
+                       dw1, dw3, dw2, ws, B, r, nullptr, s);
+}
+
+size_t moe_train_saved_size(int T, int d, int f, int n, int k, int dtype) {
+  if (!use_tc(dtype, d, f) || !sizes_ok(T, d, f, n, k)) return 0;
+  return saved_layout(T, d, f, n, k).total;
+}
+
+moe_status moe_layer_forward_train(const void* x, const void* w_gate, const float* logit_bias,
+                                   const void* w1, const void* w3, const void* w2,
+                                   const void* residual, int T, int d, int f, int n, int k,
+                                   int dtype, void* y, void* saved, size_t saved_bytes, void* ws,
+                                   size_t ws_bytes, void* stream) {
+  if (!dtype_ok(dtype) || !sizes_ok(T, d, f, n, k)) return MOE_ERR_INVALID_ARG;
+  if (!use_tc(dtype, d, f)) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  if (!x || !w_gate || !w1 || !w3 || !w2 || !y) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w_gate) || !aligned16(w1) || !aligned16(w3) || !aligned16(w2) ||
+      !aligned16(y) || (residual && !aligned16(residual)))
+    return MOE_ERR_INVALID_ARG;
+  const Layout L = layout(T, d, f, n, k, dtype);
+  if (!ws || ws_bytes < L.total || !aligned16(ws)) return MOE_ERR_WORKSPACE;
+  const SavedLayout S = saved_layout(T, d, f, n, k);
+  if (!saved || saved_bytes < S.total || !aligned16(saved)) return MOE_ERR_WORKSPACE;
+  cudaStream_t s = (cudaStream_t)stream;
+  char* base = static_cast<char*>(ws);
+  char* sv = static_cast<char*>(saved);
+  int32_t* idx = reinterpret_cast<int32_t*>(sv + S.idx);
+  float* w = reinterpret_cast<float*>(sv + S.w);
+  int32_t* offsets = reinterpret_cast<int32_t*>(sv + S.offsets);
+  int32_t* perm = reinterpret_cast<int32_t*>(sv + S.perm);
+  int32_t* inv_perm = reinterpret_cast<int32_t*>(sv + S.inv_perm);
+  int32_t* poff = reinterpret_cast<int32_t*>(sv + S.poff);
+  bf16* ab = reinterpret_cast<bf16*>(sv + S.ab);
+  const int A = T * k;
+  uint32_t* st = status_word(ws);
   cudaError_t e = launch_router_topk(x, w_gate, logit_bias, T, d, n, k, dtype, idx, w, nullptr, s);
   if (e == cudaSuccess)
     e = launch_permute(idx, A, n, offsets, perm, inv_perm,
                        reinterpret_cast<int32_t*>(base + L.scratch), st, s);
   if (e == cudaSuccess) e = launch_pad_offsets(offsets, n, poff, s);
+  if (e == cudaSuccess) e = launch_zero_pad_rows(ab, offsets, poff, n, 2 * f, s);
+  void* x_perm = base + L.x_perm;
+  bf16* h = reinterpret_cast<bf16*>(base + L.h);
+  void* y_perm = base + L.y_perm;
+  if (e == cudaSuccess) e = launch_gather_rows(x, perm, A, k, (size_t)d * 2, x_perm, s);
   if (e == cudaSuccess)
-    e = launch_gather_bwd(x, dy, offsets, poff, perm, w, n, k, R, (size_t)d * esz, x_pad, g_pad,
-                          wq, s);
-  if (use_tc(dtype, d, f)) {
-    // experts: recompute a | b, then dh' = dy w2 with the SwiGLU backward in its epilogue
-    if (e == cudaSuccess)
-      e = launch_bwd_store_ab(x_pad, poff, (const bf16*)w1, (const bf16*)w3, R, d, f, n, ab, st,
-                              wn, s);
-    if (e == cudaSuccess)
-      e = launch_bwd_dh(g_pad, poff, (const bf16*)w2, ab, wq, R, d, f, n, dwp, da, db, hw, st, wn,
-                        s);
-    if (e == cudaSuccess)
-      e = launch_bwd_dgrad_x(da, db, poff, (const bf16*)w1, (const bf16*)w3, R, d, f, n, dx_pad,
-                             st, wn, s);
-    // weight gradients: dW1_e = da_eᵀ x_e, dW3_e = db_eᵀ x_e, dW2_e = dy_eᵀ (G h)_e
-    if (e == cudaSuccess) e = launch_bwd_wgrad(da, x_pad, poff, R, f, d, n, (bf16*)dw1, st, wn, s);
-    if (e == cudaSuccess) e = launch_bwd_wgrad(db, x_pad, poff, R, f, d, n, (bf16*)dw3, st, wn, s);
-    if (e == cudaSuccess) e = launch_bwd_wgrad(g_pad, hw, poff, R, d, f, n, (bf16*)dw2, st, wn, s);
-  } else if (e == cudaSuccess) {
-    e = launch_bwd_experts_simt(x_pad, g_pad, poff, w1, w3, w2, wq, R, d, f, n, dtype, ab, dwp, da,
-                                db, hw, dx_pad, dw1, dw3, dw2, s);
-  }
-  // router: gate and logit gradients, dx, then dW_g and the bias gradient
-  if (e == cudaSuccess)
-    e = launch_router_bwd(idx, w, offsets, poff, inv_perm, dwp, B.ntiles, dx_pad, w_gate, T, d, n,
-                          k, dtype, dx, dl, s);
-  if (e == cudaSuccess) e = launch_dwg(x, dl, T, d, n, dtype, part, dw_gate, dlogit_bias, s);
-  return cuda_status(e);
+    e = launch_up_tc((const bf16*)x_perm, offsets, (const bf16*)w1, (const bf16*)w3, A, d, f, n, h,
+                     st, g_wait_ns.load(), s, ab, poff);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  moe_status ms = down_impl(h, offsets, w2, T, d, f, n, k, dtype, y_perm, ws, s);
+  if (ms != MOE_OK) return ms;
+  return cuda_status(launch_combine(y_perm, inv_perm, w, residual, T, d, k, dtype, y, s));
+}
+
+moe_status moe_layer_backward_saved(const void* x, const void* w_gate, const void* w1,
+                                    const void* w3, const void* w2, const void* dy, int T, int d,
+                                    int f, int n, int k, int dtype, const void* saved,
+                                    size_t saved_bytes, void* dx, float* dw_gate,
+                                    float* dlogit_bias, void* dw1, void* dw3, void* dw2, void* ws,
+                                    size_t ws_bytes, void* stream) {
+  moe_status st = check_backward_args(x, w_gate, w1, w3, w2, dy, T, d, f, n, k, dtype, dx,
+                                      dw_gate, dw1, dw3, dw2);
+  if (st != MOE_OK) return st;
+  if (!use_tc(dtype, d, f)) return MOE_ERR_UNSUPPORTED;
+  const BwdLayout B = bwd_layout(T, d, f, n, k, dtype);
+  if (!ws || ws_bytes < B.total || !aligned16(ws)) return MOE_ERR_WORKSPACE;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (T == 0) return zero_grads(d, f, n, dtype, dw_gate, dlogit_bias, dw1, dw3, dw2, s);
+  const SavedLayout S = saved_layout(T, d, f, n, k);
+  if (!saved || saved_bytes < S.total || !aligned16(saved)) return MOE_ERR_WORKSPACE;
+  char* sv = const_cast<char*>(static_cast<const char*>(saved));
+  Routing r;
+  r.idx = reinterpret_cast<int32_t*>(sv + S.idx);
+  r.w = reinterpret_cast<float*>(sv + S.w);
+  r.offsets = reinterpret_cast<int32_t*>(sv + S.offsets);
+  r.perm = reinterpret_cast<int32_t*>(sv + S.perm);
+  r.inv_perm = reinterpret_cast<int32_t*>(sv + S.inv_perm);
+  r.poff = reinterpret_cast<int32_t*>(sv + S.poff);
+  return backward_core(x, w_gate, w1, w3, w2, dy, T, d, f, n, k, dtype, dx, dw_gate, dlogit_bias,
+                       dw1, dw3, dw2, ws, B, r, reinterpret_cast<const bf16*>(sv + S.ab), s);
 }
 
 moe_status moe_routing_stats(const int32_t* topk_idx, int T, int k, int n, int seq_len,

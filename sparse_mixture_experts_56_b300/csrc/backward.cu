@@ -310,7 +310,26 @@ __global__ void __launch_bounds__(256) dwg_reduce_kernel(const float* __restrict
     dbias[i - d * n] = v;
 }
 
+// Block per (expert, padding row): padding rows follow each expert's rows in its segment.
+__global__ void __launch_bounds__(256) zero_pad_rows_kernel(uint4* __restrict__ buf,
+                                                            const int32_t* __restrict__ off,
+                                                            const int32_t* __restrict__ poff,
+                                                            int row_vecs) {
+  const int e = blockIdx.y, j = blockIdx.x;
+  const int row = poff[e] + (off[e + 1] - off[e]) + j;
+  if (row >= poff[e + 1]) return;
+  const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+  for (int c = threadIdx.x; c < row_vecs; c += blockDim.x) buf[(size_t)row * row_vecs + c] = z;
+}
+
 }  // namespace
+
+cudaError_t launch_zero_pad_rows(bf16* buf, const int32_t* off, const int32_t* poff, int n,
+                                 int row_elems, cudaStream_t s) {
+  dim3 grid(kRowAlign - 1, n);
+  zero_pad_rows_kernel<<<grid, 256, 0, s>>>((uint4*)buf, off, poff, row_elems / 8);
+  return cudaGetLastError();
+}
 
 int bwd_rows_max(long long A, int n) {
   const long long r = A + (long long)(kRowAlign - 1) * n;

@@ -113,6 +113,10 @@ struct TcArgs {
   bf16* da;           // kDh outputs [rows, ndim]
   bf16* db;
   bf16* hw;
+  // kSwiGLU, optional: also store a and b (bf16) for the backward, row p of expert e at
+  // padded row poff_save[e] + (p - offsets[e]) of ab_save [rows, 2 ndim]
+  bf16* ab_save;
+  const int32_t* poff_save;
 };
 
 template <int STAGES>
@@ -692,6 +696,16 @@ __global__ void __launch_bounds__(256, 1)
           if (row_ok && col0 + c * 32 < args.ndim) {
             float v[32];
             if constexpr (MODE == kSwiGLU) {
+              if (args.ab_save) {
+                const size_t q = (size_t)(args.poff_save[t.e] + (int)grow - sh.off[t.e]);
+                bf16* o = args.ab_save + q * 2 * args.ndim + col0 + c * 32;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(a[j]);
+                store_row32(o, v);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(b[j]);
+                store_row32(o + args.ndim, v);
+              }
 #pragma unroll
               for (int j = 0; j < 32; ++j) {
                 const float av = __uint_as_float(a[j]);
@@ -931,7 +945,8 @@ void set_tc_form(int form) { g_tc_form.store(form, std::memory_order_relaxed); }
 
 cudaError_t launch_up_tc(const bf16* x_perm, const int32_t* offsets, const bf16* w1, const bf16* w3,
                          int A, int d, int f, int n, bf16* h, uint32_t* status,
-                         unsigned long long wait_ns, cudaStream_t s) {
+                         unsigned long long wait_ns, cudaStream_t s, bf16* ab_save,
+                         const int32_t* poff_save) {
   if (A == 0) return cudaSuccess;
   CUtensorMap mA, mW1, mW3;
   if (!make_map(&mA, x_perm, (uint64_t)A, (uint64_t)d, BM) ||
@@ -947,6 +962,8 @@ cudaError_t launch_up_tc(const bf16* x_perm, const int32_t* offsets, const bf16*
   a.out = h;
   a.status = status;
   a.wait_ns = wait_ns;
+  a.ab_save = ab_save;
+  a.poff_save = poff_save;
   return launch_gemm<kSwiGLU>(mA, mW1, mW3, a, A, s);
 }
 

@@ -62,9 +62,12 @@ cudaError_t launch_down_simt(const void* h, const int32_t* offsets, const void* 
                              int f, int n, int dtype, void* y_perm, cudaStream_t s);
 
 // bf16 tcgen05 experts: up = w1|w3 GEMM with SiLU(a)*b fused; down = w2 GEMM.
+// ab_save / poff_save (optional): also store a and b for the backward, in the expert-padded
+// row order, as bf16 [rows, 2f].
 cudaError_t launch_up_tc(const bf16* x_perm, const int32_t* offsets, const bf16* w1, const bf16* w3,
                          int A, int d, int f, int n, bf16* h, uint32_t* status,
-                         unsigned long long wait_ns, cudaStream_t s);
+                         unsigned long long wait_ns, cudaStream_t s, bf16* ab_save = nullptr,
+                         const int32_t* poff_save = nullptr);
 cudaError_t launch_down_tc(const bf16* h, const int32_t* offsets, const bf16* w2, int A, int d,
                            int f, int n, bf16* y_perm, uint32_t* status, unsigned long long wait_ns,
                            cudaStream_t s);
@@ -106,6 +109,10 @@ cudaError_t launch_router_bwd(const int32_t* idx, const float* topk_w, const int
                               int k, int dtype, void* dx, float* dl, cudaStream_t s);
 cudaError_t launch_dwg(const void* x, const float* dl, int T, int d, int n, int dtype,
                        float* part, float* dwg, float* dbias, cudaStream_t s);
+// Zero the padding rows of a padded [rows, row_elems] bf16 buffer: rows
+// [poff[e] + (off[e+1] - off[e]), poff[e+1]) of every expert.
+cudaError_t launch_zero_pad_rows(bf16* buf, const int32_t* off, const int32_t* poff, int n,
+                                 int row_elems, cudaStream_t s);
 // The backward's expert GEMMs on CUDA cores (fp32, or bf16 shapes outside the tensor-core
 // path): recompute, dy w2 with the SwiGLU backward, dx_pad, and the three weight gradients.
 int bwd_simt_ntiles(int f);

@@ -111,6 +111,17 @@ def test_host_validation_rejects_before_launch(lib):
                                   fake, fake, nul, fake, fake, fake, fake, 16, nul) == WORKSPACE
     assert lib.moe_layer_backward(fake, fake, nul, fake, fake, fake, nul, 4, 64, 64, 8, 2, 1,
                                   fake, fake, nul, fake, fake, fake, fake, 1 << 30, nul) == INVALID
+    # training pair: tensor-core shapes only; the saved buffer is checked before launch
+    assert lib.moe_train_saved_size(64, 128, 256, 8, 2, 0) == 0
+    assert lib.moe_train_saved_size(64, 96, 256, 8, 2, 1) == 0
+    assert lib.moe_train_saved_size(64, 128, 256, 8, 2, 1) >= 2 * 2 * 256 * (128 + 8 * 127)
+    assert lib.moe_layer_forward_train(fake, fake, nul, fake, fake, fake, nul, 4, 64, 64, 8, 2, 0,
+                                       fake, fake, 1 << 30, fake, 1 << 30, nul) == UNSUPPORTED
+    assert lib.moe_layer_forward_train(fake, fake, nul, fake, fake, fake, nul, 4, 64, 64, 8, 2, 1,
+                                       fake, fake, 16, fake, 1 << 30, nul) == WORKSPACE
+    assert lib.moe_layer_backward_saved(fake, fake, fake, fake, fake, fake, 4, 64, 64, 8, 2, 1,
+                                        fake, 16, fake, fake, nul, fake, fake, fake, fake,
+                                        1 << 30, nul) == WORKSPACE
     assert lib.moe_check_device_error(nul, 0, nul) == WORKSPACE
     lib.moe_set_wait_limit_ns(0)
 

@@ -163,3 +163,34 @@ def test_full_size_backward(moe, wid):
     assert_close_rel(to_numpy_f32(out["dx"])[sample], dx_ref[sample], tol, "dx (token sample)")
     assert_close_rel(out["dw_gate"].cpu().numpy(), x.T @ dl, tol, "dw_gate")
     assert_close_rel(out["dlogit_bias"].cpu().numpy(), dl.sum(axis=0), tol, "dlogit_bias")
+
+
+@pytest.mark.parametrize("name", ["t300-d256-f384-skew", "t640-d384-f320-skew", "t5-empty-experts",
+                                  "n32-k2-t500", "t1100-d512-f768"])
+def test_training_pair_matches_the_separate_calls(moe, name):
+    """moe_layer_forward_train gives moe_layer_forward's y bit for bit, and
+    moe_layer_backward_saved the gradients of moe_layer_backward (which recomputes a | b with
+    the same tile shapes and reduction order), bit for bit; both match the oracle."""
+    T, d, f, n, k, skew = CASES[name][:6]
+    w = workloads.custom(T, d, f, n, k, "bf16", wid=700 + sorted(CASES).index(name), skew_bias=skew)
+    inp = workloads.make_inputs(w, tensors=("x", "wg", "w1", "w3", "w2", "dy"))
+    g = {t: to_device(inp[t], w, DEV) for t in ("x", "wg", "w1", "w3", "w2", "dy")}
+    bias = torch.from_numpy(inp["bias"]).to(DEV) if inp["bias"] is not None else None
+    ws = moe.workspace(T, d, f, n, k, torch.bfloat16, DEV)
+    bws = moe.backward_workspace(T, d, f, n, k, torch.bfloat16, DEV)
+    saved = moe.train_saved(T, d, f, n, k, torch.bfloat16, DEV)
+    y_ref = moe.moe_layer_forward(g["x"], g["wg"], g["w1"], g["w3"], g["w2"], k, ws, logit_bias=bias)
+    y = moe.moe_layer_forward_train(g["x"], g["wg"], g["w1"], g["w3"], g["w2"], k, ws, saved,
+                                    logit_bias=bias)
+    assert moe.moe_check_device_error(ws) == 0
+    assert torch.equal(y.view(torch.int16), y_ref.view(torch.int16))
+    a = moe.moe_layer_backward(g["x"], g["wg"], g["w1"], g["w3"], g["w2"], k, g["dy"], bws,
+                               logit_bias=bias, want_dbias=True)
+    b = moe.moe_layer_backward_saved(g["x"], g["wg"], g["w1"], g["w3"], g["w2"], k, g["dy"], saved,
+                                     bws, want_dbias=True)
+    assert moe.moe_check_device_error(bws) == 0
+    for key in a:
+        x1, x2 = a[key], b[key]
+        same = torch.equal(x1, x2) if x1.dtype == torch.float32 else \
+            torch.equal(x1.view(torch.int16), x2.view(torch.int16))
+        assert same, key

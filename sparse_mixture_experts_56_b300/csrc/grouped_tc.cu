@@ -134,9 +134,13 @@ struct Shared {
   int off[kMaxExperts + 1];
 };
 
+// Output staging for the TMA store of full tiles: 128 rows x 128 bf16 columns as two
+// 128-byte-swizzled boxes of [128 rows x 64 columns].
+constexpr uint32_t kStageOutBytes = 128 * 128 * 2;
+
 template <bool PAIR>
 constexpr size_t smem_bytes() {
-  return 1024 + (size_t)Cfg<PAIR>::kStages * Cfg<PAIR>::kStageBytes +
+  return 1024 + (size_t)Cfg<PAIR>::kStages * Cfg<PAIR>::kStageBytes + kStageOutBytes +
          sizeof(Shared<Cfg<PAIR>::kStages>);
 }
 
@@ -338,6 +342,58 @@ __device__ __forceinline__ void tmem_wait(uint32_t (&r)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" : MOE_P32(r)::"memory");
 }
 
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// 32 consecutive columns (chunk c32 of the 128 staged ones) of row r into the staging buffer:
+// box c32/2, 16-byte chunks (c32%2)*4 .. +3 of the row, at chunk ^ (r % 8) (128-byte swizzle),
+// so the 32 lanes writing 32 consecutive rows spread over all banks.
+__device__ __forceinline__ void stage_row32(uint32_t stage, int r, int c32, const float (&v)[32]) {
+  const uint32_t row = stage + (uint32_t)(c32 >> 1) * (kStageOutBytes / 2) + (uint32_t)r * 128u;
+  const int j0 = (c32 & 1) * 4;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t a = row + ((uint32_t)((j0 + i) ^ (r & 7)) << 4);
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a),
+                 "r"(pack_bf16x2(v[8 * i + 0], v[8 * i + 1])),
+                 "r"(pack_bf16x2(v[8 * i + 2], v[8 * i + 3])),
+                 "r"(pack_bf16x2(v[8 * i + 4], v[8 * i + 5])),
+                 "r"(pack_bf16x2(v[8 * i + 6], v[8 * i + 7]))
+                 : "memory");
+  }
+}
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int c0, int c1) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   (uint64_t)map),
+               "r"(src), "r"(c0), "r"(c1)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// the staging buffer may be overwritten once the stores issued so far have read it
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// barrier of the four epilogue warps only
+__device__ __forceinline__ void epilogue_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// the same barrier, returning whether `ok` holds in every epilogue thread (the four warps then
+// take the same decision, which their later barriers need)
+__device__ __forceinline__ int epilogue_all(int ok) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 q, %1, 0;\n bar.red.and.pred p, 1, 128, q;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(r)
+      : "r"(ok)
+      : "memory");
+  return (int)r;
+}
+__device__ __forceinline__ void fence_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // ------------------------------------------------------------------------------------------
 // bounded waits
 // ------------------------------------------------------------------------------------------
@@ -401,11 +457,6 @@ __device__ __forceinline__ Tile decode_tile(const int* tile_base, const int* mti
   return t;
 }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
-
 __device__ __forceinline__ void store_row32(bf16* dst, const float (&v)[32]) {
   uint4* q = reinterpret_cast<uint4*>(dst);
 #pragma unroll
@@ -444,7 +495,8 @@ __global__ void __launch_bounds__(256, 1)
     grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmA2,
                            const __grid_constant__ CUtensorMap tmB0,
-                           const __grid_constant__ CUtensorMap tmB1, const TcArgs args) {
+                           const __grid_constant__ CUtensorMap tmB1,
+                           const __grid_constant__ CUtensorMap tmOut, const TcArgs args) {
   using C = Cfg<PAIR>;
   constexpr int STAGES = C::kStages;
   static_assert(!PAIR || MODE == kSwiGLU || MODE == kDown, "the pair form serves the forward");
@@ -453,7 +505,9 @@ __global__ void __launch_bounds__(256, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;                                  // STAGES x 16 KB
   uint8_t* sB = smem + STAGES * C::kABytes;            // STAGES x B_BYTES
-  Shared<STAGES>& sh = *reinterpret_cast<Shared<STAGES>*>(smem + STAGES * C::kStageBytes);
+  const uint32_t s_out = smem_u32(smem + STAGES * C::kStageBytes);   // output staging
+  Shared<STAGES>& sh =
+      *reinterpret_cast<Shared<STAGES>*>(smem + STAGES * C::kStageBytes + kStageOutBytes);
   volatile int* abort = &sh.abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -664,7 +718,7 @@ __global__ void __launch_bounds__(256, 1)
         if (!ok) raise_abort(abort, args.status);
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
+      if (!epilogue_all(ok)) break;
       tc_fence_after();
       const int row = (int)rank * BM + r;   // row of the tile held in this TMEM lane
       const bool row_ok = MODE == kWgrad ? t.mt * BM + r < args.mdim : row < t.rows;
@@ -682,7 +736,68 @@ __global__ void __launch_bounds__(256, 1)
             mbar_arrive(tempty);
         }
       };
-      if constexpr (MODE == kSwiGLU || MODE == kStoreAB) {
+      // Full tiles of the forward GEMMs leave through shared memory and TMA stores (one
+      // elected thread issues them); the ragged last tile of an expert, whose rows past the
+      // expert's count must not be written, and the backward modes store row by row.
+      constexpr bool kStaged = MODE == kSwiGLU || MODE == kDown;
+      const bool staged = kStaged && (int)rank * BM + BM <= t.rows;
+      const bool leader = warp == 4 && lane == 0;
+      if (staged) {
+        const int orow0 = t.row0 + (int)rank * BM;
+        const int rounds = MODE == kSwiGLU ? 1 : 2;   // 128 output columns per round
+        const int col0 = MODE == kSwiGLU ? t.nt * (BN / 2) : t.nt * BN;
+        const size_t grow = (size_t)(t.row0 + row);
+#pragma unroll 1
+        for (int rd = 0; rd < rounds; ++rd) {
+          if (leader) bulk_wait_read();
+          epilogue_bar();
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            float v[32];
+            if constexpr (MODE == kSwiGLU) {
+              uint32_t a[32], b[32];
+              tmem_ld32(tb + c * 32, a);
+              tmem_ld32(tb + BN / 2 + c * 32, b);
+              tmem_wait(a);
+              tmem_wait(b);
+              if (c == 3) release_acc();
+              if (args.ab_save && col0 + c * 32 < args.ndim) {
+                const size_t q = (size_t)(args.poff_save[t.e] + (int)grow - sh.off[t.e]);
+                bf16* o = args.ab_save + q * 2 * args.ndim + col0 + c * 32;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(a[j]);
+                store_row32(o, v);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(b[j]);
+                store_row32(o + args.ndim, v);
+              }
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                const float av = __uint_as_float(a[j]);
+                const float bv = __uint_as_float(b[j]);
+                v[j] = av / (1.0f + __expf(-av)) * bv;
+              }
+            } else {
+              uint32_t a[32];
+              const int cc = rd * 4 + c;
+              tmem_ld32(tb + cc * 32, a);
+              tmem_wait(a);
+              if (cc == BN / 32 - 1) release_acc();
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(a[j]);
+            }
+            stage_row32(s_out, r, c, v);
+          }
+          fence_async_smem();
+          epilogue_bar();
+          if (leader) {
+            const int cb = col0 + rd * 128;
+            if (cb < args.ndim) tma_store_2d(&tmOut, s_out, cb, orow0);
+            if (cb + 64 < args.ndim) tma_store_2d(&tmOut, s_out + kStageOutBytes / 2, cb + 64, orow0);
+            bulk_commit();
+          }
+        }
+      } else if constexpr (MODE == kSwiGLU || MODE == kStoreAB) {
         const int col0 = t.nt * (BN / 2);
         const size_t grow = (size_t)(t.row0 + row);
 #pragma unroll 1
@@ -790,6 +905,8 @@ __global__ void __launch_bounds__(256, 1)
         acc_phase ^= 1u;
       }
     }
+    // the TMA stores must finish reading the staging buffer (and land) before the CTA exits
+    if (warp == 4 && lane == 0) bulk_wait_all();
   }
 
   __syncwarp();
@@ -904,19 +1021,20 @@ inline bool want_pair(int A, int n) {
 // Single-CTA launch over at most `tiles` tiles.
 template <int MODE>
 cudaError_t launch_single(const CUtensorMap& mA, const CUtensorMap& mA2, const CUtensorMap& mB0,
-                          const CUtensorMap& mB1, const TcArgs& a, long long tiles,
-                          cudaStream_t s) {
+                          const CUtensorMap& mB1, const CUtensorMap& mOut, const TcArgs& a,
+                          long long tiles, cudaStream_t s) {
   cudaError_t e = set_smem_attr<MODE, false>();
   if (e != cudaSuccess) return e;
   const int sms = device_sm_count();
   const int grid = (int)(tiles < sms ? (tiles > 0 ? tiles : 1) : sms);
-  grouped_gemm_tc_kernel<MODE, false><<<grid, 256, smem_bytes<false>(), s>>>(mA, mA2, mB0, mB1, a);
+  grouped_gemm_tc_kernel<MODE, false><<<grid, 256, smem_bytes<false>(), s>>>(mA, mA2, mB0, mB1,
+                                                                           mOut, a);
   return cudaGetLastError();
 }
 
 template <int MODE>
 cudaError_t launch_gemm(const CUtensorMap& mA, const CUtensorMap& mB0, const CUtensorMap& mB1,
-                        const TcArgs& a, int A, cudaStream_t s) {
+                        const CUtensorMap& mOut, const TcArgs& a, int A, cudaStream_t s) {
   const int pairs = want_pair<MODE>(A, a.n) ? max_pairs<MODE>() : 0;
   if (pairs > 0) {
     const long long tiles = ((long long)(A + 255) / 256 + a.n) * a.ntiles;
@@ -933,10 +1051,10 @@ cudaError_t launch_gemm(const CUtensorMap& mA, const CUtensorMap& mB0, const CUt
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, grouped_gemm_tc_kernel<MODE, true>, mA, mA, mB0, mB1, a);
+    return cudaLaunchKernelEx(&cfg, grouped_gemm_tc_kernel<MODE, true>, mA, mA, mB0, mB1, mOut, a);
   }
   const long long tiles = ((long long)(A + BM - 1) / BM + a.n) * a.ntiles;
-  return launch_single<MODE>(mA, mA, mB0, mB1, a, tiles, s);
+  return launch_single<MODE>(mA, mA, mB0, mB1, mOut, a, tiles, s);
 }
 
 }  // namespace
@@ -948,10 +1066,11 @@ cudaError_t launch_up_tc(const bf16* x_perm, const int32_t* offsets, const bf16*
                          unsigned long long wait_ns, cudaStream_t s, bf16* ab_save,
                          const int32_t* poff_save) {
   if (A == 0) return cudaSuccess;
-  CUtensorMap mA, mW1, mW3;
+  CUtensorMap mA, mW1, mW3, mH;
   if (!make_map(&mA, x_perm, (uint64_t)A, (uint64_t)d, BM) ||
       !make_map(&mW1, w1, (uint64_t)n * f, (uint64_t)d, BN / 2) ||
-      !make_map(&mW3, w3, (uint64_t)n * f, (uint64_t)d, BN / 2))
+      !make_map(&mW3, w3, (uint64_t)n * f, (uint64_t)d, BN / 2) ||
+      !make_map(&mH, h, (uint64_t)A, (uint64_t)f, BM))
     return cudaErrorInvalidValue;
   TcArgs a = {};
   a.offsets = offsets;
@@ -964,7 +1083,7 @@ cudaError_t launch_up_tc(const bf16* x_perm, const int32_t* offsets, const bf16*
   a.wait_ns = wait_ns;
   a.ab_save = ab_save;
   a.poff_save = poff_save;
-  return launch_gemm<kSwiGLU>(mA, mW1, mW3, a, A, s);
+  return launch_gemm<kSwiGLU>(mA, mW1, mW3, mH, a, A, s);
 }
 
 cudaError_t launch_down_tc(const bf16* h, const int32_t* offsets, const bf16* w2, int A, int d,
@@ -973,9 +1092,10 @@ cudaError_t launch_down_tc(const bf16* h, const int32_t* offsets, const bf16* w2
   if (A == 0) return cudaSuccess;
   // the pair form loads 128 of the 256 rows of a w2 tile per CTA, the single form all 256
   const uint32_t brows = want_pair<kDown>(A, n) && max_pairs<kDown>() > 0 ? BN / 2 : BN;
-  CUtensorMap mA, mW2;
+  CUtensorMap mA, mW2, mY;
   if (!make_map(&mA, h, (uint64_t)A, (uint64_t)f, BM) ||
-      !make_map(&mW2, w2, (uint64_t)n * d, (uint64_t)f, brows))
+      !make_map(&mW2, w2, (uint64_t)n * d, (uint64_t)f, brows) ||
+      !make_map(&mY, y_perm, (uint64_t)A, (uint64_t)d, BM))
     return cudaErrorInvalidValue;
   TcArgs a = {};
   a.offsets = offsets;
@@ -986,7 +1106,7 @@ cudaError_t launch_down_tc(const bf16* h, const int32_t* offsets, const bf16* w2
   a.out = y_perm;
   a.status = status;
   a.wait_ns = wait_ns;
-  return launch_gemm<kDown>(mA, mW2, mW2, a, A, s);
+  return launch_gemm<kDown>(mA, mW2, mW2, mY, a, A, s);
 }
 
 // ------------------------------------------------------------------------------------------
@@ -1013,7 +1133,8 @@ cudaError_t launch_bwd_store_ab(const bf16* x_pad, const int32_t* poff, const bf
   a.out = ab;
   a.status = status;
   a.wait_ns = wait_ns;
-  return launch_single<kStoreAB>(mA, mA, mW1, mW3, a, (long long)(rows_max / BM) * a.ntiles, s);
+  return launch_single<kStoreAB>(mA, mA, mW1, mW3, mA, a, (long long)(rows_max / BM) * a.ntiles,
+                                 s);
 }
 
 cudaError_t launch_bwd_dh(const bf16* g_pad, const int32_t* poff, const bf16* w2, const bf16* ab,
@@ -1040,7 +1161,7 @@ cudaError_t launch_bwd_dh(const bf16* g_pad, const int32_t* poff, const bf16* w2
   a.hw = hw;
   a.status = status;
   a.wait_ns = wait_ns;
-  return launch_single<kDh>(mA, mA, mW2, mW2, a, (long long)(rows_max / BM) * a.ntiles, s);
+  return launch_single<kDh>(mA, mA, mW2, mW2, mA, a, (long long)(rows_max / BM) * a.ntiles, s);
 }
 
 cudaError_t launch_bwd_dgrad_x(const bf16* da, const bf16* db, const int32_t* poff, const bf16* w1,
@@ -1064,7 +1185,8 @@ cudaError_t launch_bwd_dgrad_x(const bf16* da, const bf16* db, const int32_t* po
   a.out = dx_pad;
   a.status = status;
   a.wait_ns = wait_ns;
-  return launch_single<kDgradX>(mDa, mDb, mW1, mW3, a, (long long)(rows_max / BM) * a.ntiles, s);
+  return launch_single<kDgradX>(mDa, mDb, mW1, mW3, mDa, a,
+                                (long long)(rows_max / BM) * a.ntiles, s);
 }
 
 cudaError_t launch_bwd_wgrad(const bf16* P, const bf16* Q, const int32_t* poff, int rows_max,
@@ -1086,7 +1208,7 @@ cudaError_t launch_bwd_wgrad(const bf16* P, const bf16* Q, const int32_t* poff, 
   a.out = dW;
   a.status = status;
   a.wait_ns = wait_ns;
-  return launch_single<kWgrad>(mP, mP, mQ, mQ, a, (long long)n * a.mtiles_w * a.ntiles, s);
+  return launch_single<kWgrad>(mP, mP, mQ, mQ, mP, a, (long long)n * a.mtiles_w * a.ntiles, s);
 }
 
 }  // namespace moe

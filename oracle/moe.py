@@ -394,3 +394,38 @@ def moe_layer_backward(x, wg, w1, w3, w2, k: int, dy, bias=None, *, idx=None):
     dx += dl @ wg.T
     return {"dx": dx, "dwg": x.T @ dl, "dw1": dw1, "dw3": dw3, "dw2": dw2,
             "dbias": dl.sum(axis=0), "dlogits": dl, "dgate": dgate}
+
+
+# ------------------------------------------------------------------------------------------
+# Attention sub-block of the decoder layer (the other half of each layer)
+# ------------------------------------------------------------------------------------------
+def attention_gqa(q, k, v, seq_len: int = 0) -> np.ndarray:
+    """Causal softmax attention with grouped key/value heads: for query head h, key/value head
+    g = h // (Hq / Hkv), token i of a sequence,
+
+        o_i = sum_{j <= i} softmax_j(q_i · k_j / sqrt(dh)) v_j
+
+    over the tokens j of the same sequence ("Mixtral of Experts" (xyznot.com summary), Método:
+    32 attention heads, 8 key-value heads, hidden 4096 — so dh = 128; newsflash.city digest:
+    the full dense 32k context, i.e. no sliding window).  The pages give no positional
+    encoding; positions enter through the causal mask only.
+    q [T, Hq, dh], k and v [T, Hkv, dh]; ``seq_len`` > 0 splits the T tokens into sequences of
+    that length (the last may be shorter), 0 means one sequence.  Returns [T, Hq, dh]."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    T, hq, dh = q.shape
+    hkv = k.shape[1]
+    if hq % hkv:
+        raise ValueError("query heads must be a multiple of key-value heads")
+    group = hq // hkv
+    S = T if seq_len <= 0 else seq_len
+    out = np.zeros_like(q)
+    for s0 in range(0, T, S):
+        s1 = min(T, s0 + S)
+        n = s1 - s0
+        causal = np.tril(np.ones((n, n), dtype=bool))
+        for h in range(hq):
+            g = h // group
+            scores = q[s0:s1, h] @ k[s0:s1, g].T / np.sqrt(dh)
+            scores = np.where(causal, scores, -np.inf)
+            out[s0:s1, h] = masked_softmax(scores) @ v[s0:s1, g]
+    return out

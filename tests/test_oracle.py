@@ -360,12 +360,42 @@ def check_backward_special_cases(o):
     assert o.silu_grad(np.array([0.0]))[0] == 0.5
 
 
+def check_attention(o):
+    rng = np.random.default_rng(80)
+    # torch's scaled_dot_product_attention (causal) on key/value heads repeated per group
+    for T, hq, hkv, dh, seq in [(37, 8, 2, 16, 0), (50, 4, 4, 8, 0), (45, 6, 3, 8, 16), (9, 4, 1, 32, 4)]:
+        q = rng.standard_normal((T, hq, dh))
+        k = rng.standard_normal((T, hkv, dh))
+        v = rng.standard_normal((T, hkv, dh))
+        out = o.attention_gqa(q, k, v, seq)
+        S = T if seq == 0 else seq
+        for s0 in range(0, T, S):
+            sl = slice(s0, min(T, s0 + S))
+            tq = torch.from_numpy(q[sl]).transpose(0, 1)                       # [hq, n, dh]
+            tk = torch.from_numpy(k[sl]).transpose(0, 1).repeat_interleave(hq // hkv, dim=0)
+            tv = torch.from_numpy(v[sl]).transpose(0, 1).repeat_interleave(hq // hkv, dim=0)
+            ref = F.scaled_dot_product_attention(tq, tk, tv, is_causal=True).transpose(0, 1)
+            np.testing.assert_allclose(out[sl], ref.numpy(), rtol=1e-11, atol=1e-12)
+    # the first token of every sequence sees only itself: o = v of its head group
+    q = rng.standard_normal((24, 4, 8))
+    k = rng.standard_normal((24, 2, 8))
+    v = rng.standard_normal((24, 2, 8))
+    out = o.attention_gqa(q, k, v, 8)
+    for s0 in (0, 8, 16):
+        for h in range(4):
+            np.testing.assert_allclose(out[s0, h], v[s0, h // 2], rtol=0, atol=1e-14)
+    # zero queries give equal weights: the mean of the causal prefix of v
+    out = o.attention_gqa(np.zeros((12, 2, 8)), k[:12, :1], v[:12, :1], 0)
+    for i in range(12):
+        np.testing.assert_allclose(out[i, 0], v[:i + 1, 0].mean(axis=0), rtol=1e-13, atol=1e-14)
+
+
 CHECKS = [check_worked_example, check_gate_invariants, check_topk_bruteforce,
           check_softmax_order_equivalence, check_single_expert_is_plain_ffn,
           check_k_equals_n_is_dense_softmax_mixture, check_sparse_equals_dense, check_grouping,
           check_silu, check_bias_enters_before_topk, check_rmsnorm, check_param_counts,
           check_locality_metric, check_routing_statistics, check_backward_finite_differences,
-          check_backward_autograd, check_backward_special_cases]
+          check_backward_autograd, check_backward_special_cases, check_attention]
 
 
 @pytest.mark.parametrize("check", CHECKS, ids=lambda c: c.__name__[6:])
@@ -474,6 +504,31 @@ def _mut_swiglu_bwd_swapped_branches(xs, do, w1_e, w3_e, w2_e):
     return dxs, dw3, dw1, dw2
 
 
+_ORIG_ATTN = moe_oracle.attention_gqa
+
+
+def _mut_attn_heads_modulo(q, k, v, seq_len=0):
+    hq, hkv = np.asarray(q).shape[1], np.asarray(k).shape[1]
+    perm = [h % hkv * (hq // hkv) + h // hkv for h in range(hq)]   # query head h -> group h % hkv
+    out = _ORIG_ATTN(np.asarray(q)[:, perm], k, v, seq_len)
+    inv = np.argsort(perm)
+    return out[:, inv]
+
+
+def _mut_attn_no_scale(q, k, v, seq_len=0):
+    dh = np.asarray(q).shape[2]
+    return _ORIG_ATTN(np.asarray(q, dtype=np.float64) * np.sqrt(dh), k, v, seq_len)
+
+
+def _mut_attn_one_sequence(q, k, v, seq_len=0):
+    return _ORIG_ATTN(q, k, v, 0)
+
+
+def _mut_attn_anticausal(q, k, v, seq_len=0):
+    q, k, v = (np.asarray(a)[::-1] for a in (q, k, v))
+    return _ORIG_ATTN(q, k, v, seq_len)[::-1]
+
+
 MUTATIONS = {
     "silu->sigmoid": ("silu", _mut_sigmoid_for_silu),
     "swap w1/w3": ("expert_swiglu", _mut_swap_w1_w3),
@@ -491,6 +546,10 @@ MUTATIONS = {
     "softmax backward without centering": ("softmax_backward", _mut_softmax_bwd_no_centering),
     "dw2 layout mix-up": ("expert_swiglu_backward", _mut_swiglu_bwd_dw2_transposed),
     "dw1/dw3 swapped": ("expert_swiglu_backward", _mut_swiglu_bwd_swapped_branches),
+    "attention heads grouped modulo": ("attention_gqa", _mut_attn_heads_modulo),
+    "attention without 1/sqrt(dh)": ("attention_gqa", _mut_attn_no_scale),
+    "attention across sequences": ("attention_gqa", _mut_attn_one_sequence),
+    "attention anti-causal": ("attention_gqa", _mut_attn_anticausal),
 }
 
 

@@ -257,6 +257,25 @@ moe_status moe_layer_backward_saved(const void* x, const void* w_gate, const voi
                                     size_t ws_bytes, void* stream);
 
 /*
+ * Causal grouped-query attention, the attention sub-block's core (the pages: 32 attention
+ * heads and 8 key-value heads at hidden size 4096, i.e. head dimension 128, over the full
+ * dense 32k context; "Mixtral of Experts", Método; newsflash.city digest):
+ *     out[t, h] = sum_{s <= t, same sequence} softmax_s(q[t, h] · k[s, g] / sqrt(dh)) v[s, g]
+ * with g = h / (hq / hkv).  The pages give no positional encoding; positions enter through
+ * the causal mask only.
+ *   q, out      [T, hq, dh] bf16;   k, v  [T, hkv, dh] bf16   (dense, 16-byte aligned)
+ *   seq_len     0: the T tokens are one sequence; > 0: sequences of seq_len tokens (the last
+ *               may be shorter), attention never crosses a sequence boundary
+ *   ws          any workspace of at least 256 bytes (its status word reports timeouts)
+ * fp32 scores and softmax (online, exp2), P rounded to bf16 for the P·V product, fp32
+ * accumulation in TMEM, one rounding of the output.  Only dtype MOE_BF16 with dh = 128 is
+ * implemented (MOE_ERR_UNSUPPORTED otherwise).
+ */
+moe_status moe_attention_gqa(const void* q, const void* k, const void* v, int T, int seq_len,
+                             int hq, int hkv, int dh, int dtype, void* out, void* ws,
+                             size_t ws_bytes, void* stream);
+
+/*
  * Routing statistics of one layer from its TopK selections (newsflash.city digest,
  * "路径分析", Table 5: how often consecutive tokens are sent to the same expert;
  * "Mixtral of Experts" (xyznot.com summary), "Limitaciones": 28.4% first-choice repetition

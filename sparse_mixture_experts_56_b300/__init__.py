@@ -22,7 +22,7 @@ __all__ = [
     "moe_router_topk", "moe_permute", "moe_permute_noalloc", "moe_grouped_swiglu", "moe_expert_up", "moe_expert_down",
     "moe_combine", "moe_rmsnorm", "moe_routing_stats", "moe_backward_workspace_size",
     "backward_workspace", "moe_layer_backward", "moe_train_saved_size", "train_saved",
-    "moe_layer_forward_train", "moe_layer_backward_saved",
+    "moe_layer_forward_train", "moe_layer_backward_saved", "moe_attention_gqa",
     "moe_layer_forward", "moe_check_device_error", "moe_set_wait_limit_ns", "moe_set_tc_form",
     "MOE_TC_FORM_AUTO", "MOE_TC_FORM_SINGLE", "MOE_TC_FORM_PAIR", "moe_version",
     "library_path",
@@ -334,4 +334,18 @@ def moe_layer_backward_saved(x: torch.Tensor, w_gate: torch.Tensor, w1: torch.Te
         _ptr(out.get("dlogit_bias")), _ptr(out["dw1"]), _ptr(out["dw3"]), _ptr(out["dw2"]),
         _ptr(ws), ws.numel(), _stream(stream))
     check("moe_layer_backward_saved", st)
+    return out
+
+
+def moe_attention_gqa(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, ws: torch.Tensor,
+                      seq_len: int = 0, *, out: Optional[torch.Tensor] = None, stream=None):
+    """Causal grouped-query attention: q [T, hq, dh], k and v [T, hkv, dh] -> [T, hq, dh]."""
+    T, hq, dh = q.shape
+    hkv = k.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    st = _native.lib().moe_attention_gqa(_ptr(q), _ptr(k), _ptr(v), T, int(seq_len), hq, hkv, dh,
+                                         dtype_code(q.dtype), _ptr(out), _ptr(ws), ws.numel(),
+                                         _stream(stream))
+    check("moe_attention_gqa", st)
     return out

@@ -43,6 +43,7 @@ SIGNATURES = {
     "moe_layer_forward": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P,
                                _SZ, _P]),
     "moe_routing_stats": (_I, [_P, _I, _I, _I, _I, _P, _P, _P]),
+    "moe_attention_gqa": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P]),
     "moe_backward_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "moe_train_saved_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "moe_layer_forward_train": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _SZ,

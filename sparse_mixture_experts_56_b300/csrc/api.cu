@@ -543,6 +543,22 @@ moe_status moe_layer_backward_saved(const void* x, const void* w_gate, const voi
                        dw1, dw3, dw2, ws, B, r, reinterpret_cast<const bf16*>(sv + S.ab), s);
 }
 
+moe_status moe_attention_gqa(const void* q, const void* k, const void* v, int T, int seq_len,
+                             int hq, int hkv, int dh, int dtype, void* out, void* ws,
+                             size_t ws_bytes, void* stream) {
+  if (!dtype_ok(dtype) || T < 0 || seq_len < 0 || hq < 1 || hkv < 1 || dh < 1 || hq % hkv)
+    return MOE_ERR_INVALID_ARG;
+  if ((long long)T * hq * dh >= (1ll << 40)) return MOE_ERR_INVALID_ARG;
+  if (dtype != MOE_BF16 || dh != 128) return MOE_ERR_UNSUPPORTED;
+  if (!ws || ws_bytes < kAlign || !aligned16(ws)) return MOE_ERR_WORKSPACE;
+  if (T == 0) return MOE_OK;
+  if (!q || !k || !v || !out || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_attention_gqa((const bf16*)q, (const bf16*)k, (const bf16*)v, T,
+                                          seq_len, hq, hkv, (bf16*)out, status_word(ws),
+                                          g_wait_ns.load(), (cudaStream_t)stream));
+}
+
 moe_status moe_routing_stats(const int32_t* topk_idx, int T, int k, int n, int seq_len,
                              int64_t* expert_counts, int64_t* pair_counts, void* stream) {
   if (!sizes_ok(T, 1, 1, n, k) || seq_len < 0) return MOE_ERR_INVALID_ARG;

@@ -123,6 +123,11 @@ cudaError_t launch_bwd_experts_simt(const void* x_pad, const void* g_pad, const 
                                     void* dx_pad, void* dw1, void* dw3, void* dw2,
                                     cudaStream_t s);
 
+// Causal grouped-query attention, head dimension 128, bf16 (attention.cu).
+cudaError_t launch_attention_gqa(const bf16* q, const bf16* k, const bf16* v, int T, int seq_len,
+                                 int hq, int hkv, bf16* out, uint32_t* status,
+                                 unsigned long long wait_ns, cudaStream_t s);
+
 // Which tensor-core GEMM form the launchers pick (MOE_TC_FORM_*; process-wide).
 void set_tc_form(int form);
 

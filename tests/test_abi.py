@@ -122,6 +122,12 @@ def test_host_validation_rejects_before_launch(lib):
     assert lib.moe_layer_backward_saved(fake, fake, fake, fake, fake, fake, 4, 64, 64, 8, 2, 1,
                                         fake, 16, fake, fake, nul, fake, fake, fake, fake,
                                         1 << 30, nul) == WORKSPACE
+    # attention: head dimension 128 in bf16 only; grouping and workspace checked first
+    assert lib.moe_attention_gqa(fake, fake, fake, 8, 0, 8, 3, 128, 1, fake, fake, 256, nul) == INVALID
+    assert lib.moe_attention_gqa(fake, fake, fake, 8, 0, 8, 2, 64, 1, fake, fake, 256, nul) == UNSUPPORTED
+    assert lib.moe_attention_gqa(fake, fake, fake, 8, 0, 8, 2, 128, 0, fake, fake, 256, nul) == UNSUPPORTED
+    assert lib.moe_attention_gqa(fake, fake, fake, 8, 0, 8, 2, 128, 1, fake, fake, 16, nul) == WORKSPACE
+    assert lib.moe_attention_gqa(nul, fake, fake, 8, 0, 8, 2, 128, 1, fake, fake, 256, nul) == INVALID
     assert lib.moe_check_device_error(nul, 0, nul) == WORKSPACE
     lib.moe_set_wait_limit_ns(0)
 

@@ -1,0 +1,71 @@
+"""GPU parity of the causal grouped-query attention kernel against the fp64 oracle: head
+dimension 128, query / key-value head ratios 4 (the pages' 32 / 8), 1 and 8, single and
+multiple sequences with ragged ends (query and key blocks of 128), and one token.
+Tolerance: max|o - o_ref| <= 2e-2 * max|o_ref| (bf16 inputs and P, fp32 accumulation)."""
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def moe():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import sparse_mixture_experts_56_b300 as m
+    m._native.lib()
+    return m
+
+
+def _bf16(rng, shape):
+    bits = workloads.bf16_round_bits(rng.standard_normal(shape).astype(np.float32))
+    return bits, workloads.bf16_bits_to_f32(bits).astype(np.float64)
+
+
+CASES = [
+    # (T, hq, hkv, seq_len)
+    (300, 8, 2, 0),        # one ragged sequence: 3 query blocks, partial last block
+    (256, 4, 4, 0),        # plain multi-head attention
+    (1000, 8, 2, 300),     # four sequences of 300 (last 100), blocks straddle nothing
+    (640, 32, 8, 0),       # the pages' head counts
+    (130, 8, 1, 0),        # one key-value head
+    (1, 4, 1, 0),          # a single token attends to itself
+    (2048, 32, 8, 2048),   # a long sequence: 16 key blocks for the last query block
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "T{}-hq{}-hkv{}-s{}".format(*c))
+def test_attention_matches_oracle(moe, case):
+    T, hq, hkv, seq = case
+    rng = np.random.default_rng(T * 7 + hq)
+    qb, q = _bf16(rng, (T, hq, 128))
+    kb, k = _bf16(rng, (T, hkv, 128))
+    vb, v = _bf16(rng, (T, hkv, 128))
+    dev = lambda b: torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).to(DEV)
+    ws = torch.zeros(256, dtype=torch.uint8, device=DEV)
+    out = moe.moe_attention_gqa(dev(qb), dev(kb), dev(vb), ws, seq)
+    assert moe.moe_check_device_error(ws) == 0
+    got = out.float().cpu().numpy().astype(np.float64)
+    ref = oracle.attention_gqa(q, k, v, seq)
+    err = np.max(np.abs(got - ref))
+    assert np.all(np.isfinite(got))
+    assert err <= 2e-2 * np.max(np.abs(ref)), f"max err {err:.3e} vs scale {np.max(np.abs(ref)):.3e}"
+
+
+def test_attention_is_deterministic(moe):
+    T, hq, hkv = 700, 8, 2
+    rng = np.random.default_rng(5)
+    qb, _ = _bf16(rng, (T, hq, 128))
+    kb, _ = _bf16(rng, (T, hkv, 128))
+    vb, _ = _bf16(rng, (T, hkv, 128))
+    dev = lambda b: torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).to(DEV)
+    ws = torch.zeros(256, dtype=torch.uint8, device=DEV)
+    a = moe.moe_attention_gqa(dev(qb), dev(kb), dev(vb), ws)
+    b = moe.moe_attention_gqa(dev(qb), dev(kb), dev(vb), ws)
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))

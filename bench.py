@@ -49,9 +49,13 @@ def parse():
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
-    p.add_argument("--pass", dest="which", default="forward", choices=["forward", "backward", "train"],
+    p.add_argument("--pass", dest="which", default="forward",
+                   choices=["forward", "backward", "train", "attention"],
                    help="time the layer's forward (default), its backward (moe_layer_backward), "
-                        "or a training step (moe_layer_forward_train + moe_layer_backward_saved)")
+                        "a training step (moe_layer_forward_train + moe_layer_backward_saved), or "
+                        "the causal grouped-query attention of the layer's other sub-block")
+    p.add_argument("--seq-len", type=int, default=0,
+                   help="--pass attention: tokens per sequence (0: the workload's T)")
     return p.parse_args()
 
 
@@ -686,6 +690,69 @@ def backward_arm(args, w, dist):
         print(json.dumps(line), flush=True)
 
 
+def attention_arm(args, w, dist):
+    """Times moe_attention_gqa on the workload's tokens with the pages' head counts (32 query,
+    8 key-value heads of 128): one step = causal attention over every sequence."""
+    import torch
+    import sparse_mixture_experts_56_b300 as moe
+
+    dev = torch.device("cuda", dist.local)
+    torch.cuda.set_device(dev)
+    moe._native.lib()
+    T, hq, hkv, dh = w.T, 32, 8, 128
+    seq = args.seq_len if args.seq_len > 0 else T
+    g = torch.Generator(device="cpu").manual_seed(args.seed)
+    q = torch.randn((T, hq, dh), generator=g).to(torch.bfloat16).to(dev)
+    k = torch.randn((T, hkv, dh), generator=g).to(torch.bfloat16).to(dev)
+    v = torch.randn((T, hkv, dh), generator=g).to(torch.bfloat16).to(dev)
+    out = torch.empty_like(q)
+    ws = torch.zeros(256, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(max(3, args.warmup)):
+        moe.moe_attention_gqa(q, k, v, ws, seq, out=out)
+    if moe.moe_check_device_error(ws) != 0:
+        raise SystemExit("device status set after warm-up")
+    sampler = ClockSampler(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    e0.record(stream)
+    for _ in range(args.steps):
+        moe.moe_attention_gqa(q, k, v, ws, seq, out=out)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    sampler.stop()
+    dist.barrier()
+    if moe.moe_check_device_error(ws) != 0:
+        raise SystemExit("device status set in the timed region")
+    ms = dist.max(e0.elapsed_time(e1)) / args.steps
+    # causal FLOPs: 2 products (Q K^T, P V) x 2 FLOP x dh x the (i, j <= i) pairs, per head
+    pairs = 0
+    for s0 in range(0, T, seq):
+        m = min(seq, T - s0)
+        pairs += m * (m + 1) // 2
+    flops = 4.0 * dh * hq * pairs
+    pk, pk_kind = peaks()
+    tc_peak = float(pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    ach = flops / (ms / 1e3) / 1e12
+    line = {"metric": METRIC, "pass": "attention", "value": T * dist.world / (ms / 1e3),
+            "unit": "tokens/s", "n_gpus": dist.world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic (q, k, v ~ N(0,1))",
+            "config": {"workload": f"attention-gqa-t{T}-s{seq}", "T": T, "seq_len": seq,
+                       "q_heads": hq, "kv_heads": hkv, "head_dim": dh,
+                       "parallelism": f"replicas x{dist.world}"},
+            "tflops": flops * dist.world / (ms / 1e3) / 1e12,
+            "roofline": {"bound": "tensor", "achieved": ach, "peak": tc_peak, "unit": "TFLOP/s",
+                         "frac": ach / tc_peak, "traffic": None,
+                         "kernel": "attention_gqa_kernel (causal FLOPs 4*dh*hq*pairs)",
+                         "peak_source": f"{pk_kind} (MEASURED_PEAKS.json)"},
+            "gpu_launches": args.steps, "clocks": sampler.summary()}
+    if dist.rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     w = workloads.workload(args.workload)
@@ -698,6 +765,8 @@ def main():
     try:
         if args.which in ("backward", "train"):
             backward_arm(args, w, dist)
+        elif args.which == "attention":
+            attention_arm(args, w, dist)
         else:
             ours_arm(args, w, dist)
     finally:

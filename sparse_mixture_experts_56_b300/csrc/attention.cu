@@ -55,8 +55,12 @@ struct AttnShared {
   int abort;
 };
 
-// shared memory: Q | K0 | V0 | K1 | V1 | P | AttnShared, 1024-byte aligned tiles
-constexpr size_t kAttnSmem = 1024 + 6 * (size_t)kTile + sizeof(AttnShared);
+// shared memory: Q | K0 | V0 | K1 | V1 | P0 | P1 | AttnShared, 1024-byte aligned tiles
+constexpr size_t kAttnSmem = 1024 + 7 * (size_t)kTile + sizeof(AttnShared);
+// The running maximum used as the exponent's offset is raised only when a block's maximum
+// exceeds it by more than this (log2 units): P stays below 2^8, and most blocks skip the
+// rescaling of O.
+constexpr float kRescaleLog2 = 8.0f;
 
 __device__ __forceinline__ void umma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
                                          uint32_t idesc, uint32_t accumulate) {
@@ -114,8 +118,8 @@ __global__ void __launch_bounds__(256, 1)
   const uint32_t sQ = smem_u32(smem);
   const uint32_t sK[2] = {sQ + kTile, sQ + 3 * kTile};
   const uint32_t sV[2] = {sQ + 2 * kTile, sQ + 4 * kTile};
-  const uint32_t sP = sQ + 5 * kTile;
-  AttnShared& sh = *reinterpret_cast<AttnShared*>(smem + 6 * kTile);
+  const uint32_t sP[2] = {sQ + 5 * kTile, sQ + 6 * kTile};
+  AttnShared& sh = *reinterpret_cast<AttnShared*>(smem + 7 * kTile);
   volatile int* abort = &sh.abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -233,7 +237,7 @@ __global__ void __launch_bounds__(256, 1)
       for (int kk = 0; kk < kBlk / 16; ++kk) {
         const uint32_t aoff = (uint32_t)(kk >> 2) * kHalf + (uint32_t)(kk & 3) * 32;
         const uint32_t boff = (uint32_t)(kk >> 2) * kHalf + (uint32_t)(kk & 3) * 2048;
-        umma_f16(tmem + kColO, sw128_desc(sP + aoff), sw128_mn_desc(sV[st] + boff), kIdescPV,
+        umma_f16(tmem + kColO, sw128_desc(sP[st] + aoff), sw128_mn_desc(sV[st] + boff), kIdescPV,
                  (j > 0 || kk > 0) ? 1u : 0u);
       }
       umma_commit(smem_u32(&sh.o_done));
@@ -272,34 +276,66 @@ __global__ void __launch_bounds__(256, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&sh.s_empty[st]));
-      // mask (causal and sequence end), running maximum
+      // mask (causal, sequence end) on the diagonal block, or where the block passes the end
+      // of the sequence; every earlier block is entirely visible to every row
       const int k0 = j * kBlk;
       float mb = -1e30f;
+      if (j == qb || k0 + kBlk > n) {
 #pragma unroll
-      for (int i = 0; i < 128; ++i) {
-        const bool valid = (k0 + i <= qi) && (k0 + i < n);
-        sv[i] = valid ? sv[i] * args.scale_log2 : -INFINITY;
-        mb = fmaxf(mb, sv[i]);
+        for (int i = 0; i < 128; ++i) {
+          const bool valid = (k0 + i <= qi) && (k0 + i < n);
+          sv[i] = valid ? sv[i] * args.scale_log2 : -INFINITY;
+          mb = fmaxf(mb, sv[i]);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 128; ++i) {
+          sv[i] *= args.scale_log2;
+          mb = fmaxf(mb, sv[i]);
+        }
       }
-      const float m_new = fmaxf(m, mb);
-      const float corr = fast_exp2(m - m_new);
+      // lazy rescaling: raise the offset only when the block's maximum passes it by more
+      // than kRescaleLog2 (then every lane of the warp takes its own new offset)
+      float corr = 1.0f;
+      const bool rescale = __any_sync(0xffffffffu, mb > m + kRescaleLog2);
+      if (rescale) {
+        const float m_new = fmaxf(m, mb);
+        corr = fast_exp2(m - m_new);
+        m = m_new;
+      }
       float sum = 0.f;
 #pragma unroll
       for (int i = 0; i < 128; ++i) {
-        sv[i] = fast_exp2(sv[i] - m_new);
+        sv[i] = fast_exp2(sv[i] - m);
         sum += sv[i];
       }
       l = l * corr + sum;
-      m = m_new;
+      // P row (bf16) into buffer j % 2, the swizzled A tile of P V: key half c/2, 16-byte
+      // chunk ^ (r % 8).  P V of block j - 2, the buffer's previous reader, finished before
+      // the wait of the previous step.
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const uint32_t rowp = sP[st] + (uint32_t)(c >> 1) * kHalf + (uint32_t)r * 128u;
+        const int j0 = (c & 1) * 4;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float* v = &sv[c * 32 + 8 * i];
+          const uint32_t a = rowp + ((uint32_t)((j0 + i) ^ (r & 7)) << 4);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a),
+                       "r"(pack_bf16x2(v[0], v[1])), "r"(pack_bf16x2(v[2], v[3])),
+                       "r"(pack_bf16x2(v[4], v[5])), "r"(pack_bf16x2(v[6], v[7]))
+                       : "memory");
+        }
+      }
       if (j > 0) {
-        // P V of the previous block has finished with O and with the P buffer
+        // P V of the previous block has finished with O: rescale it if the offset moved
         if (!warp_wait(smem_u32(&sh.o_done), (uint32_t)(j - 1) & 1u, abort, limit, args.status,
                        lane)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        if (__any_sync(0xffffffffu, corr < 1.0f)) {
+        if (rescale) {
 #pragma unroll 1
           for (int c = 0; c < 4; ++c) {
             uint32_t u[32];
@@ -310,21 +346,6 @@ __global__ void __launch_bounds__(256, 1)
             tmem_st32(tmem + lane_base + kColO + c * 32, u);
           }
           tmem_st_wait();
-        }
-      }
-      // P row (bf16) into the swizzled A tile of P V: key half c/2, 16-byte chunk ^ (r % 8)
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const uint32_t rowp = sP + (uint32_t)(c >> 1) * kHalf + (uint32_t)r * 128u;
-        const int j0 = (c & 1) * 4;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float* v = &sv[c * 32 + 8 * i];
-          const uint32_t a = rowp + ((uint32_t)((j0 + i) ^ (r & 7)) << 4);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a),
-                       "r"(pack_bf16x2(v[0], v[1])), "r"(pack_bf16x2(v[2], v[3])),
-                       "r"(pack_bf16x2(v[4], v[5])), "r"(pack_bf16x2(v[6], v[7]))
-                       : "memory");
         }
       }
       fence_async_smem();

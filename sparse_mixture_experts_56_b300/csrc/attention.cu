@@ -5,16 +5,21 @@
 // query i of a sequence:
 //     o_i = sum_{j <= i} softmax_j(q_i · k_j / sqrt(128)) v_j
 //
-// One CTA per (sequence, query head, block of 128 queries), 256 threads, warp-specialised:
-//   warp 0      TMA producer: the Q tile once, then K and V tiles of 128 keys into a
-//               two-stage ring (K-major K tile; V as MN-major B operand).
-//   warp 1      MMA issuer: S = Q Kᵀ (M=N=K=128) into one of two TMEM score buffers, issued
-//               one block ahead, and O += P V (V MN-major) into the TMEM output accumulator.
-//   warp 2      allocates / frees the 512 TMEM columns (S0, S1, O).
-//   warps 4-7   softmax, one query row per thread: scores from TMEM, causal / sequence mask,
-//               online maximum and sum in fp32 (exp2 of log2e-scaled scores), O rescaled in
-//               TMEM when the maximum grows, P written as bf16 into shared memory (128-byte
-//               swizzle, the A operand of P V); finally O / l stored as bf16.
+// One CTA per (sequence, query head, pair of 128-query tiles), 384 threads, warp-specialised:
+//   warp 0      TMA producer: both Q tiles once, then K and V tiles of 128 keys into a
+//               two-stage ring (K-major K tile; V as MN-major B operand), shared by the tiles.
+//   warp 1      MMA issuer: per tile t, S_t = Q_t Kᵀ into TMEM, then O_t += P_t V with P_t
+//               read from TMEM (it overwrites S_t) and V MN-major.  The issue order
+//               S_0 S_1 | PV_0 S_0' | PV_1 S_1' | ... lets one tile's softmax run while the
+//               tensor cores work on the other tile.
+//   warp 2      allocates / frees the 512 TMEM columns: S/P_0, S/P_1, O_0, O_1 (128 each).
+//   warps 4-7, 8-11   softmax of tile 0 / tile 1, one query row per thread: the 128 scores
+//               of a block from TMEM into registers, causal / sequence mask on the diagonal
+//               block only, online softmax with lazy rescaling of O in TMEM (the
+//               exponent offset moves only when a block's maximum passes it by 2^8), P
+//               written as bf16 into TMEM; finally O / l stored as bf16.
+// The MMAs of one thread run in issue order, so the completion of S_t(j) also tells the
+// softmax that P_t V(j-1) has finished reading P_t and writing O_t.
 // Every wait is bounded (globaltimer) as in the expert GEMMs; a timeout sets the status bit,
 // every role stops, the MMAs in flight are drained and TMEM is freed.
 #include "moe_internal.cuh"
@@ -26,12 +31,14 @@ namespace {
 using namespace ptx;
 
 constexpr int kDh = 128;                         // head dimension
-constexpr int kBlk = 128;                        // queries per CTA = keys per block
+constexpr int kBlk = 128;                        // queries per tile = keys per block
 constexpr uint32_t kTile = 128 * 128 * 2;        // one 128 x 128 bf16 tile (32 KB)
 constexpr uint32_t kHalf = kTile / 2;            // a 128 x 64 (or 64 x 128) half tile
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColO = 256;                  // S0 at 0, S1 at 128, O at 256
+constexpr uint32_t kColS = 0, kColO = 256;       // S/P of tile t at 128 t, O of tile t at 256 + 128 t
 constexpr uint64_t kAttnDrainNs = 200ull * 1000 * 1000;
+constexpr float kRescaleLog2 = 8.0f;
+constexpr int kThreads = 384;
 
 // kind::f16, bf16 inputs, fp32 accumulation, M = N = 128; P V takes V MN-major (bit 16)
 constexpr uint32_t kIdescQK =
@@ -39,7 +46,7 @@ constexpr uint32_t kIdescQK =
 constexpr uint32_t kIdescPV = kIdescQK | (1u << 16);
 
 struct AttnArgs {
-  int T, seq_len, nseq, nqb, hq, hkv;
+  int T, seq_len, nseq, nqb, npairs, hq, hkv;
   float scale_log2;      // log2(e) / sqrt(dh)
   bf16* out;             // [T, hq, dh]
   uint32_t* status;
@@ -49,25 +56,30 @@ struct AttnArgs {
 struct AttnShared {
   uint64_t q_full;
   uint64_t kv_full[2], kv_empty[2];
-  uint64_t s_full[2], s_empty[2];
-  uint64_t p_full, o_done, drain;
+  uint64_t s_full[2], p_full[2], o_done[2];
+  uint64_t drain;
   uint32_t tmem_base;
   int abort;
 };
 
-// shared memory: Q | K0 | V0 | K1 | V1 | P0 | P1 | AttnShared, 1024-byte aligned tiles
-constexpr size_t kAttnSmem = 1024 + 7 * (size_t)kTile + sizeof(AttnShared);
-// The running maximum used as the exponent's offset is raised only when a block's maximum
-// exceeds it by more than this (log2 units): P stays below 2^8, and most blocks skip the
-// rescaling of O.
-constexpr float kRescaleLog2 = 8.0f;
+// shared memory: Q_0 | Q_1 | K0 | V0 | K1 | V1 | AttnShared, 1024-byte aligned tiles
+constexpr size_t kAttnSmem = 1024 + 6 * (size_t)kTile + sizeof(AttnShared);
 
-__device__ __forceinline__ void umma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
-                                         uint32_t idesc, uint32_t accumulate) {
+__device__ __forceinline__ void umma_ss(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                        uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
       " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// A operand from TMEM (rows in lanes, K packed two bf16 per column)
+__device__ __forceinline__ void umma_ts(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc,
+                                        uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(tmem_d),
+      "r"(tmem_a), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
@@ -88,6 +100,16 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
 }
+// 16 consecutive 32-bit columns (32 bf16 of P)
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15])
+      : "memory");
+}
 __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -97,7 +119,7 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
-// A lane of the softmax warps waits on `bar` for the warp (lane 0 polls); false on timeout.
+// Lane 0 of a softmax warp waits on `bar` for the warp; false on timeout.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort,
                                           uint64_t limit, uint32_t* status, int lane) {
   int ok = 1;
@@ -108,31 +130,33 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     attention_gqa_kernel(const __grid_constant__ CUtensorMap tmQ,
                          const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const AttnArgs args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  const uint32_t sQ = smem_u32(smem);
-  const uint32_t sK[2] = {sQ + kTile, sQ + 3 * kTile};
-  const uint32_t sV[2] = {sQ + 2 * kTile, sQ + 4 * kTile};
-  const uint32_t sP[2] = {sQ + 5 * kTile, sQ + 6 * kTile};
-  AttnShared& sh = *reinterpret_cast<AttnShared*>(smem + 7 * kTile);
+  const uint32_t sQ[2] = {smem_u32(smem), smem_u32(smem) + kTile};
+  const uint32_t sK[2] = {sQ[0] + 2 * kTile, sQ[0] + 4 * kTile};
+  const uint32_t sV[2] = {sQ[0] + 3 * kTile, sQ[0] + 5 * kTile};
+  AttnShared& sh = *reinterpret_cast<AttnShared*>(smem + 6 * kTile);
   volatile int* abort = &sh.abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // work unit: heavy (late) query blocks first
-  const int per_seq = args.nqb * args.hq;
+  // work unit: query tiles 2p and 2p + 1 (the second may lie past the sequence), heavy first
+  const int per_seq = args.npairs * args.hq;
   const int seq = blockIdx.x / per_seq;
   const int rem = blockIdx.x - seq * per_seq;
-  const int h = rem / args.nqb;
-  const int qb = args.nqb - 1 - (rem - h * args.nqb);
+  const int h = rem / args.npairs;
+  const int pr = args.npairs - 1 - (rem - h * args.npairs);
   const int g = h / (args.hq / args.hkv);
   const int s0 = seq * args.seq_len;                           // first token of the sequence
   const int n = min(args.seq_len, args.T - s0);                // tokens of the sequence
-  const int nkv = qb + 1;                                      // key blocks 0 .. qb (causal)
+  const int qbt[2] = {2 * pr, 2 * pr + 1};
+  const int ntiles = qbt[1] < args.nqb ? 2 : 1;
+  const int nkvt[2] = {qbt[0] + 1, ntiles == 2 ? qbt[1] + 1 : 0};   // causal key blocks
+  const int nkv = ntiles == 2 ? nkvt[1] : nkvt[0];
   const uint64_t limit = args.wait_ns;
 
   if (threadIdx.x == 0) {
@@ -142,10 +166,9 @@ __global__ void __launch_bounds__(256, 1)
       mbar_init(smem_u32(&sh.kv_full[s]), 1);
       mbar_init(smem_u32(&sh.kv_empty[s]), 1);
       mbar_init(smem_u32(&sh.s_full[s]), 1);
-      mbar_init(smem_u32(&sh.s_empty[s]), 4);
+      mbar_init(smem_u32(&sh.p_full[s]), 4);
+      mbar_init(smem_u32(&sh.o_done[s]), 1);
     }
-    mbar_init(smem_u32(&sh.p_full), 4);
-    mbar_init(smem_u32(&sh.o_done), 1);
     mbar_init(smem_u32(&sh.drain), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -168,9 +191,11 @@ __global__ void __launch_bounds__(256, 1)
     prefetch_map(&tmK);
     prefetch_map(&tmV);
     const uint32_t qf = smem_u32(&sh.q_full);
-    mbar_expect_tx(qf, kTile);
-    tma_load_2d(sQ, &tmQ, qf, h * kDh, s0 + qb * kBlk);
-    tma_load_2d(sQ + kHalf, &tmQ, qf, h * kDh + 64, s0 + qb * kBlk);
+    mbar_expect_tx(qf, (uint32_t)ntiles * kTile);
+    for (int t = 0; t < ntiles; ++t) {
+      tma_load_2d(sQ[t], &tmQ, qf, h * kDh, s0 + qbt[t] * kBlk);
+      tma_load_2d(sQ[t] + kHalf, &tmQ, qf, h * kDh + 64, s0 + qbt[t] * kBlk);
+    }
     uint32_t issued = 0, iphase = 0;
     for (int j = 0; j < nkv; ++j) {
       const int st = j & 1;
@@ -203,12 +228,10 @@ __global__ void __launch_bounds__(256, 1)
     bool ok = wait_phase(smem_u32(&sh.q_full), 0, abort, limit);
     bool any = false;
     if (!ok) raise_abort(abort, args.status);
-    // S_j = Q K_jᵀ into score buffer j % 2
-    auto issue_s = [&](int j) -> bool {
+    // S_t(j) = Q_t K_jᵀ (the K/V stage of block j must have landed)
+    auto issue_s = [&](int t, int j) -> bool {
       const int st = j & 1;
-      const uint32_t ph = (uint32_t)(j >> 1) & 1u;
-      if (!wait_phase(smem_u32(&sh.kv_full[st]), ph, abort, limit) ||
-          !wait_phase(smem_u32(&sh.s_empty[st]), ph ^ 1u, abort, limit)) {
+      if (!wait_phase(smem_u32(&sh.kv_full[st]), (uint32_t)(j >> 1) & 1u, abort, limit)) {
         raise_abort(abort, args.status);
         return false;
       }
@@ -216,31 +239,39 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
       for (int kk = 0; kk < kDh / 16; ++kk) {
         const uint32_t off = (uint32_t)(kk >> 2) * kHalf + (uint32_t)(kk & 3) * 32;
-        umma_f16(tmem + (uint32_t)st * 128, sw128_desc(sQ + off), sw128_desc(sK[st] + off),
-                 kIdescQK, kk > 0 ? 1u : 0u);
+        umma_ss(tmem + kColS + (uint32_t)t * 128, sw128_desc(sQ[t] + off),
+                sw128_desc(sK[st] + off), kIdescQK, kk > 0 ? 1u : 0u);
       }
-      umma_commit(smem_u32(&sh.s_full[st]));
+      umma_commit(smem_u32(&sh.s_full[t]));
       any = true;
       return true;
     };
-    if (ok) ok = issue_s(0);
+    for (int t = 0; ok && t < ntiles; ++t) ok = issue_s(t, 0);
     for (int j = 0; ok && j < nkv; ++j) {
-      if (j + 1 < nkv && !issue_s(j + 1)) break;
-      // O += P_j V_j once the softmax has written P_j (and rescaled O)
-      if (!wait_phase(smem_u32(&sh.p_full), (uint32_t)j & 1u, abort, limit)) {
-        raise_abort(abort, args.status);
-        break;
-      }
-      tc_fence_after();
       const int st = j & 1;
+      for (int t = 0; ok && t < ntiles; ++t) {
+        if (j >= nkvt[t]) continue;
+        // O_t += P_t V_j once the softmax has written P_t(j) into TMEM (and rescaled O_t)
+        if (!wait_phase(smem_u32(&sh.p_full[t]), (uint32_t)j & 1u, abort, limit)) {
+          raise_abort(abort, args.status);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
 #pragma unroll
-      for (int kk = 0; kk < kBlk / 16; ++kk) {
-        const uint32_t aoff = (uint32_t)(kk >> 2) * kHalf + (uint32_t)(kk & 3) * 32;
-        const uint32_t boff = (uint32_t)(kk >> 2) * kHalf + (uint32_t)(kk & 3) * 2048;
-        umma_f16(tmem + kColO, sw128_desc(sP[st] + aoff), sw128_mn_desc(sV[st] + boff), kIdescPV,
-                 (j > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < kBlk / 16; ++kk) {
+          const uint32_t boff = (uint32_t)(kk >> 2) * kHalf + (uint32_t)(kk & 3) * 2048;
+          umma_ts(tmem + kColO + (uint32_t)t * 128, tmem + kColS + (uint32_t)t * 128 + kk * 8,
+                  sw128_mn_desc(sV[st] + boff), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(smem_u32(&sh.o_done[t]));
+        // the next scores of this tile (after P_t V_j in issue order)
+        if (j + 1 < nkvt[t] && !issue_s(t, j + 1)) {
+          ok = false;
+          break;
+        }
       }
-      umma_commit(smem_u32(&sh.o_done));
+      if (!ok) break;
       umma_commit(smem_u32(&sh.kv_empty[st]));
     }
     if (any) {
@@ -248,37 +279,35 @@ __global__ void __launch_bounds__(256, 1)
       if (!drain_phase(smem_u32(&sh.drain), 0, kAttnDrainNs)) atomicOr(args.status, kDevErrTimeout);
     }
   } else if (warp >= 4) {
-    // ---------------------------------------------------------------- softmax
-    const int q = warp - 4;
-    const int r = q * 32 + lane;                    // query row of the tile (TMEM lane)
-    const int qi = qb * kBlk + r;                   // query index within the sequence
+    // ---------------------------------------------------------------- softmax of tile t
+    const int t = (warp - 4) >> 2;
+    const int q = warp & 3;                          // TMEM lane quarter of this warp
+    const int r = q * 32 + lane;                     // query row of the tile (TMEM lane)
+    const int qb = qbt[t];
+    const int qi = qb * kBlk + r;                    // query index within the sequence
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    const uint32_t tS = tmem + lane_base + kColS + (uint32_t)t * 128;
+    const uint32_t tO = tmem + lane_base + kColO + (uint32_t)t * 128;
     float m = -1e30f, l = 0.f;
-    bool ok = true;
-    for (int j = 0; j < nkv; ++j) {
-      const int st = j & 1;
-      if (!warp_wait(smem_u32(&sh.s_full[st]), (uint32_t)(j >> 1) & 1u, abort, limit,
-                     args.status, lane)) {
+    bool ok = t < ntiles;
+    for (int j = 0; ok && j < nkvt[t]; ++j) {
+      if (!warp_wait(smem_u32(&sh.s_full[t]), (uint32_t)j & 1u, abort, limit, args.status,
+                     lane)) {
         ok = false;
         break;
       }
       tc_fence_after();
+      const int k0 = j * kBlk;
       float sv[128];
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t u[32];
-        tmem_ld32(tmem + lane_base + (uint32_t)st * 128 + c * 32, u);
+        tmem_ld32(tS + c * 32, u);
         tmem_wait(u);
 #pragma unroll
         for (int i = 0; i < 32; ++i) sv[c * 32 + i] = __uint_as_float(u[i]);
       }
-      // the score buffer may be refilled
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sh.s_empty[st]));
-      // mask (causal, sequence end) on the diagonal block, or where the block passes the end
-      // of the sequence; every earlier block is entirely visible to every row
-      const int k0 = j * kBlk;
+      // scale, mask (diagonal block or past the sequence end only) and the block's maximum
       float mb = -1e30f;
       if (j == qb || k0 + kBlk > n) {
 #pragma unroll
@@ -294,74 +323,56 @@ __global__ void __launch_bounds__(256, 1)
           mb = fmaxf(mb, sv[i]);
         }
       }
-      // lazy rescaling: raise the offset only when the block's maximum passes it by more
-      // than kRescaleLog2 (then every lane of the warp takes its own new offset)
+      // lazy rescaling of the exponent offset (warp-uniform decision, per-lane offsets)
       float corr = 1.0f;
       const bool rescale = __any_sync(0xffffffffu, mb > m + kRescaleLog2);
       if (rescale) {
         const float m_new = fmaxf(m, mb);
         corr = fast_exp2(m - m_new);
         m = m_new;
-      }
-      float sum = 0.f;
-#pragma unroll
-      for (int i = 0; i < 128; ++i) {
-        sv[i] = fast_exp2(sv[i] - m);
-        sum += sv[i];
-      }
-      l = l * corr + sum;
-      // P row (bf16) into buffer j % 2, the swizzled A tile of P V: key half c/2, 16-byte
-      // chunk ^ (r % 8).  P V of block j - 2, the buffer's previous reader, finished before
-      // the wait of the previous step.
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const uint32_t rowp = sP[st] + (uint32_t)(c >> 1) * kHalf + (uint32_t)r * 128u;
-        const int j0 = (c & 1) * 4;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float* v = &sv[c * 32 + 8 * i];
-          const uint32_t a = rowp + ((uint32_t)((j0 + i) ^ (r & 7)) << 4);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a),
-                       "r"(pack_bf16x2(v[0], v[1])), "r"(pack_bf16x2(v[2], v[3])),
-                       "r"(pack_bf16x2(v[4], v[5])), "r"(pack_bf16x2(v[6], v[7]))
-                       : "memory");
-        }
-      }
-      if (j > 0) {
-        // P V of the previous block has finished with O: rescale it if the offset moved
-        if (!warp_wait(smem_u32(&sh.o_done), (uint32_t)(j - 1) & 1u, abort, limit, args.status,
-                       lane)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        if (rescale) {
+        if (j > 0) {
+          // P_t V(j-1) finished before S_t(j) (issue order): O_t may be rescaled
 #pragma unroll 1
           for (int c = 0; c < 4; ++c) {
             uint32_t u[32];
-            tmem_ld32(tmem + lane_base + kColO + c * 32, u);
+            tmem_ld32(tO + c * 32, u);
             tmem_wait(u);
 #pragma unroll
             for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * corr);
-            tmem_st32(tmem + lane_base + kColO + c * 32, u);
+            tmem_st32(tO + c * 32, u);
           }
-          tmem_st_wait();
         }
       }
-      fence_async_smem();
+      // P = exp2(score - offset) as bf16 over the first 64 columns of S_t (columns 16c ..
+      // 16c+15 hold keys 32c .. 32c+31)
+      float sum = 0.f;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float p0 = fast_exp2(sv[c * 32 + 2 * i] - m);
+          const float p1 = fast_exp2(sv[c * 32 + 2 * i + 1] - m);
+          sum += p0 + p1;
+          pk[i] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16(tS + c * 16, pk);
+      }
+      l = l * corr + sum;
+      tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sh.p_full));
+      if (lane == 0) mbar_arrive(smem_u32(&sh.p_full[t]));
     }
-    if (ok && warp_wait(smem_u32(&sh.o_done), (uint32_t)(nkv - 1) & 1u, abort, limit, args.status,
-                        lane)) {
+    if (ok && warp_wait(smem_u32(&sh.o_done[t]), (uint32_t)(nkvt[t] - 1) & 1u, abort, limit,
+                        args.status, lane)) {
       tc_fence_after();
       const float inv = 1.0f / l;
       bf16* orow = args.out + ((size_t)(s0 + qi) * args.hq + h) * kDh;
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         uint32_t u[32];
-        tmem_ld32(tmem + lane_base + kColO + c * 32, u);
+        tmem_ld32(tO + c * 32, u);
         tmem_wait(u);
         if (qi < n) {
           uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
@@ -418,14 +429,15 @@ cudaError_t launch_attention_gqa(const bf16* q, const bf16* k, const bf16* v, in
   a.seq_len = seq_len > 0 ? seq_len : T;
   a.nseq = (T + a.seq_len - 1) / a.seq_len;
   a.nqb = (a.seq_len + kBlk - 1) / kBlk;
+  a.npairs = (a.nqb + 1) / 2;
   a.hq = hq;
   a.hkv = hkv;
   a.scale_log2 = 1.4426950408889634f / sqrtf((float)kDh);
   a.out = out;
   a.status = status;
   a.wait_ns = wait_ns;
-  const long long ctas = (long long)a.nseq * hq * a.nqb;
-  attention_gqa_kernel<<<(unsigned)ctas, 256, kAttnSmem, s>>>(mQ, mK, mV, a);
+  const long long ctas = (long long)a.nseq * hq * a.npairs;
+  attention_gqa_kernel<<<(unsigned)ctas, kThreads, kAttnSmem, s>>>(mQ, mK, mV, a);
   return cudaGetLastError();
 }
 

@@ -165,9 +165,11 @@ def test_full_size_backward(moe, wid):
     assert_close_rel(out["dlogit_bias"].cpu().numpy(), dl.sum(axis=0), tol, "dlogit_bias")
 
 
-@pytest.mark.parametrize("name", ["t300-d256-f384-skew", "t640-d384-f320-skew", "t5-empty-experts",
-                                  "n32-k2-t500", "t1100-d512-f768"])
-def test_training_pair_matches_the_separate_calls(moe, name):
+@pytest.mark.parametrize("name,form", [("t300-d256-f384-skew", 0), ("t640-d384-f320-skew", 0),
+                                       ("t5-empty-experts", 0), ("n32-k2-t500", 0),
+                                       ("t1100-d512-f768", 0), ("t1100-d512-f768", 2),
+                                       ("t300-d256-f384-skew", 2)])
+def test_training_pair_matches_the_separate_calls(moe, name, form):
     """moe_layer_forward_train gives moe_layer_forward's y bit for bit, and
     moe_layer_backward_saved the gradients of moe_layer_backward (which recomputes a | b with
     the same tile shapes and reduction order), bit for bit; both match the oracle."""
@@ -180,8 +182,12 @@ def test_training_pair_matches_the_separate_calls(moe, name):
     bws = moe.backward_workspace(T, d, f, n, k, torch.bfloat16, DEV)
     saved = moe.train_saved(T, d, f, n, k, torch.bfloat16, DEV)
     y_ref = moe.moe_layer_forward(g["x"], g["wg"], g["w1"], g["w3"], g["w2"], k, ws, logit_bias=bias)
-    y = moe.moe_layer_forward_train(g["x"], g["wg"], g["w1"], g["w3"], g["w2"], k, ws, saved,
-                                    logit_bias=bias)
+    moe.moe_set_tc_form(form)   # 2: the up-projection saves a | b from the CTA-pair form too
+    try:
+        y = moe.moe_layer_forward_train(g["x"], g["wg"], g["w1"], g["w3"], g["w2"], k, ws, saved,
+                                        logit_bias=bias)
+    finally:
+        moe.moe_set_tc_form(moe.MOE_TC_FORM_AUTO)
     assert moe.moe_check_device_error(ws) == 0
     assert torch.equal(y.view(torch.int16), y_ref.view(torch.int16))
     a = moe.moe_layer_backward(g["x"], g["wg"], g["w1"], g["w3"], g["w2"], k, g["dy"], bws,

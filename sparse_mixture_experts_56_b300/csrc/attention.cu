@@ -298,31 +298,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       const int k0 = j * kBlk;
+      // the 128 raw scores: four loads in flight, one wait
       float sv[128];
+      {
+        uint32_t u0[32], u1[32], u2[32], u3[32];
+        tmem_ld32(tS, u0);
+        tmem_ld32(tS + 32, u1);
+        tmem_ld32(tS + 64, u2);
+        tmem_ld32(tS + 96, u3);
+        tmem_wait(u0);
+        tmem_wait(u1);
+        tmem_wait(u2);
+        tmem_wait(u3);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t u[32];
-        tmem_ld32(tS + c * 32, u);
-        tmem_wait(u);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) sv[c * 32 + i] = __uint_as_float(u[i]);
+        for (int i = 0; i < 32; ++i) {
+          sv[i] = __uint_as_float(u0[i]);
+          sv[32 + i] = __uint_as_float(u1[i]);
+          sv[64 + i] = __uint_as_float(u2[i]);
+          sv[96 + i] = __uint_as_float(u3[i]);
+        }
       }
-      // scale, mask (diagonal block or past the sequence end only) and the block's maximum
-      float mb = -1e30f;
+      // mask (diagonal block or past the sequence end only) and the block's maximum, taken on
+      // the raw scores and scaled once (the scale is positive)
+      float mb = -INFINITY;
       if (j == qb || k0 + kBlk > n) {
 #pragma unroll
         for (int i = 0; i < 128; ++i) {
           const bool valid = (k0 + i <= qi) && (k0 + i < n);
-          sv[i] = valid ? sv[i] * args.scale_log2 : -INFINITY;
+          sv[i] = valid ? sv[i] : -INFINITY;
           mb = fmaxf(mb, sv[i]);
         }
       } else {
 #pragma unroll
-        for (int i = 0; i < 128; ++i) {
-          sv[i] *= args.scale_log2;
-          mb = fmaxf(mb, sv[i]);
-        }
+        for (int i = 0; i < 128; ++i) mb = fmaxf(mb, sv[i]);
       }
+      mb *= args.scale_log2;
       // lazy rescaling of the exponent offset (warp-uniform decision, per-lane offsets)
       float corr = 1.0f;
       const bool rescale = __any_sync(0xffffffffu, mb > m + kRescaleLog2);
@@ -351,8 +361,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float p0 = fast_exp2(sv[c * 32 + 2 * i] - m);
-          const float p1 = fast_exp2(sv[c * 32 + 2 * i + 1] - m);
+          const float p0 = fast_exp2(fmaf(sv[c * 32 + 2 * i], args.scale_log2, -m));
+          const float p1 = fast_exp2(fmaf(sv[c * 32 + 2 * i + 1], args.scale_log2, -m));
           sum += p0 + p1;
           pk[i] = pack_bf16x2(p0, p1);
         }

@@ -69,3 +69,33 @@ def test_attention_is_deterministic(moe):
     b = moe.moe_attention_gqa(dev(qb), dev(kb), dev(vb), ws)
     torch.cuda.synchronize()
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+@pytest.mark.slow
+def test_attention_32k_context(moe):
+    """The pages' full dense 32k context: one 32768-token sequence with 32 / 8 heads.  Rows are
+    checked where the oracle is cheap: all rows of the first 1024 tokens (the causal prefix
+    is a problem of its own), and sampled late rows, each against the plain definition over
+    its whole prefix."""
+    T, hq, hkv = 32768, 32, 8
+    rng = np.random.default_rng(32768)
+    qb, q = _bf16(rng, (T, hq, 128))
+    kb, k = _bf16(rng, (T, hkv, 128))
+    vb, v = _bf16(rng, (T, hkv, 128))
+    dev = lambda b: torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).to(DEV)
+    ws = torch.zeros(256, dtype=torch.uint8, device=DEV)
+    out = moe.moe_attention_gqa(dev(qb), dev(kb), dev(vb), ws)
+    assert moe.moe_check_device_error(ws) == 0
+    got = out.float().cpu().numpy().astype(np.float64)
+    assert np.all(np.isfinite(got))
+    pre = 1024
+    ref = oracle.attention_gqa(q[:pre], k[:pre], v[:pre])
+    assert np.max(np.abs(got[:pre] - ref)) <= 2e-2 * np.max(np.abs(ref))
+    rows = np.concatenate([[T - 1, T - 128, T // 2], rng.choice(np.arange(pre, T), size=13, replace=False)])
+    for i in rows:
+        for h in (0, 5, 17, 31):
+            g = h // 4
+            sc = k[:i + 1, g] @ q[i, h] / np.sqrt(128.0)
+            w = np.exp(sc - sc.max())
+            o = (w / w.sum()) @ v[:i + 1, g]
+            assert np.max(np.abs(got[i, h] - o)) <= 2e-2 * np.max(np.abs(o)) + 1e-3, (i, h)

@@ -6,8 +6,11 @@
 //     o_i = sum_{j <= i} softmax_j(q_i · k_j / sqrt(128)) v_j
 //
 // One CTA per (sequence, query head, pair of 128-query tiles), 384 threads, warp-specialised:
-//   warp 0      TMA producer: both Q tiles once, then K and V tiles of 128 keys into a
-//               two-stage ring (K-major K tile; V as MN-major B operand), shared by the tiles.
+//   warp 0      TMA producer: both Q tiles once, then K and V tiles of 128 keys into two-stage
+//               rings (K-major K tile; V as MN-major B operand), shared by the tiles.  K and V
+//               stages are freed separately (K once the last score product on it finished, V
+//               once the last P V did), so the next K tile is on its way a block ahead of
+//               the score product that needs it.
 //   warp 1      MMA issuer: per tile t, S_t = Q_t Kᵀ into TMEM, then O_t += P_t V with P_t
 //               read from TMEM (it overwrites S_t) and V MN-major.  The issue order
 //               S_0 S_1 | PV_0 S_0' | PV_1 S_1' | ... lets one tile's softmax run while the
@@ -55,7 +58,7 @@ struct AttnArgs {
 
 struct AttnShared {
   uint64_t q_full;
-  uint64_t kv_full[2], kv_empty[2];
+  uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
   uint64_t s_full[2], p_full[2], o_done[2];
   uint64_t drain;
   uint32_t tmem_base;
@@ -124,7 +127,7 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
                                           uint64_t limit, uint32_t* status, int lane) {
   int ok = 1;
   if (lane == 0) {
-    ok = wait_phase(bar, parity, abort, limit) ? 1 : 0;
+    ok = wait_fast(bar, parity, abort, limit) ? 1 : 0;
     if (!ok) raise_abort(abort, status);
   }
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
@@ -163,8 +166,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     sh.abort = 0;
     mbar_init(smem_u32(&sh.q_full), 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(smem_u32(&sh.kv_full[s]), 1);
-      mbar_init(smem_u32(&sh.kv_empty[s]), 1);
+      mbar_init(smem_u32(&sh.k_full[s]), 1);
+      mbar_init(smem_u32(&sh.k_empty[s]), 1);
+      mbar_init(smem_u32(&sh.v_full[s]), 1);
+      mbar_init(smem_u32(&sh.v_empty[s]), 1);
       mbar_init(smem_u32(&sh.s_full[s]), 1);
       mbar_init(smem_u32(&sh.p_full[s]), 4);
       mbar_init(smem_u32(&sh.o_done[s]), 1);
@@ -196,53 +201,76 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_load_2d(sQ[t], &tmQ, qf, h * kDh, s0 + qbt[t] * kBlk);
       tma_load_2d(sQ[t] + kHalf, &tmQ, qf, h * kDh + 64, s0 + qbt[t] * kBlk);
     }
+    // bit b of issued / iphase: barrier b (K stage 0, K stage 1, V stage 0, V stage 1) has a
+    // load in flight / the phase of its last load
     uint32_t issued = 0, iphase = 0;
     for (int j = 0; j < nkv; ++j) {
       const int st = j & 1;
       const uint32_t ph = (uint32_t)(j >> 1) & 1u;
-      if (!wait_phase(smem_u32(&sh.kv_empty[st]), ph ^ 1u, abort, limit)) {
+      const int row = s0 + j * kBlk;
+      // K: 128 keys x 128 dims as two K-major halves
+      if (!wait_fast(smem_u32(&sh.k_empty[st]), ph ^ 1u, abort, limit)) {
         raise_abort(abort, args.status);
         break;
       }
-      const uint32_t fb = smem_u32(&sh.kv_full[st]);
-      mbar_expect_tx(fb, 2 * kTile);
-      const int row = s0 + j * kBlk;
-      // K: 128 keys x 128 dims as two K-major halves
-      tma_load_2d(sK[st], &tmK, fb, g * kDh, row);
-      tma_load_2d(sK[st] + kHalf, &tmK, fb, g * kDh + 64, row);
-      // V: [key half kb][dim half nc] boxes of 64 keys x 64 dims (MN-major B operand)
-      for (int kb = 0; kb < 2; ++kb)
-        for (int nc = 0; nc < 2; ++nc)
-          tma_load_2d(sV[st] + kb * kHalf + nc * (kHalf / 2), &tmV, fb, g * kDh + 64 * nc,
-                      row + 64 * kb);
+      const uint32_t kb_bar = smem_u32(&sh.k_full[st]);
+      mbar_expect_tx(kb_bar, kTile);
+      tma_load_2d(sK[st], &tmK, kb_bar, g * kDh, row);
+      tma_load_2d(sK[st] + kHalf, &tmK, kb_bar, g * kDh + 64, row);
       issued |= 1u << st;
       iphase = (iphase & ~(1u << st)) | (ph << st);
+      // V: [key half kb][dim half nc] boxes of 64 keys x 64 dims (MN-major B operand)
+      if (!wait_fast(smem_u32(&sh.v_empty[st]), ph ^ 1u, abort, limit)) {
+        raise_abort(abort, args.status);
+        break;
+      }
+      const uint32_t vb_bar = smem_u32(&sh.v_full[st]);
+      mbar_expect_tx(vb_bar, kTile);
+      for (int kb = 0; kb < 2; ++kb)
+        for (int nc = 0; nc < 2; ++nc)
+          tma_load_2d(sV[st] + kb * kHalf + nc * (kHalf / 2), &tmV, vb_bar, g * kDh + 64 * nc,
+                      row + 64 * kb);
+      issued |= 4u << st;
+      iphase = (iphase & ~(4u << st)) | (ph << (st + 2));
     }
     drain_phase(qf, 0, kAttnDrainNs);
-    for (int s = 0; s < 2; ++s)
-      if ((issued >> s) & 1u)
-        if (!drain_phase(smem_u32(&sh.kv_full[s]), (iphase >> s) & 1u, kAttnDrainNs))
+    for (int b = 0; b < 4; ++b)
+      if ((issued >> b) & 1u) {
+        const uint32_t bar = b < 2 ? smem_u32(&sh.k_full[b]) : smem_u32(&sh.v_full[b - 2]);
+        if (!drain_phase(bar, (iphase >> b) & 1u, kAttnDrainNs))
           atomicOr(args.status, kDevErrTimeout);
+      }
   } else if (warp == 1 && lane == 0) {
     // ---------------------------------------------------------------- MMA issuer
-    bool ok = wait_phase(smem_u32(&sh.q_full), 0, abort, limit);
+    bool ok = wait_fast(smem_u32(&sh.q_full), 0, abort, limit);
     bool any = false;
     if (!ok) raise_abort(abort, args.status);
-    // S_t(j) = Q_t K_jᵀ (the K/V stage of block j must have landed)
+    int k_seen = -1, v_seen = -1;   // last block whose K / V tile is known to have landed
+    // operand descriptors built once; every tile, stage and K slice is a constant offset
+    const uint64_t dQ = sw128_desc(sQ[0]);          // Q_0 | Q_1 | K0 | V0 | K1 | V1
+    const uint64_t dV = sw128_mn_desc(sQ[0]);
+    // S_t(j) = Q_t K_jᵀ (the K stage of block j must have landed); the last tile's product
+    // frees the K stage
     auto issue_s = [&](int t, int j) -> bool {
       const int st = j & 1;
-      if (!wait_phase(smem_u32(&sh.kv_full[st]), (uint32_t)(j >> 1) & 1u, abort, limit)) {
-        raise_abort(abort, args.status);
-        return false;
+      if (j > k_seen) {
+        if (!wait_fast(smem_u32(&sh.k_full[st]), (uint32_t)(j >> 1) & 1u, abort, limit)) {
+          raise_abort(abort, args.status);
+          return false;
+        }
+        k_seen = j;
       }
       tc_fence_after();
+      const uint64_t dq = desc_add(dQ, (uint32_t)t * kTile);
+      const uint64_t dk = desc_add(dQ, (uint32_t)(2 + 2 * st) * kTile);
+      const uint32_t d_s = tmem + kColS + (uint32_t)t * 128;
 #pragma unroll
       for (int kk = 0; kk < kDh / 16; ++kk) {
         const uint32_t off = (uint32_t)(kk >> 2) * kHalf + (uint32_t)(kk & 3) * 32;
-        umma_ss(tmem + kColS + (uint32_t)t * 128, sw128_desc(sQ[t] + off),
-                sw128_desc(sK[st] + off), kIdescQK, kk > 0 ? 1u : 0u);
+        umma_ss(d_s, desc_add(dq, off), desc_add(dk, off), kIdescQK, kk > 0 ? 1u : 0u);
       }
       umma_commit(smem_u32(&sh.s_full[t]));
+      if (t == ntiles - 1) umma_commit(smem_u32(&sh.k_empty[st]));
       any = true;
       return true;
     };
@@ -251,20 +279,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int st = j & 1;
       for (int t = 0; ok && t < ntiles; ++t) {
         if (j >= nkvt[t]) continue;
-        // O_t += P_t V_j once the softmax has written P_t(j) into TMEM (and rescaled O_t)
-        if (!wait_phase(smem_u32(&sh.p_full[t]), (uint32_t)j & 1u, abort, limit)) {
+        // O_t += P_t V_j once the softmax has written P_t(j) into TMEM (and rescaled O_t) and
+        // the V tile of block j has landed
+        if (!wait_fast(smem_u32(&sh.p_full[t]), (uint32_t)j & 1u, abort, limit)) {
           raise_abort(abort, args.status);
           ok = false;
           break;
         }
+        if (j > v_seen) {
+          if (!wait_fast(smem_u32(&sh.v_full[st]), (uint32_t)(j >> 1) & 1u, abort, limit)) {
+            raise_abort(abort, args.status);
+            ok = false;
+            break;
+          }
+          v_seen = j;
+        }
         tc_fence_after();
+        const uint64_t dv = desc_add(dV, (uint32_t)(3 + 2 * st) * kTile);
+        const uint32_t d_o = tmem + kColO + (uint32_t)t * 128;
+        const uint32_t a_p = tmem + kColS + (uint32_t)t * 128;
 #pragma unroll
         for (int kk = 0; kk < kBlk / 16; ++kk) {
           const uint32_t boff = (uint32_t)(kk >> 2) * kHalf + (uint32_t)(kk & 3) * 2048;
-          umma_ts(tmem + kColO + (uint32_t)t * 128, tmem + kColS + (uint32_t)t * 128 + kk * 8,
-                  sw128_mn_desc(sV[st] + boff), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+          umma_ts(d_o, a_p + kk * 8, desc_add(dv, boff), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
         }
         umma_commit(smem_u32(&sh.o_done[t]));
+        if (t == ntiles - 1) umma_commit(smem_u32(&sh.v_empty[st]));
         // the next scores of this tile (after P_t V_j in issue order)
         if (j + 1 < nkvt[t] && !issue_s(t, j + 1)) {
           ok = false;
@@ -272,7 +312,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) break;
-      umma_commit(smem_u32(&sh.kv_empty[st]));
     }
     if (any) {
       umma_commit(smem_u32(&sh.drain));
@@ -320,18 +359,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // mask (diagonal block or past the sequence end only) and the block's maximum, taken on
       // the raw scores and scaled once (the scale is positive)
-      float mb = -INFINITY;
+      // (eight independent partial maxima and sums keep the dependent chains short)
       if (j == qb || k0 + kBlk > n) {
 #pragma unroll
         for (int i = 0; i < 128; ++i) {
           const bool valid = (k0 + i <= qi) && (k0 + i < n);
           sv[i] = valid ? sv[i] : -INFINITY;
-          mb = fmaxf(mb, sv[i]);
         }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 128; ++i) mb = fmaxf(mb, sv[i]);
       }
+      float mp[8];
+#pragma unroll
+      for (int a = 0; a < 8; ++a) mp[a] = sv[a];
+#pragma unroll
+      for (int i = 8; i < 128; ++i) mp[i & 7] = fmaxf(mp[i & 7], sv[i]);
+      float mb = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                       fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
       mb *= args.scale_log2;
       // lazy rescaling of the exponent offset (warp-uniform decision, per-lane offsets)
       float corr = 1.0f;
@@ -355,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // P = exp2(score - offset) as bf16 over the first 64 columns of S_t (columns 16c ..
       // 16c+15 hold keys 32c .. 32c+31)
-      float sum = 0.f;
+      float sp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t pk[16];
@@ -363,11 +405,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 16; ++i) {
           const float p0 = fast_exp2(fmaf(sv[c * 32 + 2 * i], args.scale_log2, -m));
           const float p1 = fast_exp2(fmaf(sv[c * 32 + 2 * i + 1], args.scale_log2, -m));
-          sum += p0 + p1;
+          sp[(2 * i) & 7] += p0;
+          sp[(2 * i + 1) & 7] += p1;
           pk[i] = pack_bf16x2(p0, p1);
         }
         tmem_st16(tS + c * 16, pk);
       }
+      const float sum = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
       l = l * corr + sum;
       tmem_st_wait();
       tc_fence_before();

@@ -74,6 +74,14 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
          (1ull << 46) | (2ull << 61);
 }
 
+// The descriptor of the same layout `bytes` further on: the start address is the low field
+// (16-byte units, shared-memory addresses below 256 KB), so a byte offset is one 64-bit add.
+// Issue loops build their descriptors once and step them this way; recomputing the full
+// descriptor before every MMA measurably slowed the MMA issue (N = 256: about 10 %).
+__device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t bytes) {
+  return desc + (uint64_t)(bytes >> 4);
+}
+
 // MN-major, 128-byte swizzle: each TMA box is 64 K-rows of 64 contiguous M/N elements (8 KB);
 // boxes for successive 64-element M/N chunks sit 8 KB apart (leading byte offset), 8-row K
 // groups 1024 bytes apart (stride byte offset).
@@ -153,6 +161,14 @@ static __device__ __noinline__ bool wait_phase(uint32_t bar, uint32_t parity, vo
     if (*abort) return false;
     if (gtimer() - t0 > limit_ns) return false;
   }
+}
+
+// wait_phase with the common case inline: a phase that has already completed costs one
+// try_wait instead of a call (the call saves and restores registers, a few hundred cycles in
+// a kernel with a large register budget).
+__device__ __forceinline__ bool wait_fast(uint32_t bar, uint32_t parity, volatile int* abort,
+                                          uint64_t limit_ns) {
+  return mbar_test(bar, parity) || wait_phase(bar, parity, abort, limit_ns);
 }
 
 // Same, ignoring the abort flag (used to drain work already in flight).

@@ -180,14 +180,17 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       "l"((uint64_t)map), "r"(bar_cluster), "r"(c0), "r"(c1)
       : "memory");
 }
-// Descriptor of the 16-deep K slice kk of an operand tile at `base`.
+// Descriptor of an operand tile at `base`, and the byte step from one 16-deep K slice to
+// the next: 16 K-rows of 128 bytes (MN-major) or 32 bytes along the swizzled row (K-major).
 template <bool MN>
-__device__ __forceinline__ uint64_t slice_desc(uint32_t base, int kk) {
+__device__ __forceinline__ uint64_t tile_desc(uint32_t base) {
   if constexpr (MN)
-    return sw128_mn_desc(base + (uint32_t)kk * 16 * 128);   // 16 K-rows of 128 bytes
+    return sw128_mn_desc(base);
   else
-    return sw128_desc(base + (uint32_t)kk * UMMA_K * 2);     // 32 bytes along the swizzled row
+    return sw128_desc(base);
 }
+template <bool MN>
+constexpr uint32_t kSliceBytes = MN ? 16 * 128 : UMMA_K * 2;
 template <int MODE, bool PAIR>
 __device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
                                           uint32_t accumulate) {
@@ -454,7 +457,7 @@ __global__ void __launch_bounds__(256, 1)
       const CUtensorMap* bmap = (MODE == kSwiGLU && PAIR && rank == 1) ? &tmB1 : &tmB0;
       const int kbs = MODE == kWgrad ? t.rows / BK : KB;
       for (int kb = 0; kb < kbs; ++kb) {
-        if (!wait_phase(smem_u32(&sh.empty[stage]), phase ^ 1u, abort, limit)) {
+        if (!wait_fast(smem_u32(&sh.empty[stage]), phase ^ 1u, abort, limit)) {
           raise_abort(abort, args.status);
           ok = false;
           break;
@@ -528,6 +531,9 @@ __global__ void __launch_bounds__(256, 1)
     int stage = 0, acc = 0;
     uint32_t phase = 0, acc_phase = 0;
     bool ok = true, any_mma = false;
+    // operand descriptors of stage 0, built once; stages and K slices are constant offsets
+    const uint64_t dA0 = tile_desc<a_mn(MODE)>(smem_u32(sA));
+    const uint64_t dB0 = tile_desc<b_mn(MODE)>(smem_u32(sB));
     for (int tile = first_tile; ok && tile < total; tile += gstride) {
       int kbs = KB;
       if (MODE == kWgrad) {
@@ -535,25 +541,26 @@ __global__ void __launch_bounds__(256, 1)
             decode_tile<MODE, C::kTileM>(sh.tile_base, sh.mtiles, sh.off, n, args.ntiles, tile);
         kbs = t.rows / BK;
       }
-      if (!wait_phase(smem_u32(&sh.tempty[acc]), acc_phase ^ 1u, abort, limit)) {
+      if (!wait_fast(smem_u32(&sh.tempty[acc]), acc_phase ^ 1u, abort, limit)) {
         raise_abort(abort, args.status);
         break;
       }
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
       for (int kb = 0; kb < kbs; ++kb) {
-        if (!wait_phase(smem_u32(&sh.full[stage]), phase, abort, limit)) {
+        if (!wait_fast(smem_u32(&sh.full[stage]), phase, abort, limit)) {
           raise_abort(abort, args.status);
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t a0 = smem_u32(sA + stage * C::kABytes);
-        const uint32_t b0 = smem_u32(sB + stage * C::kBBytes);
+        const uint64_t da = desc_add(dA0, (uint32_t)stage * C::kABytes);
+        const uint64_t db = desc_add(dB0, (uint32_t)stage * C::kBBytes);
 #pragma unroll
         for (int kk = 0; kk < BK / UMMA_K; ++kk)
-          umma_bf16<MODE, PAIR>(d_tmem, slice_desc<a_mn(MODE)>(a0, kk),
-                                slice_desc<b_mn(MODE)>(b0, kk), (kb | kk) != 0 ? 1u : 0u);
+          umma_bf16<MODE, PAIR>(d_tmem, desc_add(da, kk * kSliceBytes<a_mn(MODE)>),
+                                desc_add(db, kk * kSliceBytes<b_mn(MODE)>),
+                                (kb | kk) != 0 ? 1u : 0u);
         any_mma = true;
         umma_commit_all<PAIR>(smem_u32(&sh.empty[stage]));
         if (++stage == STAGES) {
@@ -586,7 +593,7 @@ __global__ void __launch_bounds__(256, 1)
           decode_tile<MODE, C::kTileM>(sh.tile_base, sh.mtiles, sh.off, n, args.ntiles, tile);
       int ok = 1;
       if (lane == 0) {
-        ok = wait_phase(smem_u32(&sh.tfull[acc]), acc_phase, abort, limit) ? 1 : 0;
+        ok = wait_fast(smem_u32(&sh.tfull[acc]), acc_phase, abort, limit) ? 1 : 0;
         if (!ok) raise_abort(abort, args.status);
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);

@@ -122,6 +122,31 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// max(a, b, c) in one instruction
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float m;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(m) : "f"(a), "f"(b), "f"(c));
+  return m;
+}
+__device__ __forceinline__ uint64_t pair2(float lo, float hi) {
+  return ((uint64_t)__float_as_uint(hi) << 32) | __float_as_uint(lo);
+}
+// (x0, x1) * c + n for the pairs c = (c, c), n = (n, n): one packed fp32 FMA, each half
+// rounded as fmaf
+__device__ __forceinline__ void fma2(float x0, float x1, uint64_t c2, uint64_t n2, float& y0,
+                                     float& y1) {
+  asm("{\n .reg .b64 s, r;\n mov.b64 s, {%2, %3};\n fma.rn.f32x2 r, s, %4, %5;\n"
+      " mov.b64 {%0, %1}, r;\n}\n"
+      : "=f"(y0), "=f"(y1)
+      : "f"(x0), "f"(x1), "l"(c2), "l"(n2));
+}
+// acc += (x0, x1), one packed fp32 add
+__device__ __forceinline__ void add2(uint64_t& acc, float x0, float x1) {
+  asm("{\n .reg .b64 t;\n mov.b64 t, {%1, %2};\n add.rn.f32x2 %0, %0, t;\n}\n"
+      : "+l"(acc)
+      : "f"(x0), "f"(x1));
+}
+
 // Lane 0 of a softmax warp waits on `bar` for the warp; false on timeout.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort,
                                           uint64_t limit, uint32_t* status, int lane) {
@@ -359,7 +384,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // mask (diagonal block or past the sequence end only) and the block's maximum, taken on
       // the raw scores and scaled once (the scale is positive)
-      // (eight independent partial maxima and sums keep the dependent chains short)
+      // (eight independent partial maxima, three-input max instructions, and packed
+      // two-wide fp32 FMAs and adds keep the chains short and the instruction count low)
       if (j == qb || k0 + kBlk > n) {
 #pragma unroll
         for (int i = 0; i < 128; ++i) {
@@ -369,11 +395,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       float mp[8];
 #pragma unroll
-      for (int a = 0; a < 8; ++a) mp[a] = sv[a];
+      for (int a = 0; a < 8; ++a) mp[a] = fmaxf(sv[2 * a], sv[2 * a + 1]);
 #pragma unroll
-      for (int i = 8; i < 128; ++i) mp[i & 7] = fmaxf(mp[i & 7], sv[i]);
-      float mb = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
-                       fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+      for (int i = 8; i < 64; ++i) mp[i & 7] = max3(mp[i & 7], sv[2 * i], sv[2 * i + 1]);
+      float mb = max3(max3(mp[0], mp[1], mp[2]), max3(mp[3], mp[4], mp[5]), fmaxf(mp[6], mp[7]));
       mb *= args.scale_log2;
       // lazy rescaling of the exponent offset (warp-uniform decision, per-lane offsets)
       float corr = 1.0f;
@@ -397,21 +422,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // P = exp2(score - offset) as bf16 over the first 64 columns of S_t (columns 16c ..
       // 16c+15 hold keys 32c .. 32c+31)
-      float sp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      const uint64_t c2 = pair2(args.scale_log2, args.scale_log2), n2 = pair2(-m, -m);
+      uint64_t sp[4] = {0, 0, 0, 0};
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float p0 = fast_exp2(fmaf(sv[c * 32 + 2 * i], args.scale_log2, -m));
-          const float p1 = fast_exp2(fmaf(sv[c * 32 + 2 * i + 1], args.scale_log2, -m));
-          sp[(2 * i) & 7] += p0;
-          sp[(2 * i + 1) & 7] += p1;
+          float x0, x1;
+          fma2(sv[c * 32 + 2 * i], sv[c * 32 + 2 * i + 1], c2, n2, x0, x1);
+          const float p0 = fast_exp2(x0);
+          const float p1 = fast_exp2(x1);
+          add2(sp[i & 3], p0, p1);
           pk[i] = pack_bf16x2(p0, p1);
         }
         tmem_st16(tS + c * 16, pk);
       }
-      const float sum = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
+      float sum = 0.f;
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+        sum += __uint_as_float((uint32_t)sp[a]) + __uint_as_float((uint32_t)(sp[a] >> 32));
       l = l * corr + sum;
       tmem_st_wait();
       tc_fence_before();

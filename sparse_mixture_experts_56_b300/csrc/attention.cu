@@ -6,7 +6,8 @@
 //     o_i = sum_{j <= i} softmax_j(q_i · k_j / sqrt(128)) v_j
 //
 // One CTA per (sequence, query head, pair of 128-query tiles), 384 threads, warp-specialised:
-//   warp 0      TMA producer: both Q tiles once, then K and V tiles of 128 keys into two-stage
+//   warp 0      allocates / frees the 512 TMEM columns (S/P_0, S/P_1, O_0, O_1, 128 each),
+//               then its lane 0 is the TMA producer: both Q tiles once, then K and V tiles of 128 keys into two-stage
 //               rings (K-major K tile; V as MN-major B operand), shared by the tiles.  K and V
 //               stages are freed separately (K once the last score product on it finished, V
 //               once the last P V did), so the next K tile is on its way a block ahead of
@@ -15,12 +16,16 @@
 //               read from TMEM (it overwrites S_t) and V MN-major.  The issue order
 //               S_0 S_1 | PV_0 S_0' | PV_1 S_1' | ... lets one tile's softmax run while the
 //               tensor cores work on the other tile.
-//   warp 2      allocates / frees the 512 TMEM columns: S/P_0, S/P_1, O_0, O_1 (128 each).
-//   warps 4-7, 8-11   softmax of tile 0 / tile 1, one query row per thread: the 128 scores
-//               of a block from TMEM into registers, causal / sequence mask on the diagonal
-//               block only, online softmax with lazy rescaling of O in TMEM (the
-//               exponent offset moves only when a block's maximum passes it by 2^8), P
-//               written as bf16 into TMEM; finally O / l stored as bf16.
+//   warps 2-9, 10-17   softmax of tile 0 / tile 1, two threads per query row (warps 2-5
+//               take the first 64 keys of a block, warps 6-9 the last 64, and so on; a warp
+//               reaches the TMEM lanes 32 (w mod 4) .. +31, so any four consecutive warps
+//               cover the 128 rows): the
+//               scores from TMEM into registers, causal / sequence mask on the diagonal block
+//               only, the row maximum combined through shared memory, online softmax with
+//               lazy rescaling of O in TMEM (the exponent offset moves only when a block's
+//               maximum passes it by 2^8), P written as bf16 into TMEM; finally O / l stored
+//               as bf16.  The exchange of the row maximum also orders the second half's P
+//               stores after the first half's score loads (P overwrites S columns 0-63).
 // The MMAs of one thread run in issue order, so the completion of S_t(j) also tells the
 // softmax that P_t V(j-1) has finished reading P_t and writing O_t.
 // Every wait is bounded (globaltimer) as in the expert GEMMs; a timeout sets the status bit,
@@ -41,7 +46,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0, kColO = 256;       // S/P of tile t at 128 t, O of tile t at 256 + 128 t
 constexpr uint64_t kAttnDrainNs = 200ull * 1000 * 1000;
 constexpr float kRescaleLog2 = 8.0f;
-constexpr int kThreads = 384;
+constexpr int kThreads = 576;   // 2 control warps + 2 tiles x 8 softmax warps
 
 // kind::f16, bf16 inputs, fp32 accumulation, M = N = 128; P V takes V MN-major (bit 16)
 constexpr uint32_t kIdescQK =
@@ -63,6 +68,10 @@ struct AttnShared {
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
+  // the two threads of a query row (one per column half) exchange partial maxima and sums:
+  // [tile][half][row] values and the sequence number of the exchange they belong to
+  float xval[2][2][128];
+  int xseq[2][2][128];
 };
 
 // shared memory: Q_0 | Q_1 | K0 | V0 | K1 | V1 | AttnShared, 1024-byte aligned tiles
@@ -90,27 +99,19 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
                    bar)
                : "memory");
 }
-// 32 consecutive fp32 columns of this thread's TMEM lane, written back
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, "
-      "%29, %30, %31, %32};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
-      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
-      "r"(r[29]), "r"(r[30]), "r"(r[31])
-      : "memory");
+// 8 consecutive 32-bit columns of this thread's TMEM lane, loaded (the wait is separate)
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                 "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr)
+               : "memory");
 }
-// 16 consecutive 32-bit columns (32 bf16 of P)
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+// 8 consecutive 32-bit columns (16 bf16 of P)
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
   asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-      "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-      "r"(r[15])
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
       : "memory");
 }
 __device__ __forceinline__ void tmem_st_wait() {
@@ -145,6 +146,36 @@ __device__ __forceinline__ void add2(uint64_t& acc, float x0, float x1) {
   asm("{\n .reg .b64 t;\n mov.b64 t, {%1, %2};\n add.rn.f32x2 %0, %0, t;\n}\n"
       : "+l"(acc)
       : "f"(x0), "f"(x1));
+}
+
+// The two threads of a query row swap a value: publish (v, seq), then wait (bounded) for the
+// partner's entry of the same exchange.  A warp goes on only if every lane got its value.
+__device__ __forceinline__ bool row_exchange(float* xval, volatile int* xseq, int mine,
+                                             int other, float v, int seq, float& got,
+                                             volatile int* abort, uint64_t limit,
+                                             uint32_t* status) {
+  xval[mine] = v;
+  tc_fence_before();
+  __threadfence_block();
+  xseq[mine] = seq;
+  bool ok = true;
+  if (xseq[other] != seq) {
+    const uint64_t t0 = gtimer();
+    while (xseq[other] != seq) {
+      if (*abort || gtimer() - t0 > limit) {
+        ok = false;
+        break;
+      }
+    }
+  }
+  __threadfence_block();
+  tc_fence_after();
+  got = reinterpret_cast<volatile float*>(xval)[other];
+  if (!__all_sync(0xffffffffu, ok)) {
+    if (!ok) raise_abort(abort, status);
+    return false;
+  }
+  return true;
 }
 
 // Lane 0 of a softmax warp waits on `bar` for the warp; false on timeout.
@@ -189,6 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     sh.abort = 0;
+    for (int i = 0; i < 2 * 2 * 128; ++i) (&sh.xseq[0][0][0])[i] = 0;
     mbar_init(smem_u32(&sh.q_full), 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&sh.k_full[s]), 1);
@@ -196,14 +228,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&sh.v_full[s]), 1);
       mbar_init(smem_u32(&sh.v_empty[s]), 1);
       mbar_init(smem_u32(&sh.s_full[s]), 1);
-      mbar_init(smem_u32(&sh.p_full[s]), 4);
+      mbar_init(smem_u32(&sh.p_full[s]), 8);
       mbar_init(smem_u32(&sh.o_done[s]), 1);
     }
     mbar_init(smem_u32(&sh.drain), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
-  if (warp == 2) {
+  if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(&sh.tmem_base)),
                  "r"(kTmemCols)
@@ -342,9 +374,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       umma_commit(smem_u32(&sh.drain));
       if (!drain_phase(smem_u32(&sh.drain), 0, kAttnDrainNs)) atomicOr(args.status, kDevErrTimeout);
     }
-  } else if (warp >= 4) {
+  } else if (warp >= 2) {
     // ---------------------------------------------------------------- softmax of tile t
-    const int t = (warp - 4) >> 2;
+    const int t = (warp - 2) >> 3;
+    const int hh = ((warp - 2) >> 2) & 1;            // column half: keys 64 hh .. 64 hh + 63
     const int q = warp & 3;                          // TMEM lane quarter of this warp
     const int r = q * 32 + lane;                     // query row of the tile (TMEM lane)
     const int qb = qbt[t];
@@ -354,6 +387,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tO = tmem + lane_base + kColO + (uint32_t)t * 128;
     float m = -1e30f, l = 0.f;
     bool ok = t < ntiles;
+    float* xval = &sh.xval[t][0][0];
+    volatile int* xseq = &sh.xseq[t][0][0];
+    const int xm = hh * 128 + r, xo = (hh ^ 1) * 128 + r;   // this thread's / the partner's slot
+    int seq = 0;
     for (int j = 0; ok && j < nkvt[t]; ++j) {
       if (!warp_wait(smem_u32(&sh.s_full[t]), (uint32_t)j & 1u, abort, limit, args.status,
                      lane)) {
@@ -362,43 +399,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       const int k0 = j * kBlk;
-      // the 128 raw scores: four loads in flight, one wait
-      float sv[128];
-      {
-        uint32_t u0[32], u1[32], u2[32], u3[32];
-        tmem_ld32(tS, u0);
-        tmem_ld32(tS + 32, u1);
-        tmem_ld32(tS + 64, u2);
-        tmem_ld32(tS + 96, u3);
-        tmem_wait(u0);
-        tmem_wait(u1);
-        tmem_wait(u2);
-        tmem_wait(u3);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          sv[i] = __uint_as_float(u0[i]);
-          sv[32 + i] = __uint_as_float(u1[i]);
-          sv[64 + i] = __uint_as_float(u2[i]);
-          sv[96 + i] = __uint_as_float(u3[i]);
-        }
-      }
+      // this half's 64 raw scores: two loads in flight, one wait
+      uint32_t u0[32], u1[32];
+      tmem_ld32(tS + hh * 64, u0);
+      tmem_ld32(tS + hh * 64 + 32, u1);
+      tmem_wait(u0);
+      tmem_wait(u1);
+#define SV(i) (*reinterpret_cast<float*>((i) < 32 ? &u0[(i)] : &u1[(i) - 32]))
+      const int kh = k0 + hh * 64;                   // first key of this half
       // mask (diagonal block or past the sequence end only) and the block's maximum, taken on
       // the raw scores and scaled once (the scale is positive)
       // (eight independent partial maxima, three-input max instructions, and packed
       // two-wide fp32 FMAs and adds keep the chains short and the instruction count low)
       if (j == qb || k0 + kBlk > n) {
 #pragma unroll
-        for (int i = 0; i < 128; ++i) {
-          const bool valid = (k0 + i <= qi) && (k0 + i < n);
-          sv[i] = valid ? sv[i] : -INFINITY;
+        for (int i = 0; i < 64; ++i) {
+          const bool valid = (kh + i <= qi) && (kh + i < n);
+          SV(i) = valid ? SV(i) : -INFINITY;
         }
       }
       float mp[8];
 #pragma unroll
-      for (int a = 0; a < 8; ++a) mp[a] = fmaxf(sv[2 * a], sv[2 * a + 1]);
+      for (int a = 0; a < 8; ++a) mp[a] = fmaxf(SV(2 * a), SV(2 * a + 1));
 #pragma unroll
-      for (int i = 8; i < 64; ++i) mp[i & 7] = max3(mp[i & 7], sv[2 * i], sv[2 * i + 1]);
+      for (int i = 8; i < 32; ++i) mp[i & 7] = max3(mp[i & 7], SV(2 * i), SV(2 * i + 1));
       float mb = max3(max3(mp[0], mp[1], mp[2]), max3(mp[3], mp[4], mp[5]), fmaxf(mp[6], mp[7]));
+      {
+        float mo;
+        if (!row_exchange(xval, xseq, xm, xo, mb, ++seq, mo, abort, limit, args.status)) {
+          ok = false;
+          break;
+        }
+        mb = fmaxf(mb, mo);
+      }
       mb *= args.scale_log2;
       // lazy rescaling of the exponent offset (warp-uniform decision, per-lane offsets)
       float corr = 1.0f;
@@ -408,45 +441,54 @@ __global__ void __launch_bounds__(kThreads, 1)
         corr = fast_exp2(m - m_new);
         m = m_new;
         if (j > 0) {
-          // P_t V(j-1) finished before S_t(j) (issue order): O_t may be rescaled
+          // P_t V(j-1) finished before S_t(j) (issue order): O_t may be rescaled (this
+          // half's 64 columns, 8 at a time: the scores stay in registers meanwhile)
 #pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
-            uint32_t u[32];
-            tmem_ld32(tO + c * 32, u);
-            tmem_wait(u);
+          for (int c = 8 * hh; c < 8 * hh + 8; ++c) {
+            uint32_t u[8];
+            tmem_ld8(tO + c * 8, u);
+            asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(u[0]), "+r"(u[1]), "+r"(u[2]),
+                         "+r"(u[3]), "+r"(u[4]), "+r"(u[5]), "+r"(u[6]), "+r"(u[7])::"memory");
 #pragma unroll
-            for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * corr);
-            tmem_st32(tO + c * 32, u);
+            for (int i = 0; i < 8; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * corr);
+            tmem_st8(tO + c * 8, u);
           }
         }
       }
       // P = exp2(score - offset) as bf16 over the first 64 columns of S_t (columns 16c ..
-      // 16c+15 hold keys 32c .. 32c+31)
+      // 16c+15 hold keys 32c .. 32c+31; this half writes chunks 2 hh and 2 hh + 1)
       const uint64_t c2 = pair2(args.scale_log2, args.scale_log2), n2 = pair2(-m, -m);
-      uint64_t sp[4] = {0, 0, 0, 0};
+      uint64_t sp[2] = {0, 0};
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        uint32_t pk[16];
+        uint32_t pk[8];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
+        for (int i = 0; i < 8; ++i) {
           float x0, x1;
-          fma2(sv[c * 32 + 2 * i], sv[c * 32 + 2 * i + 1], c2, n2, x0, x1);
+          fma2(SV(c * 16 + 2 * i), SV(c * 16 + 2 * i + 1), c2, n2, x0, x1);
           const float p0 = fast_exp2(x0);
           const float p1 = fast_exp2(x1);
-          add2(sp[i & 3], p0, p1);
+          add2(sp[i & 1], p0, p1);
           pk[i] = pack_bf16x2(p0, p1);
         }
-        tmem_st16(tS + c * 16, pk);
+        tmem_st8(tS + hh * 32 + c * 8, pk);
       }
       float sum = 0.f;
 #pragma unroll
-      for (int a = 0; a < 4; ++a)
+      for (int a = 0; a < 2; ++a)
         sum += __uint_as_float((uint32_t)sp[a]) + __uint_as_float((uint32_t)(sp[a] >> 32));
+#undef SV
       l = l * corr + sum;
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&sh.p_full[t]));
+    }
+    // the row sum over both halves
+    if (ok) {
+      float lo;
+      ok = row_exchange(xval, xseq, xm, xo, l, ++seq, lo, abort, limit, args.status);
+      l += lo;
     }
     if (ok && warp_wait(smem_u32(&sh.o_done[t]), (uint32_t)(nkvt[t] - 1) & 1u, abort, limit,
                         args.status, lane)) {
@@ -454,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float inv = 1.0f / l;
       bf16* orow = args.out + ((size_t)(s0 + qi) * args.hq + h) * kDh;
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 2 * hh; c < 2 * hh + 2; ++c) {
         uint32_t u[32];
         tmem_ld32(tO + c * 32, u);
         tmem_wait(u);
@@ -477,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncwarp();
   tc_fence_before();
   __syncthreads();
-  if (warp == 2) {
+  if (warp == 0) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                  "r"(kTmemCols)

@@ -71,6 +71,32 @@ def test_attention_is_deterministic(moe):
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
 
 
+def test_attention_timeout_path_reports_and_recovers(moe):
+    """A wait limit of 1 ns makes the attention's roles give up at their first wait that is not
+    already satisfied (barriers, and the exchange of row maxima between the two threads of a
+    row): the kernel must stop cleanly (status MOE_ERR_TIMEOUT), drain what it issued, free
+    its TMEM, and the next call must be correct."""
+    T, hq, hkv = 1024, 32, 8
+    rng = np.random.default_rng(11)
+    qb, q = _bf16(rng, (T, hq, 128))
+    kb, k = _bf16(rng, (T, hkv, 128))
+    vb, v = _bf16(rng, (T, hkv, 128))
+    dev = lambda b: torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).to(DEV)
+    ws = torch.zeros(256, dtype=torch.uint8, device=DEV)
+    try:
+        moe.moe_set_wait_limit_ns(1)
+        moe.moe_attention_gqa(dev(qb), dev(kb), dev(vb), ws)
+        st = moe.moe_check_device_error(ws)
+    finally:
+        moe.moe_set_wait_limit_ns(0)
+    assert st in (0, 5)   # 5 = MOE_ERR_TIMEOUT (0 only if no wait ever had to spin)
+    out = moe.moe_attention_gqa(dev(qb), dev(kb), dev(vb), ws)
+    assert moe.moe_check_device_error(ws) == 0
+    got = out.float().cpu().numpy().astype(np.float64)
+    ref = oracle.attention_gqa(q, k, v)
+    assert np.max(np.abs(got - ref)) <= 2e-2 * np.max(np.abs(ref))
+
+
 @pytest.mark.slow
 def test_attention_32k_context(moe):
     """The pages' full dense 32k context: one 32768-token sequence with 32 / 8 heads.  Rows are

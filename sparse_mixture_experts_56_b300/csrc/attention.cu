@@ -5,27 +5,27 @@
 // query i of a sequence:
 //     o_i = sum_{j <= i} softmax_j(q_i · k_j / sqrt(128)) v_j
 //
-// One CTA per (sequence, query head, pair of 128-query tiles), 384 threads, warp-specialised:
-//   warp 0      allocates / frees the 512 TMEM columns (S/P_0, S/P_1, O_0, O_1, 128 each),
-//               then its lane 0 is the TMA producer: both Q tiles once, then K and V tiles of 128 keys into two-stage
-//               rings (K-major K tile; V as MN-major B operand), shared by the tiles.  K and V
-//               stages are freed separately (K once the last score product on it finished, V
-//               once the last P V did), so the next K tile is on its way a block ahead of
-//               the score product that needs it.
+// One CTA per (sequence, query head, pair of 128-query tiles), 576 threads, warp-specialised:
+//   warp 0      allocates / frees the 512 TMEM columns (S/P_0, S/P_1, O_0, O_1, 128 each);
+//               its lane 0 is the TMA producer: both Q tiles once, then K and V tiles of 128
+//               keys into two-stage rings (K-major K tile; V as MN-major B operand), shared by
+//               the tiles.  K and V stages are freed separately (K once the last score product
+//               on it finished, V once the last P V did), so the next K tile is on its way a
+//               block ahead of the score product that needs it.
 //   warp 1      MMA issuer: per tile t, S_t = Q_t Kᵀ into TMEM, then O_t += P_t V with P_t
 //               read from TMEM (it overwrites S_t) and V MN-major.  The issue order
 //               S_0 S_1 | PV_0 S_0' | PV_1 S_1' | ... lets one tile's softmax run while the
 //               tensor cores work on the other tile.
-//   warps 2-9, 10-17   softmax of tile 0 / tile 1, two threads per query row (warps 2-5
-//               take the first 64 keys of a block, warps 6-9 the last 64, and so on; a warp
-//               reaches the TMEM lanes 32 (w mod 4) .. +31, so any four consecutive warps
-//               cover the 128 rows): the
-//               scores from TMEM into registers, causal / sequence mask on the diagonal block
-//               only, the row maximum combined through shared memory, online softmax with
-//               lazy rescaling of O in TMEM (the exponent offset moves only when a block's
-//               maximum passes it by 2^8), P written as bf16 into TMEM; finally O / l stored
-//               as bf16.  The exchange of the row maximum also orders the second half's P
-//               stores after the first half's score loads (P overwrites S columns 0-63).
+//   warps 2-9, 10-17   softmax of tile 0 / tile 1, two threads per query row (warps 2-5 take
+//               the first 64 keys of a block, warps 6-9 the last 64, and so on; a warp reaches
+//               the TMEM lanes 32 (w mod 4) .. +31, so any four consecutive warps cover the
+//               128 rows): the scores from TMEM into registers, causal / sequence mask on the
+//               diagonal block only, the row maximum combined through shared memory, online
+//               softmax with lazy rescaling of O in TMEM (the exponent offset moves only when
+//               a block's maximum passes it by 2^8), P written as bf16 into TMEM; finally
+//               O / l stored as bf16.  The exchange of the row maximum also orders the second
+//               half's P stores after the first half's score loads (P overwrites S columns
+//               0-63).
 // The MMAs of one thread run in issue order, so the completion of S_t(j) also tells the
 // softmax that P_t V(j-1) has finished reading P_t and writing O_t.
 // Every wait is bounded (globaltimer) as in the expert GEMMs; a timeout sets the status bit,

@@ -853,17 +853,20 @@ int max_pairs() {
 std::atomic<int> g_tc_form{MOE_TC_FORM_AUTO};
 
 // Unless a form was forced with moe_set_tc_form: the pair form for GEMM2 (w2) when the
-// experts hold on average at least one full 256-row tile; the single form otherwise and for
-// GEMM1.  Measured on B300 at the prefill sizes (T = 4096 and 16384, d = 4096, f = 14336,
-// clocks held down by the power cap): GEMM2 runs 3-5 % faster as pairs; GEMM1 runs 1-2 %
-// slower, its 256-row tiles wasting more rows on the experts' ragged last tiles while its
-// single-CTA form already keeps up with the L2.
+// experts hold on average at least one full 256-row tile, for GEMM1 (w1|w3 + SwiGLU) when
+// they hold at least two; the single form otherwise.  Measured on B300 with interleaved runs
+// at the prefill sizes (d = 4096, f = 14336, clocks held down by the power cap): at T = 4096
+// the pair form runs GEMM1 6 % and GEMM2 12 % faster, at T = 16384 (skewed routing) GEMM1
+// equally fast and GEMM2 9 % faster.  GEMM1's shorter reduction (K = 4096) gains less: its
+// 256-row tiles waste more rows on the experts' ragged last tiles.
 template <int MODE>
 inline bool want_pair(int A, int n) {
   const int form = g_tc_form.load(std::memory_order_relaxed);
   if (form == MOE_TC_FORM_SINGLE) return false;
   if (form == MOE_TC_FORM_PAIR) return true;
-  return MODE == kDown && (long long)A >= 256ll * n;
+  if (MODE == kDown) return (long long)A >= 256ll * n;
+  if (MODE == kSwiGLU) return (long long)A >= 512ll * n;
+  return false;
 }
 
 // Single-CTA launch over at most `tiles` tiles.

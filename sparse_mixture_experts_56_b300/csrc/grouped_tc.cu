@@ -360,7 +360,7 @@ __device__ __forceinline__ void load_row32(const bf16* src, float (&v)[32]) {
   }
 }
 
-__device__ __forceinline__ float sigmoidf_(float z) { return 1.0f / (1.0f + __expf(-z)); }
+__device__ __forceinline__ float sigmoidf_(float z) { return __fdividef(1.0f, 1.0f + __expf(-z)); }
 
 // ------------------------------------------------------------------------------------------
 // the kernel
@@ -654,7 +654,7 @@ __global__ void __launch_bounds__(256, 1)
               for (int j = 0; j < 32; ++j) {
                 const float av = __uint_as_float(a[j]);
                 const float bv = __uint_as_float(b[j]);
-                v[j] = av / (1.0f + __expf(-av)) * bv;
+                v[j] = __fdividef(av, 1.0f + __expf(-av)) * bv;
               }
             } else {
               uint32_t a[32];
@@ -704,7 +704,7 @@ __global__ void __launch_bounds__(256, 1)
               for (int j = 0; j < 32; ++j) {
                 const float av = __uint_as_float(a[j]);
                 const float bv = __uint_as_float(b[j]);
-                v[j] = av / (1.0f + __expf(-av)) * bv;
+                v[j] = __fdividef(av, 1.0f + __expf(-av)) * bv;
               }
               store_row32(args.out + grow * args.ndim + col0 + c * 32, v);
             } else {

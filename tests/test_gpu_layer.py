@@ -39,8 +39,9 @@ LAYER_CASES = {
     "tc-n32-k2": (500, 128, 128, 32, 2, "bf16", False),
     "tc-t1": (1, 256, 256, 8, 2, "bf16", False),
     "simt-bf16-d200": (64, 200, 136, 8, 2, "bf16", False),     # not a multiple of 64
-    # CTA-pair tensor-core form (chosen when the experts average >= 256 rows): 256-row tiles
-    # split over two CTAs, ragged last tiles in both CTAs of a pair
+    # CTA-pair tensor-core form (the down-projection takes it when the experts average >= 256
+    # rows, the up-projection at >= 512; pair-t2048 and pair-n1-k1 run both GEMMs as pairs):
+    # 256-row tiles split over two CTAs, ragged last tiles in both CTAs of a pair
     "pair-t2048-d256-f384": (2048, 256, 384, 8, 2, "bf16", False),
     "pair-t1500-d384-f320-skew": (1500, 384, 320, 8, 2, "bf16", True),   # partial n-tiles
     "pair-n1-k1-t700": (700, 256, 256, 1, 1, "bf16", False),            # 3 tiles, 188-row tail

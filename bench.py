@@ -10,9 +10,11 @@ synthetic input, through the C ABI of libmoe.so.  Inputs are resident in HBM whe
 timed region starts; the expert weights (2.82 GB per layer) are larger than the 126 MB
 L2, so no flush is needed between steps.  `value` is tokens/s of the whole job (all ranks).
 
-Default workload: the Mixtral-shaped decode batch (T=32 tokens, d=4096, f=14336, 8
-experts, top-2).  `--impl reference` times the fp64 CPU oracle instead (the slow
-reference arm), on a bounded sample of the same workload.
+Default workload: the largest single-layer configuration, 16384 tokens with skewed routing
+(d=4096, f=14336, 8 experts, top-2; tensor-core bound).  The same line carries, under
+"decode", the 32-token decode batch (HBM bound) measured in the same process the same way.
+`--impl reference` times the fp64 CPU oracle instead (the slow reference arm), on a bounded
+sample of the same workload.
 Under torchrun each rank runs an independent replica on its own GPU (the layer needs no
 exchange between ranks), timed with a barrier on both sides and the maximum over ranks.
 """
@@ -44,11 +46,14 @@ def parse():
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=2000)
     p.add_argument("--warmup", type=int, default=20)
-    p.add_argument("--workload", type=int, default=2, choices=sorted(workloads.WORKLOADS))
+    p.add_argument("--workload", type=int, default=4, choices=sorted(workloads.WORKLOADS))
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-decode", action="store_true",
+                   help="forward pass of a workload other than the decode batch: do not add the "
+                        "decode batch's measurement under \"decode\"")
     p.add_argument("--pass", dest="which", default="forward",
                    choices=["forward", "backward", "train", "attention"],
                    help="time the layer's forward (default), its backward (moe_layer_backward), "
@@ -185,14 +190,15 @@ class ClockSampler:
 
 
 def tensor_peak(pk, clocks):
-    """The bf16 denominator for a tensor-bound line: the sustained figure (cuBLAS held at the
-    power cap) when the run's sampled clocks show the power cap, the burst figure (cuBLAS at
-    full clock) otherwise, so that the kernel is compared with cuBLAS in the same regime."""
+    """The bf16 denominator of a tensor-bound line: cuBLAS's burst figure (a GEMM timed
+    alone at full clock), the right peak for a layer step of a few milliseconds.  The
+    sustained figure (cuBLAS held for seconds at the power cap) is returned beside it, so
+    that lines can also say how they compare with cuBLAS under the cap."""
     burst = float(pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     sus = float(pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
-    if "sw_power_cap" in (clocks.get("reasons") or []):
-        return sus, "sustained (the power cap was active in the timed region)", burst, sus
-    return burst, "burst (no power cap in the timed region)", burst, sus
+    capped = "sw_power_cap" in (clocks.get("reasons") or [])
+    kind = "burst" + (" (the power cap was active in the timed region)" if capped else "")
+    return burst, kind, burst, sus
 
 
 def peaks():
@@ -341,6 +347,23 @@ def ours_arm(args, w, dist):
     dev = torch.device("cuda", dist.local)
     torch.cuda.set_device(dev)
     moe._native.lib()
+    line = forward_line(args, w, dist, dev, with_cpu=True)
+    if w.wid != 2 and not args.no_decode:
+        # the HBM-bound decode batch, measured the same way (its own inputs, timed region,
+        # clocks, roofline and end-to-end figure), carried in the same line
+        torch.cuda.empty_cache()
+        dec = forward_line(args, workloads.workload(2), dist, dev, with_cpu=False)
+        line["decode"] = {k: dec[k] for k in ("value", "unit", "ms_per_step", "tflops", "roofline",
+                                              "e2e", "clocks", "gpu_launches", "config",
+                                              "expert_counts") if k in dec}
+    if dist.rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def forward_line(args, w, dist, dev, with_cpu):
+    """Times `args.steps` layer steps of workload `w` and returns the JSON line as a dict."""
+    import torch
+    import sparse_mixture_experts_56_b300 as moe
 
     x_h, layers_h, bias_h = host_inputs(w, args.seed)
     tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
@@ -439,7 +462,8 @@ def ours_arm(args, w, dist):
         peak, kind, burst, sus = tensor_peak(pk, clk)
         ach = up_flops / (up_ms / 1e3) / 1e12
         roof = {"bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s", "frac": ach / peak,
-                "peak_kind": kind, "frac_of_burst": ach / burst, "frac_of_sustained": ach / sus}
+                "peak_kind": kind, "frac_of_sustained": ach / sus,
+                "step_frac": flops_step / (ms_total / args.steps / 1e3) / 1e12 / peak}
     roof.update({"traffic": kernel_traffic("expert_up", w.name), "kernel": "moe_expert_up (gather + w1|w3 tcgen05 GEMM + SwiGLU)",
                  "algorithmic": up_bytes if roof["bound"] == "hbm" else up_flops,
                  "ms_per_launch": up_ms, "peak_source": f"{pk_kind} (MEASURED_PEAKS.json)" if pk_kind == "measured" else "fallback",
@@ -507,13 +531,11 @@ def ours_arm(args, w, dist):
         if moe.moe_check_device_error(ws) != 0:
             raise SystemExit("device status set in the end-to-end loop")
 
-    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
-        del layers
+    if with_cpu and dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
         xf, lf, _ = oracle_prepare(w, x_h, layers_h, bias_h)
         del layers_h
         line["cpu_baseline"] = run_cpu_baseline(w, xf, lf, bias_h)
-    if dist.rank == 0:
-        print(json.dumps(line), flush=True)
+    return line
 
 
 def routing_stats_report(moe, w, step, layer, layers, x, xn, hs, idx, off, stream):

@@ -111,7 +111,11 @@ moe_status moe_router_topk(const void* x, const void* w_gate, const float* logit
  *                  bytes (only its status header and, for large T*k, per-block counts
  *                  are used)
  * An index outside [0, n) is reported by moe_check_device_error() as
- * MOE_ERR_DEVICE_INDEX; the outputs are then undefined.
+ * MOE_ERR_DEVICE_INDEX.  Its assignment goes to a trailing bucket after the last expert:
+ * expert_offsets[n] then counts only the valid assignments, the positions
+ * [expert_offsets[n], T*k) hold the bad ones in ascending a, and perm / inv_perm remain a
+ * permutation of [0, T*k), so later calls never index out of bounds with them.  The
+ * experts skip the trailing bucket; what moe_combine reads for those slots is unspecified.
  */
 moe_status moe_permute(const int32_t* topk_idx, int T, int k, int n, int32_t* expert_offsets,
                        int32_t* perm, int32_t* inv_perm, void* ws, size_t ws_bytes, void* stream);
@@ -122,15 +126,16 @@ moe_status moe_permute(const int32_t* topk_idx, int T, int k, int n, int32_t* ex
  * over — for example code that runs while a stream is being captured into a CUDA graph, or
  * inside a host runtime's enqueue callback, where cudaMalloc is not allowed.  Same inputs,
  * outputs and results as moe_permute.  Its scratch (a status word and the per-block counts)
- * is a fixed 33,024-byte array inside libmoe.so, which every GPU that loads the library
+ * is a fixed 34,048-byte array inside libmoe.so, which every GPU that loads the library
  * keeps until the process exits.
  *   - T*k must be at most 4,194,304; larger sizes return MOE_ERR_UNSUPPORTED.
- *   - The first call on a device looks up the array's device address, with that device
+ *   - The first call in a CUDA context (per device, and again after cudaDeviceReset or a
+ *     switch to another context) looks up the array's device address with that context
  *     current; make that first call before any stream capture.
  *   - All calls share the one array and it keeps the last call's contents (each call
  *     clears the part that must start at zero).  Calls that may overlap on the GPU (for
  *     instance on two streams with no ordering between them) race: results are undefined.
- *   - Expert indices outside [0, n) are skipped and leave the outputs undefined; nothing
+ *   - Expert indices outside [0, n) go to the trailing bucket as in moe_permute; nothing
  *     reports them here (moe_permute reports them through its workspace).
  */
 moe_status moe_permute_noalloc(const int32_t* topk_idx, int T, int k, int n,
@@ -312,10 +317,11 @@ void moe_set_wait_limit_ns(unsigned long long ns);
 /*
  * Which form of the tensor-core expert GEMMs the bf16 calls use (process-wide; takes effect
  * at the next launch):
- *   MOE_TC_FORM_AUTO    (default) the down-projection (w2) in the CTA-pair form (tcgen05
- *                       cta_group::2, 256-row tiles over two SMs) when the experts average
- *                       at least 256 rows, i.e. T*k >= 256*n; everything else in the
- *                       single-CTA form (128-row tiles)
+ *   MOE_TC_FORM_AUTO    (default) the CTA-pair form (tcgen05 cta_group::2, 256-row tiles
+ *                       over two SMs) for the down-projection (w2) when the experts average
+ *                       at least 256 rows (T*k >= 256*n) and for the up-projection (w1|w3
+ *                       with SwiGLU) when they average at least 512 (T*k >= 512*n); the
+ *                       single-CTA form (128-row tiles) otherwise
  *   MOE_TC_FORM_SINGLE  always the single-CTA form
  *   MOE_TC_FORM_PAIR    always the CTA-pair form (where the device can co-schedule pairs)
  * Both forms compute the same results up to the fp32 accumulation order inside a tile

@@ -14,5 +14,5 @@ from .moe import (  # noqa: F401
     silu, expert_swiglu, group_by_expert, moe_layer, moe_layer_dense, rmsnorm,
     stacked_layer, near_tie_tokens, param_counts, consecutive_same_expert_rate,
     routing_statistics, sigmoid, silu_grad, softmax_backward, expert_swiglu_backward,
-    moe_layer_backward, attention_gqa,
+    moe_layer_backward, attention_gqa, attention_gqa_rows,
 )

@@ -429,3 +429,28 @@ def attention_gqa(q, k, v, seq_len: int = 0) -> np.ndarray:
             scores = np.where(causal, scores, -np.inf)
             out[s0:s1, h] = masked_softmax(scores) @ v[s0:s1, g]
     return out
+
+
+def attention_gqa_rows(q, k, v, rows, seq_len: int = 0) -> np.ndarray:
+    """The same definition as ``attention_gqa``, evaluated only at the query positions
+    ``rows`` (so that single rows deep inside a long sequence cost O(prefix) each):
+
+        o_i = sum_{j <= i, j in the sequence of i} softmax_j(q_i · k_j / sqrt(dh)) v_j
+
+    for every query head.  q [T, Hq, dh], k and v [T, Hkv, dh]; returns [len(rows), Hq, dh]."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    T, hq, dh = q.shape
+    hkv = k.shape[1]
+    if hq % hkv:
+        raise ValueError("query heads must be a multiple of key-value heads")
+    group = hq // hkv
+    S = T if seq_len <= 0 else seq_len
+    rows = np.asarray(rows, dtype=np.int64).reshape(-1)
+    out = np.zeros((rows.size, hq, dh))
+    for r, i in enumerate(rows):
+        s0 = (i // S) * S                       # first token of the sequence holding i
+        for h in range(hq):
+            g = h // group
+            scores = k[s0:i + 1, g] @ q[i, h] / np.sqrt(dh)
+            out[r, h] = masked_softmax(scores) @ v[s0:i + 1, g]
+    return out

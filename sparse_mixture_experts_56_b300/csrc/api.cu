@@ -28,7 +28,7 @@ Layout layout(long long T, long long d, long long f, int n, int k, int dtype) {
   Layout L;
   size_t off = kAlign;  // status header
   L.scratch = off;
-  off += align_up((size_t)2 * permute_blocks(A) * n * sizeof(int32_t));
+  off += align_up(permute_scratch_words(A, n) * sizeof(int32_t));
   L.permute_end = off;
   L.idx = off;
   off += align_up((size_t)A * sizeof(int32_t));

@@ -3,7 +3,8 @@
 //   the experts' outputs return to the original token positions (ja.news.hada.io,
 //   実装と推論効率).
 // One block per token row; 16-byte vectors; fp32 accumulation in ascending slot order, one
-// rounding at the end (deterministic, no atomics).
+// rounding at the end (deterministic, no atomics).  A slot whose inv_perm entry lies outside
+// [0, T*k) adds nothing (no row is read for it).
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -19,15 +20,19 @@ __global__ void __launch_bounds__(256) combine_bf16_vec_kernel(const uint4* __re
   for (int t = blockIdx.x; t < Tn; t += gridDim.x) {
     int rows[kMaxExperts];
     float ws[kMaxExperts];
+    const int A = Tn * k;
     for (int s = 0; s < k; ++s) {
-      rows[s] = __ldg(inv_perm + (size_t)t * k + s);
-      ws[s] = __ldg(w + (size_t)t * k + s);
+      const int p = __ldg(inv_perm + (size_t)t * k + s);
+      const bool ok = p >= 0 && p < A;
+      rows[s] = ok ? p : -1;
+      ws[s] = ok ? __ldg(w + (size_t)t * k + s) : 0.f;
     }
     for (int c = threadIdx.x; c < row_vecs; c += blockDim.x) {
       float acc[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) acc[j] = 0.f;
       for (int s = 0; s < k; ++s) {
+        if (rows[s] < 0) continue;
         const uint4 v = __ldg(y_perm + (size_t)rows[s] * row_vecs + c);
         const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&v);
 #pragma unroll
@@ -67,6 +72,7 @@ __global__ void __launch_bounds__(256) combine_generic_kernel(const T* __restric
       float acc = 0.f;
       for (int s = 0; s < k; ++s) {
         const int p = __ldg(inv_perm + (size_t)t * k + s);
+        if (p < 0 || p >= Tn * k) continue;
         acc = fmaf(__ldg(w + (size_t)t * k + s), to_f32(y_perm[(size_t)p * d + c]), acc);
       }
       if (residual) acc += to_f32(residual[(size_t)t * d + c]);

@@ -98,6 +98,7 @@ constexpr uint32_t instr_desc() {
 
 struct TcArgs {
   const int32_t* offsets;  // rows of each expert: [offsets[e], offsets[e+1])
+  int mrows;               // rows of the row-indexed operands; offsets are clamped to [0, mrows]
   int n;
   int kdim;   // reduction length (not used by kWgrad, whose K is the expert's row count)
   int ndim;   // output columns
@@ -393,16 +394,21 @@ __global__ void __launch_bounds__(256, 1)
   const int units = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
 
   if (threadIdx.x == 0) {
+    // offsets made monotone inside [0, mrows], so that no tile reaches past the buffers
+    // whatever the device-side offsets hold
+    auto clamp_off = [&](int v, int lo) { return v < lo ? lo : (v > args.mrows ? args.mrows : v); };
     int acc = 0;
+    int o0 = clamp_off(args.offsets[0], 0);
     for (int e = 0; e < n; ++e) {
-      const int o0 = args.offsets[e], o1 = args.offsets[e + 1];
+      const int o1 = clamp_off(args.offsets[e + 1], o0);
       const int mt = MODE == kWgrad ? args.mtiles_w : (o1 - o0 + C::kTileM - 1) / C::kTileM;
       sh.off[e] = o0;
       sh.mtiles[e] = mt;
       sh.tile_base[e] = acc;
       acc += mt * args.ntiles;
+      o0 = o1;
     }
-    sh.off[n] = args.offsets[n];
+    sh.off[n] = o0;
     sh.tile_base[n] = acc;
     sh.total = acc;
     sh.abort = 0;
@@ -925,6 +931,7 @@ cudaError_t launch_up_tc(const bf16* x_perm, const int32_t* offsets, const bf16*
     return cudaErrorInvalidValue;
   TcArgs a = {};
   a.offsets = offsets;
+  a.mrows = A;
   a.n = n;
   a.kdim = d;
   a.ndim = f;
@@ -950,6 +957,7 @@ cudaError_t launch_down_tc(const bf16* h, const int32_t* offsets, const bf16* w2
     return cudaErrorInvalidValue;
   TcArgs a = {};
   a.offsets = offsets;
+  a.mrows = A;
   a.n = n;
   a.kdim = f;
   a.ndim = d;
@@ -977,6 +985,7 @@ cudaError_t launch_bwd_store_ab(const bf16* x_pad, const int32_t* poff, const bf
     return cudaErrorInvalidValue;
   TcArgs a = {};
   a.offsets = poff;
+  a.mrows = rows_max;
   a.n = n;
   a.kdim = d;
   a.ndim = f;
@@ -999,6 +1008,7 @@ cudaError_t launch_bwd_dh(const bf16* g_pad, const int32_t* poff, const bf16* w2
     return cudaErrorInvalidValue;
   TcArgs a = {};
   a.offsets = poff;
+  a.mrows = rows_max;
   a.n = n;
   a.kdim = d;
   a.ndim = f;
@@ -1027,6 +1037,7 @@ cudaError_t launch_bwd_dgrad_x(const bf16* da, const bf16* db, const int32_t* po
     return cudaErrorInvalidValue;
   TcArgs a = {};
   a.offsets = poff;
+  a.mrows = rows_max;
   a.n = n;
   a.kdim = 2 * f;
   a.kb_split = f / BK;
@@ -1050,6 +1061,7 @@ cudaError_t launch_bwd_wgrad(const bf16* P, const bf16* Q, const int32_t* poff, 
     return cudaErrorInvalidValue;
   TcArgs a = {};
   a.offsets = poff;
+  a.mrows = rows_max;
   a.n = n;
   a.kdim = 0;
   a.mdim = M;

@@ -42,8 +42,10 @@ cudaError_t launch_router_topk(const void* x, const void* wg, const float* bias,
                                cudaStream_t s);
 cudaError_t launch_rmsnorm(const void* h, int T, int d, float eps, int dtype, void* x, cudaStream_t s);
 
-// Permutation: per-block counts live in `scratch` (2 * nblocks * n int32) when T*k > chunk.
+// Permutation: per-block counts of the n experts and the trailing bucket of bad indices live
+// in `scratch` (permute_scratch_words int32: 2 * nblocks * (n + 1)) when T*k > chunk.
 int permute_blocks(long long A);
+size_t permute_scratch_words(long long A, int n);
 cudaError_t launch_permute(const int32_t* idx, int A, int n, int32_t* offsets, int32_t* perm,
                            int32_t* inv_perm, int32_t* scratch, uint32_t* status, cudaStream_t s);
 

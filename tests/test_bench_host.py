@@ -1,5 +1,5 @@
-"""Host logic of bench.py that decides what a bench line reports (no GPU): the bf16 peak a
-tensor-bound line is compared with, and the ncu traffic figure, which is only used while the
+"""Host logic of bench.py that decides what a bench line reports (no GPU): the default
+workload, the bf16 peak a tensor-bound line is compared with, and the ncu traffic figure, which is only used while the
 kernel source it was taken on is unchanged."""
 import hashlib
 import os
@@ -9,17 +9,29 @@ import pytest
 import bench
 
 
-def test_tensor_peak_follows_the_clock_regime():
+def test_tensor_peak_is_the_burst_figure():
+    """A layer step of a few milliseconds is compared with cuBLAS's burst figure whatever the
+    clocks did; the sustained figure is returned beside it for the side fraction."""
     pk = {"bf16_tflops": 1801.9, "bf16_tflops_sustained": 1412.0}
-    peak, kind, burst, sus = bench.tensor_peak(pk, {"reasons": ["sw_power_cap"]})
-    assert (peak, burst, sus) == (1412.0, 1801.9, 1412.0) and kind.startswith("sustained")
-    for clocks in ({"reasons": []}, {"reasons": None}, {}):
-        peak, kind, _, _ = bench.tensor_peak(pk, clocks)
-        assert peak == 1801.9 and kind.startswith("burst")
+    for clocks in ({"reasons": ["sw_power_cap"]}, {"reasons": []}, {"reasons": None}, {}):
+        peak, kind, burst, sus = bench.tensor_peak(pk, clocks)
+        assert (peak, burst, sus) == (1801.9, 1801.9, 1412.0) and kind.startswith("burst")
+    _, kind, _, _ = bench.tensor_peak(pk, {"reasons": ["sw_power_cap"]})
+    assert "power cap" in kind
     # without measured peaks the fallback figures are used
     peak, _, burst, sus = bench.tensor_peak({}, {"reasons": ["sw_power_cap"]})
     assert (burst, sus) == (bench.FALLBACK_PEAKS["bf16_tflops"],
-                            bench.FALLBACK_PEAKS["bf16_tflops_sustained"]) and peak == sus
+                            bench.FALLBACK_PEAKS["bf16_tflops_sustained"]) and peak == burst
+
+
+def test_default_line_is_the_largest_single_layer_workload(monkeypatch):
+    """With no flags bench.py measures the 16384-token skewed workload (the tensor-bound
+    target) and carries the decode batch beside it."""
+    monkeypatch.setattr("sys.argv", ["bench.py"])
+    args = bench.parse()
+    w = bench.workloads.workload(args.workload)
+    assert (w.T, w.d, w.f, w.n, w.k, w.skew_bias, w.layers) == (16384, 4096, 14336, 8, 2, True, 1)
+    assert not args.no_decode
 
 
 def _fake_tree(tmp_path, source: bytes, recorded_sha: str, traffic: int):

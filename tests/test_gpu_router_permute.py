@@ -9,7 +9,8 @@ import pytest
 
 import oracle
 import workloads
-from tests.helpers import check_selection, gate_weights_for, to_device
+from tests.helpers import (TOL, assert_close_rel, check_selection, f32_inputs, gate_weights_for,
+                           to_device, to_numpy_f32)
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -135,3 +136,57 @@ def test_permute_reports_bad_index(moe):
     moe.moe_permute(ti, 8, ws)
     assert moe.moe_check_device_error(ws) == 6   # MOE_ERR_DEVICE_INDEX
     assert moe.moe_check_device_error(ws) == 0   # cleared
+
+
+def _with_bad(rng, T, k, n, frac):
+    idx = rng.integers(0, n, (T, k))
+    bad = rng.random((T, k)) < frac
+    idx[bad] = rng.choice([-1, n, n + 5, -100], size=int(bad.sum()))
+    return idx, bad
+
+
+@pytest.mark.parametrize("T,k,n", [(45, 2, 8), (40000, 2, 8), (700, 2, 32), (20000, 2, 32)])
+def test_permute_bad_indices_go_to_a_trailing_bucket(moe, T, k, n):
+    """Assignments with an expert index outside [0, n) land after every expert, in ascending
+    order: expert_offsets[n] counts only the valid ones, perm / inv_perm stay a permutation of
+    [0, T*k).  Expected: the oracle's grouping of the same indices with every bad index
+    relabelled n, over n + 1 buckets.  Single- and multi-block launches; n = 32 puts the
+    trailing bucket in the 33rd counter."""
+    rng = np.random.default_rng(T + n)
+    idx, bad = _with_bad(rng, T, k, n, 0.05)
+    ws = moe.workspace(T, 64, 64, n, k, torch.bfloat16, DEV)
+    off, perm, inv = moe.moe_permute(torch.from_numpy(idx.astype(np.int32)).to(DEV), n, ws)
+    assert moe.moe_check_device_error(ws) == 6
+    relabel = np.where(bad, n, idx)
+    roff, rperm, rinv = oracle.group_by_expert(relabel, n + 1)
+    assert off.cpu().numpy().tolist() == roff[:n + 1].tolist()
+    assert off.cpu().numpy()[n] == T * k - bad.sum()
+    assert np.array_equal(perm.cpu().numpy(), rperm)
+    assert np.array_equal(inv.cpu().numpy(), rinv)
+
+
+def test_layer_steps_after_bad_indices_stay_in_bounds(moe):
+    """The grouping of a selection with bad indices drives the experts and the combine without
+    any out-of-bounds access; tokens whose slots are all valid still match the oracle (the
+    checks skip the tokens with a bad slot, whose output is unspecified)."""
+    w = workloads.custom(200, 128, 192, 8, 2, "bf16", wid=470)
+    inp = workloads.make_inputs(w)
+    g = {t: to_device(inp[t], w, DEV) for t in ("x", "w1", "w3", "w2")}
+    rng = np.random.default_rng(47)
+    idx, bad = _with_bad(rng, w.T, w.k, w.n, 0.1)
+    gate = rng.random((w.T, w.k)).astype(np.float32)
+    gate /= gate.sum(1, keepdims=True)
+    ws = moe.workspace(w.T, w.d, w.f, w.n, w.k, torch.bfloat16, DEV)
+    off, perm, inv = moe.moe_permute(torch.from_numpy(idx.astype(np.int32)).to(DEV), w.n, ws)
+    yp = moe.moe_grouped_swiglu(g["x"], perm, off, g["w1"], g["w3"], g["w2"], w.k, ws)
+    y = moe.moe_combine(yp, inv, torch.from_numpy(gate).to(DEV))
+    assert moe.moe_check_device_error(ws) == 6
+    ok = ~bad.any(1)
+    f = f32_inputs(inp, w)
+    xs = f["x"]
+    ref = np.zeros((int(ok.sum()), w.d))
+    for r, t in enumerate(np.flatnonzero(ok)):
+        for s in range(w.k):
+            e = idx[t, s]
+            ref[r] += gate[t, s] * oracle.expert_swiglu(xs[t:t + 1], f["w1"][e], f["w3"][e], f["w2"][e])[0]
+    assert_close_rel(to_numpy_f32(y)[ok], ref, TOL["bf16"])

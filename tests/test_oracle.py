@@ -390,12 +390,64 @@ def check_attention(o):
         np.testing.assert_allclose(out[i, 0], v[:i + 1, 0].mean(axis=0), rtol=1e-13, atol=1e-14)
 
 
+def check_near_tie_tokens(o):
+    """Hand-built logits around the 1e-4 band, with binary-exact gaps (2^-14 = 6.1e-5 is
+    inside the band, 2^-13 = 1.22e-4 outside), rows deliberately unsorted."""
+    a, b = 2.0 ** -14, 2.0 ** -13
+    # n = 4, k = 2: the set gap is between the 2nd and 3rd largest, the order gap between
+    # the 1st and 2nd
+    l2 = np.array([
+        [0.5 - a, 0.0, 3.0, 0.5],        # set gap a            -> set tie
+        [0.5 - b, 0.0, 3.0, 0.5],        # set gap b            -> none
+        [-1.0, 0.5, -2.0, 0.5 + a],      # kept pair gap a      -> order tie
+        [-1.0, 0.5, -2.0, 0.5 + b],      # kept pair gap b      -> none
+        [0.0, 3.0, 2.0, 0.0 + a],        # 3rd/4th gap a only   -> none
+        [1.0, 1.0, 1.0, 1.0],            # all equal            -> both
+        [0.5 + a, 0.5, 0.5 - a, -9.0],   # both gaps a          -> both
+    ])
+    st, ot = o.near_tie_tokens(l2, 2)
+    assert st.tolist() == [True, False, False, False, False, True, True]
+    assert ot.tolist() == [False, False, True, False, False, True, True]
+    # k = 3: order gaps (1st, 2nd) and (2nd, 3rd); the set gap (3rd, 4th)
+    l3 = np.array([
+        [5.0, 3.0, 3.0 - a, 0.0],        # 2nd/3rd gap a        -> order tie
+        [5.0, 3.0, 1.0, 1.0 - a],        # 3rd/4th gap a        -> set tie only
+        [5.0, 5.0 - b, 2.0, 0.0],        # gaps >= b            -> none
+    ])
+    st, ot = o.near_tie_tokens(l3, 3)
+    assert st.tolist() == [False, True, False]
+    assert ot.tolist() == [True, False, False]
+    # k = n: the selected set cannot be in doubt; k = 1: no slot order to decide
+    st, ot = o.near_tie_tokens(l2, 4)
+    assert not st.any()
+    st, ot = o.near_tie_tokens(l2, 1)
+    assert not ot.any() and st.tolist() == [False, False, True, False, False, True, True]
+    # a custom band
+    st, _ = o.near_tie_tokens(np.array([[1.0, 0.75, 0.5]]), 1, eps=0.3)
+    assert st.tolist() == [True]
+
+
+def check_attention_rows(o):
+    """The row-wise evaluation equals the whole-sequence one (itself pinned to torch SDPA
+    above) at every row, across sequence boundaries and with grouped heads."""
+    rng = np.random.default_rng(81)
+    for T, hq, hkv, dh, seq in [(37, 8, 2, 16, 0), (45, 6, 3, 8, 16), (9, 4, 1, 32, 4)]:
+        q = rng.standard_normal((T, hq, dh))
+        k = rng.standard_normal((T, hkv, dh))
+        v = rng.standard_normal((T, hkv, dh))
+        full = o.attention_gqa(q, k, v, seq)
+        rows = np.arange(T)[::-1]
+        np.testing.assert_allclose(o.attention_gqa_rows(q, k, v, rows, seq), full[rows],
+                                   rtol=1e-12, atol=1e-13)
+
+
 CHECKS = [check_worked_example, check_gate_invariants, check_topk_bruteforce,
           check_softmax_order_equivalence, check_single_expert_is_plain_ffn,
           check_k_equals_n_is_dense_softmax_mixture, check_sparse_equals_dense, check_grouping,
           check_silu, check_bias_enters_before_topk, check_rmsnorm, check_param_counts,
           check_locality_metric, check_routing_statistics, check_backward_finite_differences,
-          check_backward_autograd, check_backward_special_cases, check_attention]
+          check_backward_autograd, check_backward_special_cases, check_attention,
+          check_near_tie_tokens, check_attention_rows]
 
 
 @pytest.mark.parametrize("check", CHECKS, ids=lambda c: c.__name__[6:])
@@ -529,6 +581,48 @@ def _mut_attn_anticausal(q, k, v, seq_len=0):
     return _ORIG_ATTN(q, k, v, seq_len)[::-1]
 
 
+_ORIG_NEAR_TIE = moe_oracle.near_tie_tokens
+
+
+def _mut_near_tie_wrong_gap(logits, k, eps=1e-4):
+    """the set gap taken between the (K+1)-th and (K+2)-th largest logits"""
+    l = np.sort(np.asarray(logits, dtype=np.float64), axis=1)[:, ::-1]
+    _, order_tie = _ORIG_NEAR_TIE(logits, k, eps)
+    set_tie = np.zeros(l.shape[0], dtype=bool)
+    if k + 1 < l.shape[1]:
+        set_tie = (l[:, k] - l[:, k + 1]) < eps
+    return set_tie, order_tie
+
+
+def _mut_near_tie_order_off_by_one(logits, k, eps=1e-4):
+    """the slot-order loop runs one gap too far (into the set gap)"""
+    l = np.sort(np.asarray(logits, dtype=np.float64), axis=1)[:, ::-1]
+    set_tie, _ = _ORIG_NEAR_TIE(logits, k, eps)
+    order_tie = np.zeros(l.shape[0], dtype=bool)
+    for j in range(min(k, l.shape[1] - 1)):
+        order_tie |= (l[:, j] - l[:, j + 1]) < eps
+    return set_tie, order_tie
+
+
+_ORIG_ATTN_ROWS = moe_oracle.attention_gqa_rows
+
+
+def _mut_attn_rows_excludes_self(q, k, v, rows, seq_len=0):
+    """each row attends to the keys strictly before it (the diagonal dropped)"""
+    q, k, v = (np.asarray(a, dtype=np.float64) for a in (q, k, v))
+    T, hq, dh = q.shape
+    group = hq // k.shape[1]
+    S = T if seq_len <= 0 else seq_len
+    out = np.zeros((len(rows), hq, dh))
+    for r, i in enumerate(rows):
+        s0 = (i // S) * S
+        hi = max(i, s0 + 1)
+        for h in range(hq):
+            sc = k[s0:hi, h // group] @ q[i, h] / np.sqrt(dh)
+            out[r, h] = moe_oracle.masked_softmax(sc) @ v[s0:hi, h // group]
+    return out
+
+
 MUTATIONS = {
     "silu->sigmoid": ("silu", _mut_sigmoid_for_silu),
     "swap w1/w3": ("expert_swiglu", _mut_swap_w1_w3),
@@ -550,6 +644,9 @@ MUTATIONS = {
     "attention without 1/sqrt(dh)": ("attention_gqa", _mut_attn_no_scale),
     "attention across sequences": ("attention_gqa", _mut_attn_one_sequence),
     "attention anti-causal": ("attention_gqa", _mut_attn_anticausal),
+    "near-tie set gap one too deep": ("near_tie_tokens", _mut_near_tie_wrong_gap),
+    "near-tie order loop off by one": ("near_tie_tokens", _mut_near_tie_order_off_by_one),
+    "attention rows without the diagonal": ("attention_gqa_rows", _mut_attn_rows_excludes_self),
 }
 
 

@@ -486,56 +486,93 @@ def forward_line(args, w, dist, dev, with_cpu):
                                                  stream)
 
     if not args.no_e2e:
-        # end to end through the public call with host buffers: pinned H2D of x, the layer,
-        # D2H of y, every step
-        x_pin = torch.from_numpy(np.ascontiguousarray(x_h).view(np.int16) if w.dtype == "bf16" else x_h)
-        x_pin = (x_pin.view(torch.bfloat16) if w.dtype == "bf16" else x_pin).pin_memory()
-        y_pin = torch.empty_like(x_pin).pin_memory()
-        x_dev = torch.empty_like(x)
-        y_dev = torch.empty_like(x)
-        ws_full = ws
-        xn2 = torch.empty_like(x)
-        hbuf2 = [torch.empty_like(x) for _ in range(2)]
-
-        def e2e_step():
-            x_dev.copy_(x_pin, non_blocking=True)
-            if w.layers == 1:
-                moe.moe_layer_forward(x_dev, layers[0]["wg"], layers[0]["w1"], layers[0]["w3"],
-                                      layers[0]["w2"], k, ws_full, logit_bias=bias, y=y_dev)
-                y_pin.copy_(y_dev, non_blocking=True)
-            else:
-                h_in = x_dev
-                for li, L in enumerate(layers):
-                    moe.moe_rmsnorm(h_in, w.rms_eps, x=xn2)
-                    out = hbuf2[li % 2]
-                    moe.moe_layer_forward(xn2, L["wg"], L["w1"], L["w3"], L["w2"], k, ws_full,
-                                          residual=h_in, y=out)
-                    h_in = out
-                y_pin.copy_(h_in, non_blocking=True)
-
-        for _ in range(3):
-            e2e_step()
-        torch.cuda.synchronize()
-        dist.barrier()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(args.steps):
-            e2e_step()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        dist.barrier()
-        e_ms = dist.max(e0.elapsed_time(e1))
-        line["e2e"] = {"value": T * dist.world * args.steps / (e_ms / 1e3), "unit": "tokens/s",
-                       "h2d_bytes_per_step": T * d * esz, "d2h_bytes_per_step": T * d * esz,
-                       "ms_per_step": e_ms / args.steps, "api": "moe_layer_forward"}
-        if moe.moe_check_device_error(ws) != 0:
-            raise SystemExit("device status set in the end-to-end loop")
+        line["e2e"] = e2e_forward(args, w, dist, moe, x_h, layers, bias, ws, stream)
 
     if with_cpu and dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
         xf, lf, _ = oracle_prepare(w, x_h, layers_h, bias_h)
         del layers_h
         line["cpu_baseline"] = run_cpu_baseline(w, xf, lf, bias_h)
     return line
+
+
+def e2e_forward(args, w, dist, moe, x_h, layers, bias, ws, stream):
+    """End to end through the public call, moe_layer_forward, with host buffers: every step
+    copies its x from pinned host memory to the device, runs the layer (or the stack) and
+    copies y back to pinned host memory.  The copies run on their own streams, one step
+    ahead (H2D) and one behind (D2H) the layer, as a serving loop would overlap them; every
+    copy of every step is inside the timed region, which ends when the last y is on the
+    host."""
+    import torch
+    k = w.k
+    esz = 2 if w.dtype == "bf16" else 4
+    x_pin = torch.from_numpy(np.ascontiguousarray(x_h).view(np.int16) if w.dtype == "bf16" else x_h)
+    x_pin = (x_pin.view(torch.bfloat16) if w.dtype == "bf16" else x_pin).pin_memory()
+    y_pin = [torch.empty_like(x_pin).pin_memory() for _ in range(2)]
+    x_dev = [torch.empty(x_pin.shape, dtype=x_pin.dtype, device=ws.device) for _ in range(2)]
+    y_dev = [torch.empty_like(x_dev[0]) for _ in range(2)]
+    xn = torch.empty_like(x_dev[0])
+    hb = [torch.empty_like(x_dev[0]) for _ in range(2)]
+    h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event()
+    loaded = [ev(), ev()]     # x_dev[b] holds the step's input
+    used = [ev(), ev()]       # the layer has finished reading x_dev[b] and writing y_dev[b]
+    drained = [ev(), ev()]    # y_dev[b] is on the host
+
+    def layer_step(b):
+        if w.layers == 1:
+            moe.moe_layer_forward(x_dev[b], layers[0]["wg"], layers[0]["w1"], layers[0]["w3"],
+                                  layers[0]["w2"], k, ws, logit_bias=bias, y=y_dev[b])
+            return
+        h_in = x_dev[b]
+        for li, L in enumerate(layers):
+            moe.moe_rmsnorm(h_in, w.rms_eps, x=xn)
+            out = y_dev[b] if li == len(layers) - 1 else hb[li % 2]
+            moe.moe_layer_forward(xn, L["wg"], L["w1"], L["w3"], L["w2"], k, ws, residual=h_in, y=out)
+            h_in = out
+
+    def load(i):
+        b = i % 2
+        with torch.cuda.stream(h2d):
+            if i >= 2:
+                h2d.wait_event(used[b])          # step i-2 has finished with x_dev[b]
+            x_dev[b].copy_(x_pin, non_blocking=True)
+            loaded[b].record(h2d)
+
+    def run(steps):
+        load(0)
+        for i in range(steps):
+            b = i % 2
+            if i + 1 < steps:
+                load(i + 1)
+            stream.wait_event(loaded[b])
+            if i >= 2:
+                stream.wait_event(drained[b])    # y_dev[b] of step i-2 is on the host
+            layer_step(b)
+            used[b].record(stream)
+            with torch.cuda.stream(d2h):
+                d2h.wait_event(used[b])
+                y_pin[b].copy_(y_dev[b], non_blocking=True)
+                drained[b].record(d2h)
+        for b in range(min(2, steps)):
+            stream.wait_event(drained[b])
+
+    run(3)
+    torch.cuda.synchronize()
+    dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    h2d.wait_event(e0)
+    run(args.steps)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    if moe.moe_check_device_error(ws) != 0:
+        raise SystemExit("device status set in the end-to-end loop")
+    e_ms = dist.max(e0.elapsed_time(e1))
+    return {"value": w.T * dist.world * args.steps / (e_ms / 1e3), "unit": "tokens/s",
+            "h2d_bytes_per_step": w.T * w.d * esz, "d2h_bytes_per_step": w.T * w.d * esz,
+            "ms_per_step": e_ms / args.steps, "api": "moe_layer_forward",
+            "copies": "pinned H2D one step ahead and D2H one step behind, on their own streams"}
 
 
 def routing_stats_report(moe, w, step, layer, layers, x, xn, hs, idx, off, stream):

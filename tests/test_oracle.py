@@ -15,6 +15,7 @@ import pytest
 import torch
 import torch.nn.functional as F
 
+import oracle.ep as ep_oracle
 import oracle.moe as moe_oracle
 import workloads
 
@@ -441,13 +442,63 @@ def check_attention_rows(o):
                                    rtol=1e-12, atol=1e-13)
 
 
+def check_ep_plan(o):
+    """Expert-parallel bookkeeping against the single-rank grouping: with G ranks of T tokens
+    each, the rows a rank's expert receives, in the order the plan evaluates them, are the
+    rows the single-rank grouping of all G*T tokens (rank s's tokens at s*T..) gives that
+    expert; every assignment is sent exactly once; counts add up; G = 1 is the identity."""
+    rng = np.random.default_rng(90)
+    for G, T, n, k in [(1, 37, 8, 2), (2, 50, 8, 2), (4, 33, 8, 2), (8, 20, 8, 2), (2, 40, 4, 3),
+                       (4, 0, 8, 2)]:
+        idx = [rng.integers(0, n, (T, k)) for _ in range(G)]
+        if T:
+            idx[0][:, 0] = 0                                     # a crowded expert
+        plans = ep_oracle.ep_exchange_plan(idx, n, G)
+        E = n // G
+        off_all, perm_all, _ = o.group_by_expert(np.concatenate(idx) if T else np.zeros((0, k), int), n)
+        seen = set()
+        for g, p in enumerate(plans):
+            # brute-force counts
+            for s in range(G):
+                for j in range(E):
+                    assert p["recv_counts"][s, j] == int(np.count_nonzero(idx[s] == g * E + j))
+            assert p["send_counts"].tolist() == [
+                int(np.count_nonzero((idx[g] >= h * E) & (idx[g] < (h + 1) * E))) for h in range(G)]
+            R = int(p["recv_counts"].sum())
+            assert p["local_offsets"][-1] == R and len(p["row_map"]) == R
+            assert sorted(p["row_map"].tolist()) == list(range(R))
+            for j in range(E):
+                e = g * E + j
+                rows = p["row_map"][p["local_offsets"][j]:p["local_offsets"][j + 1]]
+                got = list(zip(p["recv_src"][rows].tolist(), p["recv_assign"][rows].tolist()))
+                want = [divmod(int(a), T * k) for a in perm_all[off_all[e]:off_all[e + 1]]]
+                assert got == want
+                for sa in got:
+                    assert idx[sa[0]].reshape(-1)[sa[1]] == e
+                    seen.add(sa)
+        assert len(seen) == G * T * k                            # each assignment sent once
+        if G == 1:
+            off, _, _ = o.group_by_expert(idx[0], n)
+            assert plans[0]["row_map"].tolist() == list(range(T * k))
+            assert plans[0]["local_offsets"].tolist() == off.tolist()
+        assert ep_oracle.ep_load(plans).sum() == G * T * k
+    # unequal batches per rank: the receive buffer is the sources' blocks in source order
+    idx = [np.array([[1, 3], [0, 1]]), np.array([[3, 2]]), np.zeros((0, 2), int)]
+    with pytest.raises(ValueError):
+        ep_oracle.ep_exchange_plan(idx, 4, 3)                            # 4 experts over 3 ranks
+    p = ep_oracle.ep_exchange_plan(idx + [np.array([[2, 0]])], 4, 4)
+    assert p[1]["recv_src"].tolist() == [0, 0] and p[1]["recv_assign"].tolist() == [0, 3]
+    assert p[3]["recv_src"].tolist() == [0, 1] and p[3]["recv_assign"].tolist() == [1, 0]
+    assert p[0]["recv_counts"][:, 0].tolist() == [1, 0, 0, 1]
+
+
 CHECKS = [check_worked_example, check_gate_invariants, check_topk_bruteforce,
           check_softmax_order_equivalence, check_single_expert_is_plain_ffn,
           check_k_equals_n_is_dense_softmax_mixture, check_sparse_equals_dense, check_grouping,
           check_silu, check_bias_enters_before_topk, check_rmsnorm, check_param_counts,
           check_locality_metric, check_routing_statistics, check_backward_finite_differences,
           check_backward_autograd, check_backward_special_cases, check_attention,
-          check_near_tie_tokens, check_attention_rows]
+          check_near_tie_tokens, check_attention_rows, check_ep_plan]
 
 
 @pytest.mark.parametrize("check", CHECKS, ids=lambda c: c.__name__[6:])
@@ -623,6 +674,29 @@ def _mut_attn_rows_excludes_self(q, k, v, rows, seq_len=0):
     return out
 
 
+_ORIG_EP_PLAN = ep_oracle.ep_exchange_plan
+_ORIG_EP_OF = ep_oracle.ep_experts_of
+
+
+def _mut_ep_strided_experts(rank, n, G):
+    """rank r holds experts r, r+G, r+2G, ... instead of a contiguous block"""
+    if G < 1 or n % G:
+        raise ValueError("n must be a multiple of the number of ranks")
+    return range(rank, n, G)
+
+
+def _mut_ep_order_by_assignment(idx_per_rank, n, G):
+    """a receiver orders an expert's rows by assignment index before source rank"""
+    plans = _ORIG_EP_PLAN(idx_per_rank, n, G)
+    for p in plans:
+        lo = p["local_offsets"]
+        for j in range(len(lo) - 1):
+            seg = p["row_map"][lo[j]:lo[j + 1]]
+            key = np.lexsort((p["recv_src"][seg], p["recv_assign"][seg]))
+            p["row_map"][lo[j]:lo[j + 1]] = seg[key]
+    return plans
+
+
 MUTATIONS = {
     "silu->sigmoid": ("silu", _mut_sigmoid_for_silu),
     "swap w1/w3": ("expert_swiglu", _mut_swap_w1_w3),
@@ -647,13 +721,16 @@ MUTATIONS = {
     "near-tie set gap one too deep": ("near_tie_tokens", _mut_near_tie_wrong_gap),
     "near-tie order loop off by one": ("near_tie_tokens", _mut_near_tie_order_off_by_one),
     "attention rows without the diagonal": ("attention_gqa_rows", _mut_attn_rows_excludes_self),
+    "EP experts strided over ranks": (ep_oracle, "ep_experts_of", _mut_ep_strided_experts),
+    "EP rows ordered by assignment first": (ep_oracle, "ep_exchange_plan", _mut_ep_order_by_assignment),
 }
 
 
 @pytest.mark.parametrize("name", sorted(MUTATIONS))
 def test_pins_catch_mutations(name, monkeypatch):
-    attr, fn = MUTATIONS[name]
-    monkeypatch.setattr(moe_oracle, attr, fn)
+    spec = MUTATIONS[name]
+    module, attr, fn = spec if len(spec) == 3 else (moe_oracle,) + spec
+    monkeypatch.setattr(module, attr, fn)
     failed = []
     for check in CHECKS:
         try:

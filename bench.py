@@ -59,6 +59,10 @@ def parse():
                    help="time the layer's forward (default), its backward (moe_layer_backward), "
                         "a training step (moe_layer_forward_train + moe_layer_backward_saved), or "
                         "the causal grouped-query attention of the layer's other sub-block")
+    p.add_argument("--ep", action="store_true",
+                   help="expert parallelism: the N ranks hold n/N experts each and exchange token "
+                        "rows by NCCL all-to-all (sparse_mixture_experts_56_b300.ep); every rank "
+                        "routes T tokens of its own")
     p.add_argument("--seq-len", type=int, default=0,
                    help="--pass attention: tokens per sequence (0: the workload's T)")
     return p.parse_args()
@@ -830,6 +834,96 @@ def attention_arm(args, w, dist):
         print(json.dumps(line), flush=True)
 
 
+def ep_arm(args, w, dist):
+    """Times the expert-parallel layer pass: rank r of N holds experts [r*n/N, (r+1)*n/N) and
+    T tokens of its own (seeded per rank); one step = route, group, the count and row
+    all-to-alls, the local experts, the return all-to-all and the combine, on every rank."""
+    import torch
+    import sparse_mixture_experts_56_b300 as moe
+    from sparse_mixture_experts_56_b300 import ep
+
+    if w.dtype != "bf16" or w.layers != 1:
+        raise SystemExit("bench.py --ep: single-layer bf16 workloads only")
+    dev = torch.device("cuda", dist.local)
+    torch.cuda.set_device(dev)
+    moe._native.lib()
+    G, r = dist.world, dist.rank
+    blk = ep.expert_block(r, w.n, G)
+    weights = workloads.make_inputs(w, seed=args.seed, tensors=("wg", "w1", "w3", "w2"))
+    x = to_dev(workloads.make_inputs(w, seed=args.seed + r, tensors=("x",))["x"], w, dev)
+    wg = to_dev(weights["wg"], w, dev)
+    wl = {t: to_dev(np.ascontiguousarray(weights[t][blk.start:blk.stop]), w, dev) for t in ("w1", "w3", "w2")}
+    del weights
+    bias = torch.from_numpy(workloads.logit_bias_vector(w.n)).to(dev) if w.skew_bias else None
+    comm = ep.TorchComm() if dist.world > 1 or dist.pg else None
+    if comm is None:
+        import torch.distributed as td
+        td.init_process_group("nccl", init_method="tcp://127.0.0.1:%d" % _free_port(), rank=0,
+                              world_size=1, device_id=dev)
+        dist.pg = td
+        comm = ep.TorchComm()
+    ops = ep.NativeOps(dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        return ep.ep_layer_forward(comm, ops, x, wg, wl["w1"], wl["w3"], wl["w2"], w.k, w.n, bias)
+
+    for _ in range(max(3, args.warmup)):
+        _, stats = step()
+    sampler = ClockSampler(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    e0.record(stream)
+    for _ in range(args.steps):
+        _, stats = step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    sampler.stop()
+    dist.barrier()
+    ms = dist.max(e0.elapsed_time(e1)) / args.steps
+    rows = torch.tensor([stats["expert_rows"]], dtype=torch.int64, device=dev)
+    if G > 1:
+        allr = [torch.empty_like(rows) for _ in range(G)]
+        dist.pg.all_gather(allr, rows)
+        load = [int(t.item()) for t in allr]
+    else:
+        load = [int(rows.item())]
+    flops = workloads.active_flops(w) * G
+    pk, pk_kind = peaks()
+    clk = sampler.summary()
+    tc_peak, kind, burst, sus = tensor_peak(pk, clk)
+    ach = flops / (ms / 1e3) / 1e12
+    line = {"metric": METRIC, "pass": "forward-ep", "value": w.T * G / (ms / 1e3), "unit": "tokens/s",
+            "n_gpus": G, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded Gaussian, Mixtral-shaped; tokens seeded per rank)",
+            "config": {"workload": w.name, "T_per_rank": w.T, "d_model": w.d, "d_ff": w.f,
+                       "n_experts": w.n, "top_k": w.k, "skewed_bias": w.skew_bias,
+                       "parallelism": f"ep{G} (experts {w.n // G} per rank, NCCL all-to-all)",
+                       "l2": "no flush: per-step weights exceed the 126 MB L2"},
+            "tflops": ach,
+            "roofline": {"bound": "tensor", "achieved": ach, "peak": tc_peak * G, "unit": "TFLOP/s",
+                         "frac": ach / (tc_peak * G), "traffic": None, "peak_kind": kind,
+                         "kernel": "whole EP layer pass on every rank (active FLOPs 6*T*K*d*f per rank)",
+                         "peak_source": f"{pk_kind} (MEASURED_PEAKS.json), times the ranks"},
+            "ep": {"ranks": G, "expert_rows_per_rank": load,
+                   "imbalance_max_over_mean": max(load) / (sum(load) / len(load)) if sum(load) else None},
+            # router, grouping (1 or 3), gather, regroup, up (gather + GEMM), down, gather back,
+            # combine; NCCL's own kernels are not counted
+            "gpu_launches": (9 + (2 if w.T * w.k > 32768 else 0)) * args.steps, "clocks": clk}
+    if dist.rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def _free_port():
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
 def main():
     args = parse()
     w = workloads.workload(args.workload)
@@ -840,7 +934,9 @@ def main():
     import torch
     dist.init("nccl" if torch.cuda.is_available() else "gloo")
     try:
-        if args.which in ("backward", "train"):
+        if args.ep:
+            ep_arm(args, w, dist)
+        elif args.which in ("backward", "train"):
             backward_arm(args, w, dist)
         elif args.which == "attention":
             attention_arm(args, w, dist)

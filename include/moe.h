@@ -301,6 +301,40 @@ moe_status moe_routing_stats(const int32_t* topk_idx, int T, int k, int n, int s
                              int64_t* expert_counts, int64_t* pair_counts, void* stream);
 
 /*
+ * Expert parallelism (EP): the layer spread over G GPUs by experts.  Tokens an expert must
+ * process go to the GPU holding it and its outputs return to the original token positions
+ * (newsflash.city digest, section "专家层的混合"; ja.news.hada.io, section "実装と推論効率").
+ * Rank g of G holds the experts [g*E, (g+1)*E), E = n/G.  A layer pass on rank g is:
+ * moe_router_topk and moe_permute on its own tokens; moe_gather_rows of x into grouping
+ * order; an all-to-all of the per-expert counts and an all-to-all-v of the rows (the
+ * caller's collective library, e.g. NCCL); moe_ep_regroup; moe_gather_rows into the
+ * experts' order; moe_expert_up / moe_expert_down with the local experts' weights (k = 1,
+ * n = E); moe_gather_rows back to receive order; the reverse all-to-all-v; moe_combine.
+ *
+ * moe_ep_regroup: the receive buffer of rank g holds, source after source (s = 0..G-1),
+ * each source's rows for g's experts in the source's order (local expert j = 0..E-1, then
+ * assignment).  Orders them by local expert, then source:
+ *   recv_counts   [G, E] int32 in (device): rows from source s for local expert j
+ *   R             total rows = sum of recv_counts (known to the caller, who sized the
+ *                 buffers with it); positions at or past R are never written
+ *   local_offsets [E+1] int32 out: exclusive prefix sum of the local experts' rows
+ *   row_map       [R] int32 out: row_map[p] = receive-buffer row at grouped position p
+ *   inv_row_map   [R] int32 out: inv_row_map[q] = grouped position of receive row q
+ * Negative counts count as 0.  Bit-exact (integer only), deterministic.
+ */
+moe_status moe_ep_regroup(const int32_t* recv_counts, int G, int E, int R, int32_t* local_offsets,
+                          int32_t* row_map, int32_t* inv_row_map, void* stream);
+
+/*
+ * Row gather by an index vector:  dst[p] = src[index[p] / k]  for p < rows.
+ *   src [rows_src, row_bytes] in; index [rows] int32 in; dst [rows, row_bytes] out.
+ * An index outside [0, rows_src * k) gives a zero row (no read out of bounds).  16-byte
+ * vectors when row_bytes and both pointers allow it.  Used by the EP sequence above.
+ */
+moe_status moe_gather_rows(const void* src, int rows_src, const int32_t* index, int rows, int k,
+                           size_t row_bytes, void* dst, void* stream);
+
+/*
  * Synchronise `stream`, read the device status word that the kernels of the last calls
  * using this workspace may have set, and clear it.  Returns MOE_OK, MOE_ERR_TIMEOUT or
  * MOE_ERR_DEVICE_INDEX (or MOE_ERR_CUDA if the synchronisation itself failed).

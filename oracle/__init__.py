@@ -16,4 +16,4 @@ from .moe import (  # noqa: F401
     routing_statistics, sigmoid, silu_grad, softmax_backward, expert_swiglu_backward,
     moe_layer_backward, attention_gqa, attention_gqa_rows,
 )
-from .ep import ep_experts_of, ep_send_counts, ep_exchange_plan, ep_load  # noqa: F401
+from .ep import ep_experts_of, ep_send_counts, ep_exchange_plan, ep_load, ep_regroup  # noqa: F401

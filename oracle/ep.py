@@ -99,3 +99,27 @@ def ep_exchange_plan(idx_per_rank: Sequence, n: int, G: int) -> List[dict]:
 def ep_load(plans: Sequence[dict]) -> np.ndarray:
     """Rows each rank's experts process in the pass (the load [JA] asks to balance)."""
     return np.array([int(p["recv_counts"].sum()) for p in plans], dtype=np.int64)
+
+
+def ep_regroup(recv_counts) -> tuple:
+    """The receiving side from its counts alone: ``recv_counts`` [G, E] rows from source s
+    for local expert j.  The receive buffer lists the sources' blocks in source order, each
+    block its experts' rows in expert order; the experts evaluate the rows of local expert j
+    source by source.  Returns (local_offsets [E+1], row_map [R], inv_row_map [R]) with
+    row_map[p] = receive-buffer row at grouped position p."""
+    c = np.maximum(np.asarray(recv_counts, dtype=np.int64), 0)
+    G, E = c.shape
+    recv_pos = {}
+    q = 0
+    for s in range(G):
+        for j in range(E):
+            for i in range(int(c[s, j])):
+                recv_pos[(s, j, i)] = q
+                q += 1
+    row_map = [recv_pos[(s, j, i)] for j in range(E) for s in range(G) for i in range(int(c[s, j]))]
+    row_map = np.asarray(row_map, dtype=np.int64)
+    inv = np.empty_like(row_map)
+    inv[row_map] = np.arange(row_map.size, dtype=np.int64)
+    local_offsets = np.concatenate([[0], np.cumsum(c.sum(axis=0))]).astype(np.int64)
+    return local_offsets, row_map, inv
+

@@ -25,7 +25,7 @@ __all__ = [
     "moe_layer_forward_train", "moe_layer_backward_saved", "moe_attention_gqa",
     "moe_layer_forward", "moe_check_device_error", "moe_set_wait_limit_ns", "moe_set_tc_form",
     "MOE_TC_FORM_AUTO", "MOE_TC_FORM_SINGLE", "MOE_TC_FORM_PAIR", "moe_version",
-    "library_path",
+    "library_path", "moe_ep_regroup", "moe_gather_rows",
 ]
 
 
@@ -349,3 +349,37 @@ def moe_attention_gqa(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, ws: tor
                                          _stream(stream))
     check("moe_attention_gqa", st)
     return out
+
+
+def moe_ep_regroup(recv_counts: torch.Tensor, R: int, *, local_offsets: Optional[torch.Tensor] = None,
+                   row_map: Optional[torch.Tensor] = None, inv_row_map: Optional[torch.Tensor] = None,
+                   stream=None):
+    """recv_counts [G, E] int32 (device) -> (local_offsets [E+1], row_map [R], inv_row_map [R])."""
+    G, E = recv_counts.shape
+    dev = recv_counts.device
+    if local_offsets is None:
+        local_offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    if row_map is None:
+        row_map = torch.empty(R, dtype=torch.int32, device=dev)
+    if inv_row_map is None:
+        inv_row_map = torch.empty(R, dtype=torch.int32, device=dev)
+    st = _native.lib().moe_ep_regroup(_ptr(recv_counts), G, E, R, _ptr(local_offsets),
+                                      _ptr(row_map), _ptr(inv_row_map), _stream(stream))
+    check("moe_ep_regroup", st)
+    return local_offsets, row_map, inv_row_map
+
+
+def moe_gather_rows(src: torch.Tensor, index: torch.Tensor, k: int = 1, *,
+                    dst: Optional[torch.Tensor] = None, stream=None):
+    """dst[p] = src[index[p] // k] (zero rows for indices outside [0, rows(src) * k))."""
+    rows = index.shape[0]
+    if dst is None:
+        dst = torch.empty((rows,) + tuple(src.shape[1:]), dtype=src.dtype, device=src.device)
+    if rows == 0:
+        return dst
+    row_bytes = (dst.numel() // rows) * dst.element_size()
+    st = _native.lib().moe_gather_rows(_ptr(src), src.shape[0], _ptr(index), rows, k, row_bytes,
+                                       _ptr(dst), _stream(stream))
+    check("moe_gather_rows", st)
+    return dst
+

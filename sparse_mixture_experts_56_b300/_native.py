@@ -52,6 +52,8 @@ SIGNATURES = {
                                       _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_layer_backward": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P,
                                 _P, _P, _P, _SZ, _P]),
+    "moe_ep_regroup": (_I, [_P, _I, _I, _I, _P, _P, _P, _P]),
+    "moe_gather_rows": (_I, [_P, _I, _P, _I, _I, _SZ, _P, _P]),
     "moe_check_device_error": (_I, [_P, _SZ, _P]),
     "moe_set_wait_limit_ns": (None, [ctypes.c_ulonglong]),
     "moe_set_tc_form": (_I, [_I]),

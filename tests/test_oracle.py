@@ -482,6 +482,12 @@ def check_ep_plan(o):
             assert plans[0]["row_map"].tolist() == list(range(T * k))
             assert plans[0]["local_offsets"].tolist() == off.tolist()
         assert ep_oracle.ep_load(plans).sum() == G * T * k
+        # the receiver's regrouping from its counts alone is the plan's
+        for p in plans:
+            lo, rm, inv = ep_oracle.ep_regroup(p["recv_counts"])
+            assert lo.tolist() == p["local_offsets"].tolist()
+            assert rm.tolist() == p["row_map"].tolist()
+            assert np.array_equal(rm[inv], np.arange(rm.size))
     # unequal batches per rank: the receive buffer is the sources' blocks in source order
     idx = [np.array([[1, 3], [0, 1]]), np.array([[3, 2]]), np.zeros((0, 2), int)]
     with pytest.raises(ValueError):

@@ -55,10 +55,11 @@ def parse():
                    help="forward pass of a workload other than the decode batch: do not add the "
                         "decode batch's measurement under \"decode\"")
     p.add_argument("--pass", dest="which", default="forward",
-                   choices=["forward", "backward", "train", "attention"],
+                   choices=["forward", "backward", "train", "attention", "decoder"],
                    help="time the layer's forward (default), its backward (moe_layer_backward), "
                         "a training step (moe_layer_forward_train + moe_layer_backward_saved), or "
-                        "the causal grouped-query attention of the layer's other sub-block")
+                        "the causal grouped-query attention of the layer's other sub-block, or one "
+                        "whole decoder layer (attention sub-block + MoE sub-block)")
     p.add_argument("--ep", action="store_true",
                    help="expert parallelism: the N ranks hold n/N experts each and exchange token "
                         "rows by NCCL all-to-all (sparse_mixture_experts_56_b300.ep); every rank "
@@ -834,6 +835,82 @@ def attention_arm(args, w, dist):
         print(json.dumps(line), flush=True)
 
 
+def decoder_arm(args, w, dist):
+    """Times moe_decoder_layer_forward on the workload's tokens with the pages' attention
+    shapes (32 query / 8 key-value heads of 128, d = 4096): RMSNorm, q/k/v projections, causal
+    GQA attention, output projection + residual, RMSNorm, the MoE layer + residual."""
+    import torch
+    import sparse_mixture_experts_56_b300 as moe
+
+    if w.dtype != "bf16" or w.layers != 1:
+        raise SystemExit("bench.py --pass decoder: single-layer bf16 workloads only")
+    dev = torch.device("cuda", dist.local)
+    torch.cuda.set_device(dev)
+    moe._native.lib()
+    T, d, f, n, k, hq, hkv = w.T, w.d, w.f, w.n, w.k, 32, 8
+    seq = args.seq_len if args.seq_len > 0 else min(T, 4096)
+    inp = workloads.make_inputs(w, seed=args.seed, tensors=("x", "wg", "w1", "w3", "w2"))
+    g = {t: to_dev(inp[t], w, dev) for t in ("x", "wg", "w1", "w3", "w2")}
+    gen = torch.Generator(device="cpu").manual_seed(args.seed)
+    proj = {name: (torch.randn(shape, generator=gen) * shape[1] ** -0.5).to(torch.bfloat16).to(dev)
+            for name, shape in (("wq", (hq * 128, d)), ("wk", (hkv * 128, d)), ("wv", (hkv * 128, d)),
+                                ("wo", (d, hq * 128)))}
+    bias = torch.from_numpy(inp["bias"]).to(dev) if inp["bias"] is not None else None
+    ws = moe.decoder_workspace(T, d, f, n, k, hq, hkv, dev)
+    y = torch.empty_like(g["x"])
+    stream = torch.cuda.current_stream()
+
+    def step():
+        moe.moe_decoder_layer_forward(g["x"], proj["wq"], proj["wk"], proj["wv"], proj["wo"], g["wg"],
+                                      g["w1"], g["w3"], g["w2"], k, hq, hkv, ws, seq_len=seq,
+                                      logit_bias=bias, y=y)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    if moe.moe_check_device_error(ws) != 0:
+        raise SystemExit("device status set after warm-up")
+    sampler = ClockSampler(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    sampler.stop()
+    dist.barrier()
+    if moe.moe_check_device_error(ws) != 0:
+        raise SystemExit("device status set in the timed region")
+    ms = dist.max(e0.elapsed_time(e1)) / args.steps
+    pairs = sum(min(seq, T - s0) * (min(seq, T - s0) + 1) // 2 for s0 in range(0, T, seq))
+    flops = (2.0 * T * d * (hq + 2 * hkv) * 128 + 2.0 * T * hq * 128 * d + 4.0 * 128 * hq * pairs
+             + workloads.active_flops(w))
+    pk, pk_kind = peaks()
+    clk = sampler.summary()
+    tc_peak, kind, burst, sus = tensor_peak(pk, clk)
+    ach = flops / (ms / 1e3) / 1e12
+    line = {"metric": METRIC, "pass": "decoder", "value": T * dist.world / (ms / 1e3),
+            "unit": "tokens/s", "n_gpus": dist.world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic (seeded Gaussian, Mixtral-shaped)",
+            "config": {"workload": f"decoder-layer-{w.name}", "T": T, "seq_len": seq, "d_model": d,
+                       "d_ff": f, "n_experts": n, "top_k": k, "q_heads": hq, "kv_heads": hkv,
+                       "parallelism": f"replicas x{dist.world}"},
+            "tflops": flops * dist.world / (ms / 1e3) / 1e12,
+            "roofline": {"bound": "tensor", "achieved": ach, "peak": tc_peak, "unit": "TFLOP/s",
+                         "frac": ach / tc_peak, "traffic": None, "peak_kind": kind,
+                         "frac_of_sustained": ach / sus,
+                         "kernel": "whole decoder layer (projections, causal attention, MoE FLOPs)",
+                         "peak_source": f"{pk_kind} (MEASURED_PEAKS.json)"},
+            # rmsnorm, span offsets, q, k, v, attention, o, residual add, rmsnorm, then the MoE
+            # layer's router, grouping (1 or 3), gather, up, down, combine
+            "gpu_launches": (9 + 5 + (1 if T * k <= 32768 else 3)) * args.steps, "clocks": clk}
+    if dist.rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def ep_arm(args, w, dist):
     """Times the expert-parallel layer pass: rank r of N holds experts [r*n/N, (r+1)*n/N) and
     T tokens of its own (seeded per rank); one step = route, group, the count and row
@@ -940,6 +1017,8 @@ def main():
             backward_arm(args, w, dist)
         elif args.which == "attention":
             attention_arm(args, w, dist)
+        elif args.which == "decoder":
+            decoder_arm(args, w, dist)
         else:
             ours_arm(args, w, dist)
     finally:

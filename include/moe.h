@@ -301,6 +301,32 @@ moe_status moe_routing_stats(const int32_t* topk_idx, int T, int k, int n, int s
                              int64_t* expert_counts, int64_t* pair_counts, void* stream);
 
 /*
+ * One decoder layer of the Mixtral stack: Mistral 7B's layer with the feed-forward sub-block
+ * replaced by the MoE layer ("Mixtral of Experts", Método: 32 query heads, 8 key-value heads,
+ * hidden 4096, so head dimension 128):
+ *     a  = RMSNorm(h)
+ *     h1 = h + attention_gqa(a wqᵀ, a wkᵀ, a wvᵀ) woᵀ        (moe_attention_gqa, dh = 128)
+ *     y  = h1 + MoE(RMSNorm(h1))                              (moe_layer_forward)
+ * The pages name neither the normalisation nor a positional encoding: RMSNorm with unit
+ * weight (eps) before each sub-block, and no positional encoding.
+ *   h, y      [T, d] bf16 (y may alias h)
+ *   wq        [hq*128, d], wk / wv [hkv*128, d], wo [d, hq*128] bf16 (out x in)
+ *   w_gate, logit_bias, w1, w3, w2, k, n, f: as for moe_layer_forward
+ *   seq_len   tokens per sequence for the attention (0: one sequence)
+ *   topk_idx_out [T, k] int32, nullable: the MoE sub-block's expert choices
+ *   ws        at least moe_decoder_workspace_size(...) bytes; status header as usual
+ * bf16 only, d and f multiples of 64 (the tensor-core path); otherwise MOE_ERR_UNSUPPORTED.
+ * The projections run on the grouped tensor-core GEMM with one group holding every row.
+ */
+size_t moe_decoder_workspace_size(int T, int d, int f, int n, int k, int hq, int hkv);
+moe_status moe_decoder_layer_forward(const void* h, const void* wq, const void* wk, const void* wv,
+                                     const void* wo, const void* w_gate, const float* logit_bias,
+                                     const void* w1, const void* w3, const void* w2, int T, int d,
+                                     int f, int n, int k, int hq, int hkv, int seq_len, float eps,
+                                     int dtype, void* y, int32_t* topk_idx_out, void* ws,
+                                     size_t ws_bytes, void* stream);
+
+/*
  * Expert parallelism (EP): the layer spread over G GPUs by experts.  Tokens an expert must
  * process go to the GPU holding it and its outputs return to the original token positions
  * (newsflash.city digest, section "专家层的混合"; ja.news.hada.io, section "実装と推論効率").

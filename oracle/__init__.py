@@ -14,6 +14,6 @@ from .moe import (  # noqa: F401
     silu, expert_swiglu, group_by_expert, moe_layer, moe_layer_dense, rmsnorm,
     stacked_layer, near_tie_tokens, param_counts, consecutive_same_expert_rate,
     routing_statistics, sigmoid, silu_grad, softmax_backward, expert_swiglu_backward,
-    moe_layer_backward, attention_gqa, attention_gqa_rows,
+    moe_layer_backward, attention_gqa, attention_gqa_rows, decoder_layer,
 )
 from .ep import ep_experts_of, ep_send_counts, ep_exchange_plan, ep_load, ep_regroup  # noqa: F401

@@ -454,3 +454,35 @@ def attention_gqa_rows(q, k, v, rows, seq_len: int = 0) -> np.ndarray:
             scores = k[s0:i + 1, g] @ q[i, h] / np.sqrt(dh)
             out[r, h] = masked_softmax(scores) @ v[s0:i + 1, g]
     return out
+
+
+# ------------------------------------------------------------------------------------------
+# One decoder layer: the attention sub-block and the MoE sub-block, each with a residual
+# ------------------------------------------------------------------------------------------
+def decoder_layer(h, wq, wk, wv, wo, wg, w1, w3, w2, k: int, hq: int, hkv: int,
+                  seq_len: int = 0, eps: float = 1e-5, bias=None, *, with_logits: bool = False):
+    """One decoder layer of the Mixtral stack ("Mixtral of Experts" (xyznot.com summary),
+    Método: Mistral 7B's layers of attention (32 query heads, 8 key-value heads, hidden
+    4096) with every feed-forward sub-block replaced by the MoE layer):
+
+        a  = RMSNorm(h)
+        h1 = h + (attention_gqa(a wqᵀ, a wkᵀ, a wvᵀ) flattened) woᵀ
+        h2 = h1 + MoE(RMSNorm(h1))
+
+    The pages give neither the normalisation nor a positional encoding: RMSNorm with unit
+    weight before each sub-block (as in the stacked workload) and no positional encoding
+    (positions enter through the causal mask).  wq [hq*dh, d], wk / wv [hkv*dh, d],
+    wo [d, hq*dh] (out x in), dh = 128 in the pages' shapes.  ``with_logits`` also returns
+    the MoE sub-block's router logits."""
+    h = _f64(h)
+    T = h.shape[0]
+    a = rmsnorm(h, eps)
+    q = (a @ _f64(wq).T).reshape(T, hq, -1)
+    kk = (a @ _f64(wk).T).reshape(T, hkv, -1)
+    v = (a @ _f64(wv).T).reshape(T, hkv, -1)
+    o = attention_gqa(q, kk, v, seq_len).reshape(T, -1)
+    h1 = h + o @ _f64(wo).T
+    x2 = rmsnorm(h1, eps)
+    h2 = h1 + moe_layer(x2, wg, w1, w3, w2, k, bias)
+    return (h2, router_logits(x2, wg, bias)) if with_logits else h2
+

@@ -25,7 +25,8 @@ __all__ = [
     "moe_layer_forward_train", "moe_layer_backward_saved", "moe_attention_gqa",
     "moe_layer_forward", "moe_check_device_error", "moe_set_wait_limit_ns", "moe_set_tc_form",
     "MOE_TC_FORM_AUTO", "MOE_TC_FORM_SINGLE", "MOE_TC_FORM_PAIR", "moe_version",
-    "library_path", "moe_ep_regroup", "moe_gather_rows",
+    "library_path", "moe_ep_regroup", "moe_gather_rows", "moe_decoder_workspace_size",
+    "decoder_workspace", "moe_decoder_layer_forward",
 ]
 
 
@@ -382,4 +383,39 @@ def moe_gather_rows(src: torch.Tensor, index: torch.Tensor, k: int = 1, *,
                                        _ptr(dst), _stream(stream))
     check("moe_gather_rows", st)
     return dst
+
+
+def moe_decoder_workspace_size(T: int, d: int, f: int, n: int, k: int, hq: int, hkv: int) -> int:
+    return int(_native.lib().moe_decoder_workspace_size(T, d, f, n, k, hq, hkv))
+
+
+def decoder_workspace(T: int, d: int, f: int, n: int, k: int, hq: int, hkv: int,
+                      device="cuda") -> torch.Tensor:
+    """A workspace for moe_decoder_layer_forward with its status header zeroed."""
+    size = moe_decoder_workspace_size(T, d, f, n, k, hq, hkv)
+    if size == 0:
+        raise ValueError("invalid sizes")
+    ws = torch.empty(size, dtype=torch.uint8, device=device)
+    ws[:256].zero_()
+    return ws
+
+
+def moe_decoder_layer_forward(h: torch.Tensor, wq: torch.Tensor, wk: torch.Tensor, wv: torch.Tensor,
+                              wo: torch.Tensor, w_gate: torch.Tensor, w1: torch.Tensor,
+                              w3: torch.Tensor, w2: torch.Tensor, k: int, hq: int, hkv: int,
+                              ws: torch.Tensor, *, seq_len: int = 0, eps: float = 1e-5,
+                              logit_bias: Optional[torch.Tensor] = None,
+                              y: Optional[torch.Tensor] = None,
+                              topk_idx_out: Optional[torch.Tensor] = None, stream=None):
+    """One decoder layer (attention sub-block + MoE sub-block, each with its residual)."""
+    T, d = h.shape
+    n, f, _ = w1.shape
+    if y is None:
+        y = torch.empty_like(h)
+    st = _native.lib().moe_decoder_layer_forward(
+        _ptr(h), _ptr(wq), _ptr(wk), _ptr(wv), _ptr(wo), _ptr(w_gate), _ptr(logit_bias), _ptr(w1),
+        _ptr(w3), _ptr(w2), T, d, f, n, k, hq, hkv, seq_len, eps, dtype_code(h.dtype), _ptr(y),
+        _ptr(topk_idx_out), _ptr(ws), ws.numel(), _stream(stream))
+    check("moe_decoder_layer_forward", st)
+    return y
 

@@ -52,6 +52,9 @@ SIGNATURES = {
                                       _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_layer_backward": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P,
                                 _P, _P, _P, _SZ, _P]),
+    "moe_decoder_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
+    "moe_decoder_layer_forward": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I,
+                                       _I, _I, _I, _F, _I, _P, _P, _P, _SZ, _P]),
     "moe_ep_regroup": (_I, [_P, _I, _I, _I, _P, _P, _P, _P]),
     "moe_gather_rows": (_I, [_P, _I, _P, _I, _I, _SZ, _P, _P]),
     "moe_check_device_error": (_I, [_P, _SZ, _P]),

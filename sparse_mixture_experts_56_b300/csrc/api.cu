@@ -90,6 +90,35 @@ BwdLayout bwd_layout(long long T, long long d, long long f, int n, int k, int dt
   return B;
 }
 
+// Decoder layer workspace: the MoE layer's workspace first (its status header is the
+// decoder's), then the attention sub-block's buffers.
+struct DecLayout {
+  size_t offs, xn, q, k, v, o, oproj, h1, xn2, total;
+};
+
+DecLayout dec_layout(long long T, long long d, long long f, int n, int k, int hq, int hkv) {
+  const Layout L = layout(T, d, f, n, k, MOE_BF16);
+  DecLayout D;
+  size_t off = L.total;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off += align_up(bytes);
+    return at;
+  };
+  const size_t row = (size_t)T * 2;
+  D.offs = take(2 * sizeof(int32_t));
+  D.xn = take(row * d);
+  D.q = take(row * hq * 128);
+  D.k = take(row * hkv * 128);
+  D.v = take(row * hkv * 128);
+  D.o = take(row * hq * 128);
+  D.oproj = take(row * d);
+  D.h1 = take(row * d);
+  D.xn2 = take(row * d);
+  D.total = off;
+  return D;
+}
+
 inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 inline bool dtype_ok(int dt) { return dt == MOE_F32 || dt == MOE_BF16; }
 
@@ -557,6 +586,63 @@ moe_status moe_attention_gqa(const void* q, const void* k, const void* v, int T,
   return cuda_status(launch_attention_gqa((const bf16*)q, (const bf16*)k, (const bf16*)v, T,
                                           seq_len, hq, hkv, (bf16*)out, status_word(ws),
                                           g_wait_ns.load(), (cudaStream_t)stream));
+}
+
+size_t moe_decoder_workspace_size(int T, int d, int f, int n, int k, int hq, int hkv) {
+  if (!sizes_ok(T, d, f, n, k) || hq < 1 || hkv < 1 || hq % hkv) return 0;
+  return dec_layout(T, d, f, n, k, hq, hkv).total;
+}
+
+moe_status moe_decoder_layer_forward(const void* h, const void* wq, const void* wk, const void* wv,
+                                     const void* wo, const void* w_gate, const float* logit_bias,
+                                     const void* w1, const void* w3, const void* w2, int T, int d,
+                                     int f, int n, int k, int hq, int hkv, int seq_len, float eps,
+                                     int dtype, void* y, int32_t* topk_idx_out, void* ws,
+                                     size_t ws_bytes, void* stream) {
+  if (!dtype_ok(dtype) || !sizes_ok(T, d, f, n, k) || hq < 1 || hkv < 1 || hq % hkv ||
+      seq_len < 0 || !(eps >= 0.f))
+    return MOE_ERR_INVALID_ARG;
+  if ((long long)T * hq * 128 >= (1ll << 40)) return MOE_ERR_INVALID_ARG;
+  if (dtype != MOE_BF16 || !use_tc(dtype, d, f)) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  if (!h || !wq || !wk || !wv || !wo || !w_gate || !w1 || !w3 || !w2 || !y)
+    return MOE_ERR_INVALID_ARG;
+  const void* ptrs[] = {h, wq, wk, wv, wo, w_gate, w1, w3, w2, y};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return MOE_ERR_INVALID_ARG;
+  const Layout L = layout(T, d, f, n, k, dtype);
+  const DecLayout D = dec_layout(T, d, f, n, k, hq, hkv);
+  if (!ws || ws_bytes < D.total || !aligned16(ws)) return MOE_ERR_WORKSPACE;
+  cudaStream_t s = (cudaStream_t)stream;
+  char* base = static_cast<char*>(ws);
+  int32_t* offs = reinterpret_cast<int32_t*>(base + D.offs);
+  bf16* xn = reinterpret_cast<bf16*>(base + D.xn);
+  bf16* q = reinterpret_cast<bf16*>(base + D.q);
+  bf16* kk = reinterpret_cast<bf16*>(base + D.k);
+  bf16* v = reinterpret_cast<bf16*>(base + D.v);
+  bf16* o = reinterpret_cast<bf16*>(base + D.o);
+  bf16* oproj = reinterpret_cast<bf16*>(base + D.oproj);
+  bf16* h1 = reinterpret_cast<bf16*>(base + D.h1);
+  bf16* xn2 = reinterpret_cast<bf16*>(base + D.xn2);
+  uint32_t* st = status_word(ws);
+  const unsigned long long wn = g_wait_ns.load();
+  const int dq = hq * 128, dkv = hkv * 128;
+  // attention sub-block: RMSNorm, the three projections (plain GEMMs: the grouped tensor-core
+  // kernel over one group holding every row), causal GQA attention, the output projection and
+  // the residual
+  cudaError_t e = launch_rmsnorm(h, T, d, eps, dtype, xn, s);
+  if (e == cudaSuccess) e = launch_span_offsets(offs, T, s);
+  if (e == cudaSuccess) e = launch_down_tc(xn, offs, (const bf16*)wq, T, dq, d, 1, q, st, wn, s);
+  if (e == cudaSuccess) e = launch_down_tc(xn, offs, (const bf16*)wk, T, dkv, d, 1, kk, st, wn, s);
+  if (e == cudaSuccess) e = launch_down_tc(xn, offs, (const bf16*)wv, T, dkv, d, 1, v, st, wn, s);
+  if (e == cudaSuccess) e = launch_attention_gqa(q, kk, v, T, seq_len, hq, hkv, o, st, wn, s);
+  if (e == cudaSuccess) e = launch_down_tc(o, offs, (const bf16*)wo, T, d, dq, 1, oproj, st, wn, s);
+  if (e == cudaSuccess) e = launch_add_rows_bf16(h, oproj, (size_t)T * d, h1, s);
+  // MoE sub-block: RMSNorm, the layer, the residual (in its combine)
+  if (e == cudaSuccess) e = launch_rmsnorm(h1, T, d, eps, dtype, xn2, s);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  return moe_layer_forward(xn2, w_gate, logit_bias, w1, w3, w2, h1, T, d, f, n, k, dtype, y,
+                           topk_idx_out, nullptr, ws, L.total, stream);
 }
 
 moe_status moe_routing_stats(const int32_t* topk_idx, int T, int k, int n, int seq_len,

@@ -81,7 +81,52 @@ __global__ void __launch_bounds__(256) combine_generic_kernel(const T* __restric
   }
 }
 
+// y = a + b row by row (bf16 storage, fp32 add, one rounding): the residual of a sub-block
+// whose output is not already summed with it.
+__global__ void __launch_bounds__(256) add_rows_bf16_kernel(const uint4* __restrict__ a,
+                                                            const uint4* __restrict__ b,
+                                                            size_t vecs, uint4* __restrict__ y) {
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < vecs;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const uint4 u = __ldg(a + i), v = __ldg(b + i);
+    const __nv_bfloat162* pu = reinterpret_cast<const __nv_bfloat162*>(&u);
+    const __nv_bfloat162* pv = reinterpret_cast<const __nv_bfloat162*>(&v);
+    uint4 o;
+    __nv_bfloat162* po = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 x = __bfloat1622float2(pu[j]), z = __bfloat1622float2(pv[j]);
+      po[j] = __floats2bfloat162_rn(x.x + z.x, x.y + z.y);
+    }
+    y[i] = o;
+  }
+}
+
+// offsets of one group holding every row: {0, rows}
+__global__ void span_offsets_kernel(int32_t* off, int rows) {
+  if (threadIdx.x == 0) {
+    off[0] = 0;
+    off[1] = rows;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_add_rows_bf16(const void* a, const void* b, size_t elems, void* y,
+                                 cudaStream_t s) {
+  if (elems == 0) return cudaSuccess;
+  const size_t vecs = elems / 8;
+  const int cap = device_sm_count() * 8;
+  const size_t want = (vecs + 255) / 256;
+  const int grid = (int)(want < (size_t)cap ? (want > 0 ? want : 1) : cap);
+  add_rows_bf16_kernel<<<grid, 256, 0, s>>>((const uint4*)a, (const uint4*)b, vecs, (uint4*)y);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_span_offsets(int32_t* off, int rows, cudaStream_t s) {
+  span_offsets_kernel<<<1, 32, 0, s>>>(off, rows);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_combine(const void* y_perm, const int32_t* inv_perm, const float* w,
                            const void* residual, int T, int d, int k, int dtype, void* y,

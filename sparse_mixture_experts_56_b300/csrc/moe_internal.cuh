@@ -53,6 +53,11 @@ cudaError_t launch_permute(const int32_t* idx, int A, int n, int32_t* offsets, i
 cudaError_t launch_gather_rows(const void* x, const int32_t* perm, int A, int k, size_t row_bytes,
                                void* x_perm, cudaStream_t s);
 
+// y = a + b for bf16 buffers of `elems` elements (a multiple of 8, 16-byte aligned)
+cudaError_t launch_add_rows_bf16(const void* a, const void* b, size_t elems, void* y, cudaStream_t s);
+// off[0] = 0, off[1] = rows: one group of every row (a plain GEMM through the grouped kernels)
+cudaError_t launch_span_offsets(int32_t* off, int rows, cudaStream_t s);
+
 cudaError_t launch_combine(const void* y_perm, const int32_t* inv_perm, const float* w,
                            const void* residual, int T, int d, int k, int dtype, void* y,
                            cudaStream_t s);

@@ -498,13 +498,54 @@ def check_ep_plan(o):
     assert p[0]["recv_counts"][:, 0].tolist() == [1, 0, 0, 1]
 
 
+def check_decoder_layer(o):
+    """One decoder layer against torch primitives: F.rms_norm, F.linear, causal SDPA with the
+    key-value heads repeated per group, and the MoE written with torch.topk / softmax (ties
+    have probability zero with these Gaussian inputs)."""
+    rng = np.random.default_rng(95)
+    T, hq, hkv, dh, n, k, f, seq = 21, 4, 2, 8, 4, 2, 12, 8
+    d = hq * dh
+    h = rng.standard_normal((T, d))
+    wq, wo = rng.standard_normal((hq * dh, d)) / 4, rng.standard_normal((d, hq * dh)) / 4
+    wk, wv = rng.standard_normal((hkv * dh, d)) / 4, rng.standard_normal((hkv * dh, d)) / 4
+    wg = rng.standard_normal((d, n))
+    w1, w3 = rng.standard_normal((n, f, d)) / 4, rng.standard_normal((n, f, d)) / 4
+    w2 = rng.standard_normal((n, d, f)) / 4
+    out = o.decoder_layer(h, wq, wk, wv, wo, wg, w1, w3, w2, k, hq, hkv, seq)
+    t = torch.from_numpy
+    ht = t(h)
+    a = F.rms_norm(ht, (d,), eps=1e-5)
+    q = F.linear(a, t(wq)).view(T, hq, dh)
+    kk = F.linear(a, t(wk)).view(T, hkv, dh)
+    v = F.linear(a, t(wv)).view(T, hkv, dh)
+    att = torch.zeros(T, hq, dh, dtype=torch.float64)
+    for s0 in range(0, T, seq):
+        sl = slice(s0, min(T, s0 + seq))
+        tq = q[sl].transpose(0, 1)
+        tk = kk[sl].transpose(0, 1).repeat_interleave(hq // hkv, dim=0)
+        tv = v[sl].transpose(0, 1).repeat_interleave(hq // hkv, dim=0)
+        att[sl] = F.scaled_dot_product_attention(tq, tk, tv, is_causal=True).transpose(0, 1)
+    h1 = ht + F.linear(att.reshape(T, d), t(wo))
+    x2 = F.rms_norm(h1, (d,), eps=1e-5)
+    top, ti = torch.topk(x2 @ t(wg), k, dim=1)
+    gw = torch.softmax(top, dim=1)
+    moe = torch.zeros_like(h1)
+    for s in range(k):
+        for e in range(n):
+            rows = ti[:, s] == e
+            if rows.any():
+                moe[rows] += gw[rows, s:s + 1] * F.linear(
+                    F.silu(F.linear(x2[rows], t(w1[e]))) * F.linear(x2[rows], t(w3[e])), t(w2[e]))
+    np.testing.assert_allclose(out, (h1 + moe).numpy(), rtol=1e-10, atol=1e-11)
+
+
 CHECKS = [check_worked_example, check_gate_invariants, check_topk_bruteforce,
           check_softmax_order_equivalence, check_single_expert_is_plain_ffn,
           check_k_equals_n_is_dense_softmax_mixture, check_sparse_equals_dense, check_grouping,
           check_silu, check_bias_enters_before_topk, check_rmsnorm, check_param_counts,
           check_locality_metric, check_routing_statistics, check_backward_finite_differences,
           check_backward_autograd, check_backward_special_cases, check_attention,
-          check_near_tie_tokens, check_attention_rows, check_ep_plan]
+          check_near_tie_tokens, check_attention_rows, check_ep_plan, check_decoder_layer]
 
 
 @pytest.mark.parametrize("check", CHECKS, ids=lambda c: c.__name__[6:])
@@ -703,6 +744,18 @@ def _mut_ep_order_by_assignment(idx_per_rank, n, G):
     return plans
 
 
+def _mut_decoder_moe_on_h(h, wq, wk, wv, wo, wg, w1, w3, w2, k, hq, hkv, seq_len=0, eps=1e-5,
+                          bias=None):
+    """the MoE sub-block normalises the layer input h instead of h1"""
+    h = np.asarray(h, dtype=np.float64)
+    T = h.shape[0]
+    a = moe_oracle.rmsnorm(h, eps)
+    q = (a @ np.asarray(wq).T).reshape(T, hq, -1)
+    kk = (a @ np.asarray(wk).T).reshape(T, hkv, -1)
+    v = (a @ np.asarray(wv).T).reshape(T, hkv, -1)
+    h1 = h + moe_oracle.attention_gqa(q, kk, v, seq_len).reshape(T, -1) @ np.asarray(wo).T
+    return h1 + moe_oracle.moe_layer(a, wg, w1, w3, w2, k, bias)
+
 MUTATIONS = {
     "silu->sigmoid": ("silu", _mut_sigmoid_for_silu),
     "swap w1/w3": ("expert_swiglu", _mut_swap_w1_w3),
@@ -728,6 +781,7 @@ MUTATIONS = {
     "near-tie order loop off by one": ("near_tie_tokens", _mut_near_tie_order_off_by_one),
     "attention rows without the diagonal": ("attention_gqa_rows", _mut_attn_rows_excludes_self),
     "EP experts strided over ranks": (ep_oracle, "ep_experts_of", _mut_ep_strided_experts),
+    "decoder MoE normalises h, not h1": ("decoder_layer", _mut_decoder_moe_on_h),
     "EP rows ordered by assignment first": (ep_oracle, "ep_exchange_plan", _mut_ep_order_by_assignment),
 }
 

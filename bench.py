@@ -168,7 +168,7 @@ class ClockSampler:
                  "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self._thr = threading.Thread(target=self._run_smi, daemon=True)
-            time.sleep(0.3)   # let the first samples arrive
+            time.sleep(1.0)   # nvidia-smi's start-up is over before the timed region
         if self._thr:
             self._thr.start()
 
@@ -355,11 +355,14 @@ def ours_arm(args, w, dist):
     line = forward_line(args, w, dist, dev, with_cpu=True)
     if w.wid != 2 and not args.no_decode:
         # the HBM-bound decode batch, measured the same way (its own inputs, timed region,
-        # clocks, roofline and end-to-end figure), carried in the same line
+        # clocks, roofline and end-to-end figure), carried in the same line; a decode step is
+        # half a millisecond, so it is timed over at least 400 steps (the number is reported)
         torch.cuda.empty_cache()
-        dec = forward_line(args, workloads.workload(2), dist, dev, with_cpu=False)
-        line["decode"] = {k: dec[k] for k in ("value", "unit", "ms_per_step", "tflops", "roofline",
-                                              "e2e", "clocks", "gpu_launches", "config",
+        dargs = argparse.Namespace(**vars(args))
+        dargs.steps = max(args.steps, 400)
+        dec = forward_line(dargs, workloads.workload(2), dist, dev, with_cpu=False)
+        line["decode"] = {k: dec[k] for k in ("value", "unit", "steps", "ms_per_step", "tflops",
+                                              "roofline", "e2e", "clocks", "gpu_launches", "config",
                                               "expert_counts") if k in dec}
     if dist.rank == 0:
         print(json.dumps(line), flush=True)

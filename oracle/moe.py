@@ -460,7 +460,8 @@ def attention_gqa_rows(q, k, v, rows, seq_len: int = 0) -> np.ndarray:
 # One decoder layer: the attention sub-block and the MoE sub-block, each with a residual
 # ------------------------------------------------------------------------------------------
 def decoder_layer(h, wq, wk, wv, wo, wg, w1, w3, w2, k: int, hq: int, hkv: int,
-                  seq_len: int = 0, eps: float = 1e-5, bias=None, *, with_logits: bool = False):
+                  seq_len: int = 0, eps: float = 1e-5, bias=None, *, with_logits: bool = False,
+                  tokens: Optional[Sequence[int]] = None):
     """One decoder layer of the Mixtral stack ("Mixtral of Experts" (xyznot.com summary),
     Método: Mistral 7B's layers of attention (32 query heads, 8 key-value heads, hidden
     4096) with every feed-forward sub-block replaced by the MoE layer):
@@ -473,16 +474,24 @@ def decoder_layer(h, wq, wk, wv, wo, wg, w1, w3, w2, k: int, hq: int, hkv: int,
     weight before each sub-block (as in the stacked workload) and no positional encoding
     (positions enter through the causal mask).  wq [hq*dh, d], wk / wv [hkv*dh, d],
     wo [d, hq*dh] (out x in), dh = 128 in the pages' shapes.  ``with_logits`` also returns
-    the MoE sub-block's router logits."""
+    the MoE sub-block's router logits; ``tokens`` evaluates only those rows (keys and values
+    still come from every token, queries and everything after them only from those rows)."""
     h = _f64(h)
     T = h.shape[0]
     a = rmsnorm(h, eps)
-    q = (a @ _f64(wq).T).reshape(T, hq, -1)
     kk = (a @ _f64(wk).T).reshape(T, hkv, -1)
     v = (a @ _f64(wv).T).reshape(T, hkv, -1)
-    o = attention_gqa(q, kk, v, seq_len).reshape(T, -1)
-    h1 = h + o @ _f64(wo).T
+    if tokens is None:
+        q = (a @ _f64(wq).T).reshape(T, hq, -1)
+        o = attention_gqa(q, kk, v, seq_len).reshape(T, -1)
+        hs = h
+    else:
+        tokens = np.asarray(tokens, dtype=np.int64)
+        q = np.zeros((T, hq, kk.shape[2]))
+        q[tokens] = (a[tokens] @ _f64(wq).T).reshape(tokens.size, hq, -1)
+        o = attention_gqa_rows(q, kk, v, tokens, seq_len).reshape(tokens.size, -1)
+        hs = h[tokens]
+    h1 = hs + o @ _f64(wo).T
     x2 = rmsnorm(h1, eps)
     h2 = h1 + moe_layer(x2, wg, w1, w3, w2, k, bias)
     return (h2, router_logits(x2, wg, bias)) if with_logits else h2
-

@@ -113,3 +113,84 @@ def test_full_size_stack_of_four(moe):
         rel = assert_close_rel(to_numpy_f32(h)[tok][keep], href[keep], TOL["bf16"], f"h after layer {layer}")
         print(f"\nlayer {layer}: {keep.sum()}/{tok.size} tokens compared, rel err {rel:.3e}, counts {hist[-1]}")
     assert all(sum(c) == w.T * w.k for c in hist)
+
+
+@pytest.mark.parametrize("wid,G", [(2, 8), (3, 4)])
+def test_full_size_expert_parallel_emulated(moe, wid, G):
+    """Expert parallelism at the full sizes through the kernels, G ranks emulated on one GPU:
+    the decode batch over 8 ranks of one expert each (4 tokens per rank) and the prefill
+    batch over 4 ranks of two experts (1024 tokens per rank).  Every rank's routing is
+    checked on every token, its outputs on a token sample, against the single-GPU oracle."""
+    from sparse_mixture_experts_56_b300 import ep
+    w = workloads.workload(wid)
+    inp = workloads.make_inputs(w)
+    g = {k: to_device(inp[k], w, DEV) for k in ("x", "wg", "w1", "w3", "w2")}
+    Tr = w.T // G
+    xs = [g["x"][r * Tr:(r + 1) * Tr].contiguous() for r in range(G)]
+    ys, stats = ep.ep_layer_forward_emulated(ep.NativeOps(DEV), xs, g["wg"], g["w1"], g["w3"], g["w2"],
+                                             w.k, w.n, G)
+    torch.cuda.synchronize()
+    del g
+    xf = workloads.as_f32(inp["x"], w)
+    wgf = workloads.as_f32(inp["wg"], w)
+    f = {k: workloads.as_f32(inp[k], w) for k in ("w1", "w3", "w2")}
+    rng = np.random.default_rng(wid * 10 + G)
+    for r in range(G):
+        rows = slice(r * Tr, (r + 1) * Tr)
+        lref = oracle.router_logits(xf[rows], wgf)
+        gi = stats["topk_idx"][r].cpu().numpy().astype(np.int64)
+        check_selection(gi, lref, w.k)
+        tok = _sample(Tr, gi, w.n, rng, per_expert=2, extra=8)
+        yref = oracle.moe_layer(xf[rows], wgf, f["w1"], f["w3"], f["w2"], w.k, idx=gi,
+                                w=gate_weights_for(gi, lref), tokens=tok)
+        assert_close_rel(to_numpy_f32(ys[r])[tok], yref, TOL["bf16"], f"rank {r}")
+    plans = oracle.ep_exchange_plan([i.cpu().numpy() for i in stats["topk_idx"]], w.n, G)
+    assert stats["expert_rows"] == oracle.ep_load(plans).tolist()
+    print(f"\n{w.name} over {G} emulated ranks: rows per rank {stats['expert_rows']}")
+
+
+def test_full_size_decoder_layer(moe):
+    """One decoder layer at the pages' shapes (d=4096, 32 query / 8 key-value heads of 128,
+    f=14336, 8 experts, top-2) over one 4096-token sequence: routing on every token within
+    the band the bf16 roundings before the router allow, outputs on a token sample against
+    the oracle (keys and values from every token, the rest on the sample)."""
+    w = workloads.workload(3)
+    T, d, f, n, k, hq, hkv = w.T, w.d, w.f, w.n, w.k, 32, 8
+    inp = workloads.make_inputs(w)
+    rng = np.random.default_rng(77)
+
+    def bf16(shape, scale):
+        bits = workloads.bf16_round_bits((rng.standard_normal(shape) * scale).astype(np.float32))
+        return bits, workloads.bf16_bits_to_f32(bits).astype(np.float64)
+
+    wqb, wq = bf16((hq * 128, d), d ** -0.5)
+    wkb, wk = bf16((hkv * 128, d), d ** -0.5)
+    wvb, wv = bf16((hkv * 128, d), d ** -0.5)
+    wob, wo = bf16((d, hq * 128), (hq * 128) ** -0.5)
+    dev = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).to(DEV)
+    g = {t: to_device(inp[t], w, DEV) for t in ("x", "wg", "w1", "w3", "w2")}
+    ws = moe.decoder_workspace(T, d, f, n, k, hq, hkv, DEV)
+    idx = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    y = moe.moe_decoder_layer_forward(g["x"], dev(wqb), dev(wkb), dev(wvb), dev(wob), g["wg"], g["w1"],
+                                      g["w3"], g["w2"], k, hq, hkv, ws, seq_len=T, topk_idx_out=idx)
+    assert moe.moe_check_device_error(ws) == 0
+    yg = to_numpy_f32(y)
+    gi = idx.cpu().numpy().astype(np.int64)
+    del g, ws
+    torch.cuda.empty_cache()
+    h = workloads.as_f32(inp["x"], w).astype(np.float64)
+    wgf = workloads.as_f32(inp["wg"], w)
+    fw = {t: workloads.as_f32(inp[t], w) for t in ("w1", "w3", "w2")}
+    tok = np.unique(np.concatenate([[0, 1, 127, 128, T - 1], rng.choice(T, size=35, replace=False)]))
+    yref, lref = oracle.decoder_layer(h, wq, wk, wv, wo, wgf, fw["w1"], fw["w3"], fw["w2"], k, hq, hkv,
+                                      T, with_logits=True, tokens=tok)
+    gs = gi[tok]
+    same = np.all(np.sort(gs, 1) == np.sort(oracle.topk_select(lref, k), 1), axis=1)
+    x2 = oracle.rmsnorm(h[tok])
+    sigma = 2.0 ** -9 / np.sqrt(3) * np.sqrt(((x2[:, :, None] * wgf[None]) ** 2).sum(1)).max(1)
+    kth = np.sort(lref, 1)[:, ::-1][:, k - 1]
+    chosen = np.take_along_axis(lref, gs, axis=1)
+    assert np.all(chosen[~same] >= kth[~same, None] - 20 * sigma[~same, None])
+    assert same.sum() >= 0.85 * tok.size
+    rel = assert_close_rel(yg[tok][same], yref[same], TOL["bf16"])
+    print(f"\ndecoder layer T={T}: {same.sum()}/{tok.size} sampled tokens compared, rel err {rel:.3e}")

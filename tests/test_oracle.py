@@ -537,6 +537,10 @@ def check_decoder_layer(o):
                 moe[rows] += gw[rows, s:s + 1] * F.linear(
                     F.silu(F.linear(x2[rows], t(w1[e]))) * F.linear(x2[rows], t(w3[e])), t(w2[e]))
     np.testing.assert_allclose(out, (h1 + moe).numpy(), rtol=1e-10, atol=1e-11)
+    # the evaluation on a token sample gives the same rows
+    sel = np.array([0, 7, 8, 15, 20])
+    np.testing.assert_allclose(o.decoder_layer(h, wq, wk, wv, wo, wg, w1, w3, w2, k, hq, hkv, seq,
+                                               tokens=sel), out[sel], rtol=1e-12, atol=1e-12)
 
 
 CHECKS = [check_worked_example, check_gate_invariants, check_topk_bruteforce,
@@ -745,7 +749,7 @@ def _mut_ep_order_by_assignment(idx_per_rank, n, G):
 
 
 def _mut_decoder_moe_on_h(h, wq, wk, wv, wo, wg, w1, w3, w2, k, hq, hkv, seq_len=0, eps=1e-5,
-                          bias=None):
+                          bias=None, **_):
     """the MoE sub-block normalises the layer input h instead of h1"""
     h = np.asarray(h, dtype=np.float64)
     T = h.shape[0]

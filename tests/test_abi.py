@@ -128,6 +128,34 @@ def test_host_validation_rejects_before_launch(lib):
     assert lib.moe_attention_gqa(fake, fake, fake, 8, 0, 8, 2, 128, 0, fake, fake, 256, nul) == UNSUPPORTED
     assert lib.moe_attention_gqa(fake, fake, fake, 8, 0, 8, 2, 128, 1, fake, fake, 16, nul) == WORKSPACE
     assert lib.moe_attention_gqa(nul, fake, fake, 8, 0, 8, 2, 128, 1, fake, fake, 256, nul) == INVALID
+    # expert-parallel regrouping and the row gather: sizes and pointers before launch
+    assert lib.moe_ep_regroup(fake, 0, 4, 10, fake, fake, fake, nul) == INVALID
+    assert lib.moe_ep_regroup(fake, 2, 33, 10, fake, fake, fake, nul) == INVALID
+    assert lib.moe_ep_regroup(fake, 2, 4, -1, fake, fake, fake, nul) == INVALID
+    assert lib.moe_ep_regroup(fake, 2, 4, 10, fake, nul, fake, nul) == INVALID
+    assert lib.moe_ep_regroup(nul, 2, 4, 0, fake, nul, nul, nul) == INVALID
+    assert lib.moe_gather_rows(fake, 4, fake, -1, 1, 16, fake, nul) == INVALID
+    assert lib.moe_gather_rows(fake, 4, fake, 8, 0, 16, fake, nul) == INVALID
+    assert lib.moe_gather_rows(fake, 4, fake, 8, 1, 0, fake, nul) == INVALID
+    assert lib.moe_gather_rows(nul, 4, fake, 8, 1, 16, fake, nul) == INVALID
+    assert lib.moe_gather_rows(nul, 0, nul, 0, 1, 16, nul, nul) == OK
+    # decoder layer: bf16 tensor-core shapes only, grouping of heads, workspace
+    dws = lib.moe_decoder_workspace_size
+    assert dws(64, 512, 256, 8, 2, 4, 2) > lib.moe_workspace_size(64, 512, 256, 8, 2, 1)
+    assert dws(64, 512, 256, 8, 2, 4, 3) == 0 and dws(64, 512, 256, 8, 9, 4, 2) == 0
+    args = [fake] * 6 + [nul] + [fake] * 3
+    assert lib.moe_decoder_layer_forward(*args, 64, 512, 256, 8, 2, 4, 3, 0, 1e-5, 1, fake, nul,
+                                         fake, 1 << 30, nul) == INVALID
+    assert lib.moe_decoder_layer_forward(*args, 64, 512, 256, 8, 2, 4, 2, 0, -1.0, 1, fake, nul,
+                                         fake, 1 << 30, nul) == INVALID
+    assert lib.moe_decoder_layer_forward(*args, 64, 512, 256, 8, 2, 4, 2, 0, 1e-5, 0, fake, nul,
+                                         fake, 1 << 30, nul) == UNSUPPORTED
+    assert lib.moe_decoder_layer_forward(*args, 64, 500, 256, 8, 2, 4, 2, 0, 1e-5, 1, fake, nul,
+                                         fake, 1 << 30, nul) == UNSUPPORTED
+    assert lib.moe_decoder_layer_forward(*args, 64, 512, 256, 8, 2, 4, 2, 0, 1e-5, 1, fake, nul,
+                                         fake, 256, nul) == WORKSPACE
+    assert lib.moe_decoder_layer_forward(*args, 0, 512, 256, 8, 2, 4, 2, 0, 1e-5, 1, fake, nul,
+                                         fake, 0, nul) == OK
     assert lib.moe_check_device_error(nul, 0, nul) == WORKSPACE
     lib.moe_set_wait_limit_ns(0)
 

@@ -112,3 +112,60 @@ def test_ep_one_nccl_rank(moe, tmp_path):
         dist.destroy_process_group()
     assert stats["expert_rows"] == Tr * k and stats["recv_rows"] == [Tr * k]
     _check_rank_output(y, stats["topk_idx"], inp, w, slice(0, Tr))
+
+
+def test_ep_ranks_without_tokens_or_rows(moe):
+    """Degenerate expert-parallel passes: a rank with no tokens of its own, and ranks whose
+    experts receive no rows at all (every token routed to rank 0's experts by the logit
+    bias); the others still match the oracle and the empty ones return empty outputs."""
+    from sparse_mixture_experts_56_b300 import ep
+    G, Tr, d, f, n, k = 4, 96, 256, 384, 8, 2
+    w = workloads.custom(G * Tr, d, f, n, k, "bf16", wid=497)
+    inp = workloads.make_inputs(w)
+    g = {t: to_device(inp[t], w, DEV) for t in ("x", "wg", "w1", "w3", "w2")}
+    ops = ep.NativeOps(DEV)
+    # rank 2 has no tokens
+    xs = [g["x"][r * Tr:(r + 1) * Tr].contiguous() for r in range(G)]
+    xs[2] = g["x"][:0].contiguous()
+    ys, stats = ep.ep_layer_forward_emulated(ops, xs, g["wg"], g["w1"], g["w3"], g["w2"], k, n, G)
+    torch.cuda.synchronize()
+    assert ys[2].shape == (0, d)
+    for r in (0, 1, 3):
+        _check_rank_output(ys[r], stats["topk_idx"][r], inp, w, slice(r * Tr, (r + 1) * Tr))
+    # a bias that sends every token to experts 0 and 1 (both on rank 0): ranks 1-3 get no rows
+    bias = torch.tensor([60.0, 50.0] + [0.0] * (n - 2), device=DEV)
+    xs = [g["x"][r * Tr:(r + 1) * Tr].contiguous() for r in range(G)]
+    ys, stats = ep.ep_layer_forward_emulated(ops, xs, g["wg"], g["w1"], g["w3"], g["w2"], k, n, G, bias)
+    torch.cuda.synchronize()
+    assert stats["expert_rows"] == [G * Tr * k, 0, 0, 0]
+    f32 = f32_inputs(inp, w)
+    for r in range(G):
+        gi = stats["topk_idx"][r].cpu().numpy().astype(np.int64)
+        assert np.all(np.sort(gi, 1) == [0, 1])
+        rows = slice(r * Tr, (r + 1) * Tr)
+        lref = oracle.router_logits(f32["x"][rows], f32["wg"], bias.cpu().numpy())
+        yref = oracle.moe_layer(f32["x"][rows], f32["wg"], f32["w1"], f32["w3"], f32["w2"], k,
+                                idx=gi, w=gate_weights_for(gi, lref))
+        assert_close_rel(to_numpy_f32(ys[r]), yref, TOL["bf16"])
+
+
+def test_empty_inputs(moe):
+    """T = 0 through the layer, the decoder layer and the attention: nothing launched that
+    reads an input, expert offsets all zero, empty outputs."""
+    ws = moe.workspace(1, 256, 256, 8, 2, torch.bfloat16, DEV)
+    x = torch.empty((0, 256), dtype=torch.bfloat16, device=DEV)
+    wg = torch.zeros((256, 8), dtype=torch.bfloat16, device=DEV)
+    w1 = torch.zeros((8, 256, 256), dtype=torch.bfloat16, device=DEV)
+    off = torch.full((9,), -1, dtype=torch.int32, device=DEV)
+    y = moe.moe_layer_forward(x, wg, w1, w1, w1, 2, ws, expert_offsets_out=off)
+    assert y.shape == (0, 256) and off.cpu().tolist() == [0] * 9
+    dws = moe.decoder_workspace(1, 256, 256, 8, 2, 2, 1, DEV)
+    wq = torch.zeros((256, 256), dtype=torch.bfloat16, device=DEV)
+    wk = torch.zeros((128, 256), dtype=torch.bfloat16, device=DEV)
+    y = moe.moe_decoder_layer_forward(x, wq, wk, wk, wq, wg, w1, w1, w1, 2, 2, 1, dws)
+    assert y.shape == (0, 256)
+    q = torch.empty((0, 2, 128), dtype=torch.bfloat16, device=DEV)
+    kv = torch.empty((0, 1, 128), dtype=torch.bfloat16, device=DEV)
+    out = moe.moe_attention_gqa(q, kv, kv, torch.zeros(256, dtype=torch.uint8, device=DEV))
+    assert out.shape == (0, 2, 128)
+    assert moe.moe_check_device_error(ws) == 0

@@ -70,3 +70,39 @@ def test_forward_and_backward_replay_in_a_graph(moe, T):
         a, b = outs[key], ge[key]
         assert torch.equal(a.view(torch.int16) if a.dtype == torch.bfloat16 else a,
                            b.view(torch.int16) if b.dtype == torch.bfloat16 else b), key
+
+
+def test_decoder_layer_replays_in_a_graph(moe):
+    """moe_decoder_layer_forward is stream-ordered with no host synchronisation: a captured
+    call replays on new inputs bit for bit like an eager call."""
+    T, hq, hkv, f, n, k = 384, 4, 2, 256, 8, 2
+    d = hq * 128
+    rng = np.random.default_rng(31)
+    t = lambda shape, s: (torch.from_numpy((rng.standard_normal(shape) * s).astype(np.float32))
+                          .to(torch.bfloat16).to(DEV))
+    wq, wk, wv = t((hq * 128, d), d ** -0.5), t((hkv * 128, d), d ** -0.5), t((hkv * 128, d), d ** -0.5)
+    wo, wg = t((d, hq * 128), (hq * 128) ** -0.5), t((d, n), 0.02)
+    w1, w3, w2 = t((n, f, d), d ** -0.5), t((n, f, d), d ** -0.5), t((n, d, f), f ** -0.5)
+    ws = moe.decoder_workspace(T, d, f, n, k, hq, hkv, DEV)
+    h_static = t((T, d), 1.0)
+    y_static = torch.empty_like(h_static)
+
+    def body():
+        moe.moe_decoder_layer_forward(h_static, wq, wk, wv, wo, wg, w1, w3, w2, k, hq, hkv, ws,
+                                      seq_len=200, y=y_static)
+
+    body()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        body()
+    h_new = t((T, d), 1.0)
+    h_static.copy_(h_new)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert moe.moe_check_device_error(ws) == 0
+    y_eager = moe.moe_decoder_layer_forward(h_new, wq, wk, wv, wo, wg, w1, w3, w2, k, hq, hkv,
+                                            moe.decoder_workspace(T, d, f, n, k, hq, hkv, DEV),
+                                            seq_len=200)
+    torch.cuda.synchronize()
+    assert torch.equal(y_static.view(torch.int16), y_eager.view(torch.int16))

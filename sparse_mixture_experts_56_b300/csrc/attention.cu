@@ -5,29 +5,28 @@
 // query i of a sequence:
 //     o_i = sum_{j <= i} softmax_j(q_i · k_j / sqrt(128)) v_j
 //
-// One CTA per (sequence, query head, pair of 128-query tiles), 576 threads, warp-specialised:
-//   warp 0      allocates / frees the 512 TMEM columns (S/P_0, S/P_1, O_0, O_1, 128 each);
-//               its lane 0 is the TMA producer: both Q tiles once, then K and V tiles of 128
-//               keys into two-stage rings (K-major K tile; V as MN-major B operand), shared by
-//               the tiles.  K and V stages are freed separately (K once the last score product
-//               on it finished, V once the last P V did), so the next K tile is on its way a
-//               block ahead of the score product that needs it.
-//   warp 1      MMA issuer: per tile t, S_t = Q_t Kᵀ into TMEM, then O_t += P_t V with P_t
-//               read from TMEM (it overwrites S_t) and V MN-major.  The issue order
-//               S_0 S_1 | PV_0 S_0' | PV_1 S_1' | ... lets one tile's softmax run while the
-//               tensor cores work on the other tile.
-//   warps 2-9, 10-17   softmax of tile 0 / tile 1, two threads per query row (warps 2-5 take
-//               the first 64 keys of a block, warps 6-9 the last 64, and so on; a warp reaches
-//               the TMEM lanes 32 (w mod 4) .. +31, so any four consecutive warps cover the
-//               128 rows): the scores from TMEM into registers, causal / sequence mask on the
+// One CTA per (sequence, query head, 128-query tile), heaviest tiles first, 320 threads,
+// warp-specialised:
+//   warp 0      allocates / frees the TMEM columns (two score buffers S_a, S_b and O, 128
+//               each); its lane 0 is the TMA producer: the Q tile once, then K and V tiles of
+//               128 keys into two-stage rings (K-major K tile; V as MN-major B operand), K and
+//               V stages freed separately.
+//   warp 1      MMA issuer.  The scores of key block j go to buffer j mod 2, so the scores of
+//               block j + 1 are computed while the softmax works on block j: the issue order is
+//               S(0) S(1) | PV(0) S(2) | PV(1) S(3) | ..., with P(j) read from TMEM (it
+//               overwrites S(j) in its buffer) and V MN-major.  The softmax therefore never
+//               waits for a score product that depends on its own previous P.
+//   warps 2-9   softmax, two threads per query row (warps 2-5 take the first 64 keys of a
+//               block, warps 6-9 the last 64; a warp reaches the TMEM lanes 32 (w mod 4) ..
+//               +31): the scores from TMEM into registers, causal / sequence mask on the
 //               diagonal block only, the row maximum combined through shared memory, online
 //               softmax with lazy rescaling of O in TMEM (the exponent offset moves only when
-//               a block's maximum passes it by 2^8), P written as bf16 into TMEM; finally
-//               O / l stored as bf16.  The exchange of the row maximum also orders the second
-//               half's P stores after the first half's score loads (P overwrites S columns
-//               0-63).
-// The MMAs of one thread run in issue order, so the completion of S_t(j) also tells the
-// softmax that P_t V(j-1) has finished reading P_t and writing O_t.
+//               a block's maximum passes it by 2^8; O is rescaled after the P V product of the
+//               previous block has finished), P written as bf16 into TMEM; finally O / l
+//               stored as bf16.  The exchange of the row maximum also orders the second half's
+//               P stores after the first half's score loads (P overwrites S columns 0-63).
+// MMAs of one thread run in issue order: S(j + 2) is issued after P V(j), so the completion
+// of S(j) tells the softmax that P V(j - 2) has finished reading buffer j mod 2.
 // Every wait is bounded (globaltimer) as in the expert GEMMs; a timeout sets the status bit,
 // every role stops, the MMAs in flight are drained and TMEM is freed.
 #include "moe_internal.cuh"
@@ -43,10 +42,10 @@ constexpr int kBlk = 128;                        // queries per tile = keys per 
 constexpr uint32_t kTile = 128 * 128 * 2;        // one 128 x 128 bf16 tile (32 KB)
 constexpr uint32_t kHalf = kTile / 2;            // a 128 x 64 (or 64 x 128) half tile
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0, kColO = 256;       // S/P of tile t at 128 t, O of tile t at 256 + 128 t
+constexpr uint32_t kColS = 0, kColO = 256;       // S/P of block j at 128 (j mod 2), O at 256
 constexpr uint64_t kAttnDrainNs = 200ull * 1000 * 1000;
 constexpr float kRescaleLog2 = 8.0f;
-constexpr int kThreads = 576;   // 2 control warps + 2 tiles x 8 softmax warps
+constexpr int kThreads = 320;   // 2 control warps + 8 softmax warps
 
 // kind::f16, bf16 inputs, fp32 accumulation, M = N = 128; P V takes V MN-major (bit 16)
 constexpr uint32_t kIdescQK =
@@ -54,7 +53,7 @@ constexpr uint32_t kIdescQK =
 constexpr uint32_t kIdescPV = kIdescQK | (1u << 16);
 
 struct AttnArgs {
-  int T, seq_len, nseq, nqb, npairs, hq, hkv;
+  int T, seq_len, nseq, nqb, hq, hkv;
   float scale_log2;      // log2(e) / sqrt(dh)
   bf16* out;             // [T, hq, dh]
   uint32_t* status;
@@ -64,18 +63,18 @@ struct AttnArgs {
 struct AttnShared {
   uint64_t q_full;
   uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
-  uint64_t s_full[2], p_full[2], o_done[2];
+  uint64_t s_full[2], p_full[2], o_done;
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
   // the two threads of a query row (one per column half) exchange partial maxima and sums:
-  // [tile][half][row] values and the sequence number of the exchange they belong to
-  float xval[2][2][128];
-  int xseq[2][2][128];
+  // [half][row] values and the sequence number of the exchange they belong to
+  float xval[2][128];
+  int xseq[2][128];
 };
 
-// shared memory: Q_0 | Q_1 | K0 | V0 | K1 | V1 | AttnShared, 1024-byte aligned tiles
-constexpr size_t kAttnSmem = 1024 + 6 * (size_t)kTile + sizeof(AttnShared);
+// shared memory: Q | K0 | V0 | K1 | V1 | AttnShared, 1024-byte aligned tiles
+constexpr size_t kAttnSmem = 1024 + 5 * (size_t)kTile + sizeof(AttnShared);
 
 __device__ __forceinline__ void umma_ss(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
                                         uint32_t idesc, uint32_t accumulate) {
@@ -196,31 +195,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  const uint32_t sQ[2] = {smem_u32(smem), smem_u32(smem) + kTile};
-  const uint32_t sK[2] = {sQ[0] + 2 * kTile, sQ[0] + 4 * kTile};
-  const uint32_t sV[2] = {sQ[0] + 3 * kTile, sQ[0] + 5 * kTile};
-  AttnShared& sh = *reinterpret_cast<AttnShared*>(smem + 6 * kTile);
+  const uint32_t sQ = smem_u32(smem);
+  const uint32_t sK[2] = {sQ + kTile, sQ + 3 * kTile};
+  const uint32_t sV[2] = {sQ + 2 * kTile, sQ + 4 * kTile};
+  AttnShared& sh = *reinterpret_cast<AttnShared*>(smem + 5 * kTile);
   volatile int* abort = &sh.abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // work unit: query tiles 2p and 2p + 1 (the second may lie past the sequence), heavy first
-  const int per_seq = args.npairs * args.hq;
-  const int seq = blockIdx.x / per_seq;
-  const int rem = blockIdx.x - seq * per_seq;
-  const int h = rem / args.npairs;
-  const int pr = args.npairs - 1 - (rem - h * args.npairs);
+  // work unit: one query tile; units of the same tile index (equal work) for every sequence
+  // and head are adjacent, the heaviest tile index first
+  const int per_qb = args.nseq * args.hq;
+  const int qb = args.nqb - 1 - (int)(blockIdx.x / per_qb);
+  const int rem = (int)(blockIdx.x % per_qb);
+  const int seq = rem / args.hq;
+  const int h = rem - seq * args.hq;
   const int g = h / (args.hq / args.hkv);
   const int s0 = seq * args.seq_len;                           // first token of the sequence
   const int n = min(args.seq_len, args.T - s0);                // tokens of the sequence
-  const int qbt[2] = {2 * pr, 2 * pr + 1};
-  const int ntiles = qbt[1] < args.nqb ? 2 : 1;
-  const int nkvt[2] = {qbt[0] + 1, ntiles == 2 ? qbt[1] + 1 : 0};   // causal key blocks
-  const int nkv = ntiles == 2 ? nkvt[1] : nkvt[0];
+  const int nkv = qb + 1;                                      // causal key blocks
   const uint64_t limit = args.wait_ns;
 
   if (threadIdx.x == 0) {
     sh.abort = 0;
-    for (int i = 0; i < 2 * 2 * 128; ++i) (&sh.xseq[0][0][0])[i] = 0;
+    for (int i = 0; i < 2 * 128; ++i) (&sh.xseq[0][0])[i] = 0;
     mbar_init(smem_u32(&sh.q_full), 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&sh.k_full[s]), 1);
@@ -229,8 +226,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&sh.v_empty[s]), 1);
       mbar_init(smem_u32(&sh.s_full[s]), 1);
       mbar_init(smem_u32(&sh.p_full[s]), 8);
-      mbar_init(smem_u32(&sh.o_done[s]), 1);
     }
+    mbar_init(smem_u32(&sh.o_done), 1);
     mbar_init(smem_u32(&sh.drain), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -253,29 +250,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_map(&tmK);
     prefetch_map(&tmV);
     const uint32_t qf = smem_u32(&sh.q_full);
-    mbar_expect_tx(qf, (uint32_t)ntiles * kTile);
-    for (int t = 0; t < ntiles; ++t) {
-      tma_load_2d(sQ[t], &tmQ, qf, h * kDh, s0 + qbt[t] * kBlk);
-      tma_load_2d(sQ[t] + kHalf, &tmQ, qf, h * kDh + 64, s0 + qbt[t] * kBlk);
-    }
+    mbar_expect_tx(qf, kTile);
+    tma_load_2d(sQ, &tmQ, qf, h * kDh, s0 + qb * kBlk);
+    tma_load_2d(sQ + kHalf, &tmQ, qf, h * kDh + 64, s0 + qb * kBlk);
     // bit b of issued / iphase: barrier b (K stage 0, K stage 1, V stage 0, V stage 1) has a
-    // load in flight / the phase of its last load
+    // load in flight / the phase of its last load.  K runs one block ahead of V: the scores
+    // of block j + 2 are issued right after P V(j), so K(j + 2) is loaded before the wait
+    // for the V stage that P V(j - 2) frees.
     uint32_t issued = 0, iphase = 0;
-    for (int j = 0; j < nkv; ++j) {
+    // K tile of block j: 128 keys x 128 dims as two K-major halves
+    auto load_k = [&](int j) -> bool {
       const int st = j & 1;
       const uint32_t ph = (uint32_t)(j >> 1) & 1u;
-      const int row = s0 + j * kBlk;
-      // K: 128 keys x 128 dims as two K-major halves
       if (!wait_fast(smem_u32(&sh.k_empty[st]), ph ^ 1u, abort, limit)) {
         raise_abort(abort, args.status);
-        break;
+        return false;
       }
       const uint32_t kb_bar = smem_u32(&sh.k_full[st]);
       mbar_expect_tx(kb_bar, kTile);
-      tma_load_2d(sK[st], &tmK, kb_bar, g * kDh, row);
-      tma_load_2d(sK[st] + kHalf, &tmK, kb_bar, g * kDh + 64, row);
+      tma_load_2d(sK[st], &tmK, kb_bar, g * kDh, s0 + j * kBlk);
+      tma_load_2d(sK[st] + kHalf, &tmK, kb_bar, g * kDh + 64, s0 + j * kBlk);
       issued |= 1u << st;
       iphase = (iphase & ~(1u << st)) | (ph << st);
+      return true;
+    };
+    bool go = load_k(0);
+    for (int j = 0; go && j < nkv; ++j) {
+      const int st = j & 1;
+      const uint32_t ph = (uint32_t)(j >> 1) & 1u;
+      if (j + 1 < nkv && !load_k(j + 1)) break;
       // V: [key half kb][dim half nc] boxes of 64 keys x 64 dims (MN-major B operand)
       if (!wait_fast(smem_u32(&sh.v_empty[st]), ph ^ 1u, abort, limit)) {
         raise_abort(abort, args.status);
@@ -286,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int kb = 0; kb < 2; ++kb)
         for (int nc = 0; nc < 2; ++nc)
           tma_load_2d(sV[st] + kb * kHalf + nc * (kHalf / 2), &tmV, vb_bar, g * kDh + 64 * nc,
-                      row + 64 * kb);
+                      s0 + j * kBlk + 64 * kb);
       issued |= 4u << st;
       iphase = (iphase & ~(4u << st)) | (ph << (st + 2));
     }
@@ -302,97 +305,81 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = wait_fast(smem_u32(&sh.q_full), 0, abort, limit);
     bool any = false;
     if (!ok) raise_abort(abort, args.status);
-    int k_seen = -1, v_seen = -1;   // last block whose K / V tile is known to have landed
-    // operand descriptors built once; every tile, stage and K slice is a constant offset
-    const uint64_t dQ = sw128_desc(sQ[0]);          // Q_0 | Q_1 | K0 | V0 | K1 | V1
-    const uint64_t dV = sw128_mn_desc(sQ[0]);
-    // S_t(j) = Q_t K_jᵀ (the K stage of block j must have landed); the last tile's product
-    // frees the K stage
-    auto issue_s = [&](int t, int j) -> bool {
+    // operand descriptors built once; every buffer, stage and K slice is a constant offset
+    const uint64_t dQ = sw128_desc(sQ);             // Q | K0 | V0 | K1 | V1
+    const uint64_t dV = sw128_mn_desc(sQ);
+    // S(j) = Q K_jᵀ into score buffer j mod 2 (the K stage of block j must have landed); the
+    // product frees the K stage
+    auto issue_s = [&](int j) -> bool {
       const int st = j & 1;
-      if (j > k_seen) {
-        if (!wait_fast(smem_u32(&sh.k_full[st]), (uint32_t)(j >> 1) & 1u, abort, limit)) {
-          raise_abort(abort, args.status);
-          return false;
-        }
-        k_seen = j;
+      if (!wait_fast(smem_u32(&sh.k_full[st]), (uint32_t)(j >> 1) & 1u, abort, limit)) {
+        raise_abort(abort, args.status);
+        return false;
       }
       tc_fence_after();
-      const uint64_t dq = desc_add(dQ, (uint32_t)t * kTile);
-      const uint64_t dk = desc_add(dQ, (uint32_t)(2 + 2 * st) * kTile);
-      const uint32_t d_s = tmem + kColS + (uint32_t)t * 128;
+      const uint64_t dk = desc_add(dQ, (uint32_t)(1 + 2 * st) * kTile);
+      const uint32_t d_s = tmem + kColS + (uint32_t)st * 128;
 #pragma unroll
       for (int kk = 0; kk < kDh / 16; ++kk) {
         const uint32_t off = (uint32_t)(kk >> 2) * kHalf + (uint32_t)(kk & 3) * 32;
-        umma_ss(d_s, desc_add(dq, off), desc_add(dk, off), kIdescQK, kk > 0 ? 1u : 0u);
+        umma_ss(d_s, desc_add(dQ, off), desc_add(dk, off), kIdescQK, kk > 0 ? 1u : 0u);
       }
-      umma_commit(smem_u32(&sh.s_full[t]));
-      if (t == ntiles - 1) umma_commit(smem_u32(&sh.k_empty[st]));
+      umma_commit(smem_u32(&sh.s_full[st]));
+      umma_commit(smem_u32(&sh.k_empty[st]));
       any = true;
       return true;
     };
-    for (int t = 0; ok && t < ntiles; ++t) ok = issue_s(t, 0);
+    for (int j = 0; ok && j < 2 && j < nkv; ++j) ok = issue_s(j);
     for (int j = 0; ok && j < nkv; ++j) {
       const int st = j & 1;
-      for (int t = 0; ok && t < ntiles; ++t) {
-        if (j >= nkvt[t]) continue;
-        // O_t += P_t V_j once the softmax has written P_t(j) into TMEM (and rescaled O_t) and
-        // the V tile of block j has landed
-        if (!wait_fast(smem_u32(&sh.p_full[t]), (uint32_t)j & 1u, abort, limit)) {
-          raise_abort(abort, args.status);
-          ok = false;
-          break;
-        }
-        if (j > v_seen) {
-          if (!wait_fast(smem_u32(&sh.v_full[st]), (uint32_t)(j >> 1) & 1u, abort, limit)) {
-            raise_abort(abort, args.status);
-            ok = false;
-            break;
-          }
-          v_seen = j;
-        }
-        tc_fence_after();
-        const uint64_t dv = desc_add(dV, (uint32_t)(3 + 2 * st) * kTile);
-        const uint32_t d_o = tmem + kColO + (uint32_t)t * 128;
-        const uint32_t a_p = tmem + kColS + (uint32_t)t * 128;
-#pragma unroll
-        for (int kk = 0; kk < kBlk / 16; ++kk) {
-          const uint32_t boff = (uint32_t)(kk >> 2) * kHalf + (uint32_t)(kk & 3) * 2048;
-          umma_ts(d_o, a_p + kk * 8, desc_add(dv, boff), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
-        }
-        umma_commit(smem_u32(&sh.o_done[t]));
-        if (t == ntiles - 1) umma_commit(smem_u32(&sh.v_empty[st]));
-        // the next scores of this tile (after P_t V_j in issue order)
-        if (j + 1 < nkvt[t] && !issue_s(t, j + 1)) {
-          ok = false;
-          break;
-        }
+      // O += P(j) V_j once the softmax has written P(j) into buffer j mod 2 (and rescaled O)
+      // and the V tile of block j has landed
+      if (!wait_fast(smem_u32(&sh.p_full[st]), (uint32_t)(j >> 1) & 1u, abort, limit) ||
+          !wait_fast(smem_u32(&sh.v_full[st]), (uint32_t)(j >> 1) & 1u, abort, limit)) {
+        raise_abort(abort, args.status);
+        ok = false;
+        break;
       }
-      if (!ok) break;
+      tc_fence_after();
+      const uint64_t dv = desc_add(dV, (uint32_t)(2 + 2 * st) * kTile);
+      const uint32_t d_o = tmem + kColO;
+      const uint32_t a_p = tmem + kColS + (uint32_t)st * 128;
+#pragma unroll
+      for (int kk = 0; kk < kBlk / 16; ++kk) {
+        const uint32_t boff = (uint32_t)(kk >> 2) * kHalf + (uint32_t)(kk & 3) * 2048;
+        umma_ts(d_o, a_p + kk * 8, desc_add(dv, boff), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+      }
+      umma_commit(smem_u32(&sh.o_done));
+      umma_commit(smem_u32(&sh.v_empty[st]));
+      // the scores two blocks ahead go to the buffer P(j) came from (after P V(j) in issue
+      // order)
+      if (j + 2 < nkv && !issue_s(j + 2)) {
+        ok = false;
+        break;
+      }
     }
     if (any) {
       umma_commit(smem_u32(&sh.drain));
       if (!drain_phase(smem_u32(&sh.drain), 0, kAttnDrainNs)) atomicOr(args.status, kDevErrTimeout);
     }
   } else if (warp >= 2) {
-    // ---------------------------------------------------------------- softmax of tile t
-    const int t = (warp - 2) >> 3;
-    const int hh = ((warp - 2) >> 2) & 1;            // column half: keys 64 hh .. 64 hh + 63
+    // ---------------------------------------------------------------- softmax
+    const int hh = (warp - 2) >> 2;                  // column half: keys 64 hh .. 64 hh + 63
     const int q = warp & 3;                          // TMEM lane quarter of this warp
     const int r = q * 32 + lane;                     // query row of the tile (TMEM lane)
-    const int qb = qbt[t];
     const int qi = qb * kBlk + r;                    // query index within the sequence
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-    const uint32_t tS = tmem + lane_base + kColS + (uint32_t)t * 128;
-    const uint32_t tO = tmem + lane_base + kColO + (uint32_t)t * 128;
+    const uint32_t tO = tmem + lane_base + kColO;
     float m = -1e30f, l = 0.f;
-    bool ok = t < ntiles;
-    float* xval = &sh.xval[t][0][0];
-    volatile int* xseq = &sh.xseq[t][0][0];
+    bool ok = true;
+    float* xval = &sh.xval[0][0];
+    volatile int* xseq = &sh.xseq[0][0];
     const int xm = hh * 128 + r, xo = (hh ^ 1) * 128 + r;   // this thread's / the partner's slot
     int seq = 0;
-    for (int j = 0; ok && j < nkvt[t]; ++j) {
-      if (!warp_wait(smem_u32(&sh.s_full[t]), (uint32_t)j & 1u, abort, limit, args.status,
+    for (int j = 0; ok && j < nkv; ++j) {
+      const int st = j & 1;
+      const uint32_t tS = tmem + lane_base + kColS + (uint32_t)st * 128;
+      if (!warp_wait(smem_u32(&sh.s_full[st]), (uint32_t)(j >> 1) & 1u, abort, limit, args.status,
                      lane)) {
         ok = false;
         break;
@@ -441,8 +428,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         corr = fast_exp2(m - m_new);
         m = m_new;
         if (j > 0) {
-          // P_t V(j-1) finished before S_t(j) (issue order): O_t may be rescaled (this
-          // half's 64 columns, 8 at a time: the scores stay in registers meanwhile)
+          // O may be rescaled once P V(j - 1) has finished accumulating into it (this half's
+          // 64 columns, 8 at a time: the scores stay in registers meanwhile)
+          if (!warp_wait(smem_u32(&sh.o_done), (uint32_t)(j - 1) & 1u, abort, limit, args.status,
+                         lane)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
 #pragma unroll 1
           for (int c = 8 * hh; c < 8 * hh + 8; ++c) {
             uint32_t u[8];
@@ -455,8 +448,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      // P = exp2(score - offset) as bf16 over the first 64 columns of S_t (columns 16c ..
-      // 16c+15 hold keys 32c .. 32c+31; this half writes chunks 2 hh and 2 hh + 1)
+      // P = exp2(score - offset) as bf16 over the first 64 columns of the buffer (columns
+      // 16c .. 16c+15 hold keys 32c .. 32c+31; this half writes chunks 2 hh and 2 hh + 1)
       const uint64_t c2 = pair2(args.scale_log2, args.scale_log2), n2 = pair2(-m, -m);
       uint64_t sp[2] = {0, 0};
 #pragma unroll
@@ -482,7 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sh.p_full[t]));
+      if (lane == 0) mbar_arrive(smem_u32(&sh.p_full[st]));
     }
     // the row sum over both halves
     if (ok) {
@@ -490,8 +483,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = row_exchange(xval, xseq, xm, xo, l, ++seq, lo, abort, limit, args.status);
       l += lo;
     }
-    if (ok && warp_wait(smem_u32(&sh.o_done[t]), (uint32_t)(nkvt[t] - 1) & 1u, abort, limit,
-                        args.status, lane)) {
+    if (ok && warp_wait(smem_u32(&sh.o_done), (uint32_t)(nkv - 1) & 1u, abort, limit, args.status,
+                        lane)) {
       tc_fence_after();
       const float inv = 1.0f / l;
       bf16* orow = args.out + ((size_t)(s0 + qi) * args.hq + h) * kDh;
@@ -555,14 +548,13 @@ cudaError_t launch_attention_gqa(const bf16* q, const bf16* k, const bf16* v, in
   a.seq_len = seq_len > 0 ? seq_len : T;
   a.nseq = (T + a.seq_len - 1) / a.seq_len;
   a.nqb = (a.seq_len + kBlk - 1) / kBlk;
-  a.npairs = (a.nqb + 1) / 2;
   a.hq = hq;
   a.hkv = hkv;
   a.scale_log2 = 1.4426950408889634f / sqrtf((float)kDh);
   a.out = out;
   a.status = status;
   a.wait_ns = wait_ns;
-  const long long ctas = (long long)a.nseq * hq * a.npairs;
+  const long long ctas = (long long)a.nseq * hq * a.nqb;
   attention_gqa_kernel<<<(unsigned)ctas, kThreads, kAttnSmem, s>>>(mQ, mK, mV, a);
   return cudaGetLastError();
 }

@@ -68,9 +68,10 @@ struct AttnShared {
   uint32_t tmem_base;
   int abort;
   // the two threads of a query row (one per column half) exchange partial maxima and sums:
-  // [half][row] values and the sequence number of the exchange they belong to
-  float xval[2][128];
-  int xseq[2][128];
+  // [slot][half][row] values and the number of the exchange they belong to (slot = parity of
+  // the exchange)
+  float xval[2][2][128];
+  int xseq[2][2][128];
 };
 
 // shared memory: Q | K0 | V0 | K1 | V1 | AttnShared, 1024-byte aligned tiles
@@ -147,20 +148,25 @@ __device__ __forceinline__ void add2(uint64_t& acc, float x0, float x1) {
       : "f"(x0), "f"(x1));
 }
 
-// The two threads of a query row swap a value: publish (v, seq), then wait (bounded) for the
-// partner's entry of the same exchange.  A warp goes on only if every lane got its value.
+// The two threads of a query row swap a value: publish (v, seq) in the slot of seq's parity,
+// then wait (bounded) for the partner's entry of the same exchange in that slot.  A thread
+// that runs ahead to exchange seq + 1 writes the other slot, and it cannot reach seq + 2
+// before its partner has published seq + 1, which the partner does only after reading
+// exchange seq -- so neither the value nor the sequence number the partner waits for is
+// overwritten early.  A warp goes on only if every lane got its value.
 __device__ __forceinline__ bool row_exchange(float* xval, volatile int* xseq, int mine,
                                              int other, float v, int seq, float& got,
                                              volatile int* abort, uint64_t limit,
                                              uint32_t* status) {
-  xval[mine] = v;
+  const int so = (seq & 1) << 8;   // slot offset: [slot][half][row]
+  xval[so + mine] = v;
   tc_fence_before();
   __threadfence_block();
-  xseq[mine] = seq;
+  xseq[so + mine] = seq;
   bool ok = true;
-  if (xseq[other] != seq) {
+  if (xseq[so + other] != seq) {
     const uint64_t t0 = gtimer();
-    while (xseq[other] != seq) {
+    while (xseq[so + other] != seq) {
       if (*abort || gtimer() - t0 > limit) {
         ok = false;
         break;
@@ -169,7 +175,7 @@ __device__ __forceinline__ bool row_exchange(float* xval, volatile int* xseq, in
   }
   __threadfence_block();
   tc_fence_after();
-  got = reinterpret_cast<volatile float*>(xval)[other];
+  got = reinterpret_cast<volatile float*>(xval)[so + other];
   if (!__all_sync(0xffffffffu, ok)) {
     if (!ok) raise_abort(abort, status);
     return false;
@@ -215,9 +221,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nkv = qb + 1;                                      // causal key blocks
   const uint64_t limit = args.wait_ns;
 
+  for (int i = threadIdx.x; i < 2 * 2 * 128; i += blockDim.x) (&sh.xseq[0][0][0])[i] = 0;
   if (threadIdx.x == 0) {
     sh.abort = 0;
-    for (int i = 0; i < 2 * 128; ++i) (&sh.xseq[0][0])[i] = 0;
     mbar_init(smem_u32(&sh.q_full), 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&sh.k_full[s]), 1);
@@ -372,8 +378,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tO = tmem + lane_base + kColO;
     float m = -1e30f, l = 0.f;
     bool ok = true;
-    float* xval = &sh.xval[0][0];
-    volatile int* xseq = &sh.xseq[0][0];
+    float* xval = &sh.xval[0][0][0];
+    volatile int* xseq = &sh.xseq[0][0][0];
     const int xm = hh * 128 + r, xo = (hh ^ 1) * 128 + r;   // this thread's / the partner's slot
     int seq = 0;
     for (int j = 0; ok && j < nkv; ++j) {

@@ -381,9 +381,12 @@ void moe_set_wait_limit_ns(unsigned long long ns);
  *                       over two SMs) for the down-projection (w2) when the experts average
  *                       at least 256 rows (T*k >= 256*n) and for the up-projection (w1|w3
  *                       with SwiGLU) when they average at least 512 (T*k >= 512*n); the
- *                       single-CTA form (128-row tiles) otherwise
+ *                       single-CTA form (128-row tiles) otherwise.  In the backward the
+ *                       weight-gradient GEMMs (dW1, dW3, dW2: 256-row tiles of dW) always
+ *                       take the pair form and the other backward GEMMs the single form.
  *   MOE_TC_FORM_SINGLE  always the single-CTA form
- *   MOE_TC_FORM_PAIR    always the CTA-pair form (where the device can co-schedule pairs)
+ *   MOE_TC_FORM_PAIR    always the CTA-pair form for the forward GEMMs and the weight
+ *                       gradients (where the device can co-schedule pairs)
  * Both forms compute the same results up to the fp32 accumulation order inside a tile
  * (which is the same: both accumulate K in ascending order), so outputs are identical.
  * Returns MOE_ERR_INVALID_ARG for any other value.

@@ -375,7 +375,8 @@ __global__ void __launch_bounds__(256, 1)
                            const __grid_constant__ CUtensorMap tmOut, const TcArgs args) {
   using C = Cfg<PAIR>;
   constexpr int STAGES = C::kStages;
-  static_assert(!PAIR || MODE == kSwiGLU || MODE == kDown, "the pair form serves the forward");
+  static_assert(!PAIR || MODE == kSwiGLU || MODE == kDown || MODE == kWgrad,
+                "the pair form serves the forward GEMMs and the weight gradients");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -475,8 +476,20 @@ __global__ void __launch_bounds__(256, 1)
           // both CTAs' bytes land on the even CTA's barrier, which the MMA issuer waits on
           if (rank == 0) mbar_expect_tx(fb, 2 * C::kStageBytes);
           const uint32_t fb0 = peer_addr(fb, 0);
-          tma_load_2d_pair(a_dst, &tmA, fb0, kb * BK, arow);
-          tma_load_2d_pair(b_dst, bmap, fb0, kb * BK, brow);
+          if constexpr (MODE == kWgrad) {
+            // both operands MN-major: this CTA's 128 M columns of P and 128 N columns of Q,
+            // as 64-column chunks of 64 K-rows
+            const int m0 = t.mt * C::kTileM + (int)rank * BM;
+            const int n0 = t.nt * BN + (int)rank * C::kBRows;
+            const int krow = t.row0 + kb * BK;
+            tma_load_2d_pair(a_dst, &tmA, fb0, m0, krow);
+            tma_load_2d_pair(a_dst + kMnChunkBytes, &tmA, fb0, m0 + 64, krow);
+            tma_load_2d_pair(b_dst, &tmB0, fb0, n0, krow);
+            tma_load_2d_pair(b_dst + kMnChunkBytes, &tmB0, fb0, n0 + 64, krow);
+          } else {
+            tma_load_2d_pair(a_dst, &tmA, fb0, kb * BK, arow);
+            tma_load_2d_pair(b_dst, bmap, fb0, kb * BK, brow);
+          }
         } else {
           mbar_expect_tx(fb, C::kStageBytes);
           // A: 128 rows x 64 K (K-major), or for kWgrad 64 K-rows x 2 chunks of 64 M columns
@@ -606,7 +619,9 @@ __global__ void __launch_bounds__(256, 1)
       if (!epilogue_all(ok)) break;
       tc_fence_after();
       const int row = (int)rank * BM + r;   // row of the tile held in this TMEM lane
-      const bool row_ok = MODE == kWgrad ? t.mt * BM + r < args.mdim : row < t.rows;
+      // kWgrad: row of the weight gradient held in this TMEM lane
+      const int wrow = t.mt * C::kTileM + (int)rank * BM + r;
+      const bool row_ok = MODE == kWgrad ? wrow < args.mdim : row < t.rows;
       const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
       const uint32_t tempty_local = smem_u32(&sh.tempty[acc]);
       // the even CTA's MMA issuer waits for the epilogue warps of both CTAs
@@ -763,11 +778,11 @@ __global__ void __launch_bounds__(256, 1)
         }
         if (row_ok) args.dwp[grow * args.ntiles + t.nt] = dot;
       } else {
-        // kDown, kDgradX: rows of the tile; kWgrad: rows t.mt*128.. of expert e's gradient
+        // kDown, kDgradX: rows of the tile; kWgrad: rows of expert e's gradient
         const int col0 = t.nt * BN;
         bf16* orow;
         if constexpr (MODE == kWgrad)
-          orow = args.out + ((size_t)t.e * args.mdim + (size_t)(t.mt * BM + r)) * args.ndim + col0;
+          orow = args.out + ((size_t)t.e * args.mdim + (size_t)wrow) * args.ndim + col0;
         else
           orow = args.out + (size_t)(t.row0 + row) * args.ndim + col0;
         const bool empty_k = MODE == kWgrad && t.rows == 0;
@@ -872,6 +887,7 @@ inline bool want_pair(int A, int n) {
   if (form == MOE_TC_FORM_PAIR) return true;
   if (MODE == kDown) return (long long)A >= 256ll * n;
   if (MODE == kSwiGLU) return (long long)A >= 512ll * n;
+  if (MODE == kWgrad) return true;   // M and N are weight dimensions: no row is wasted
   return false;
 }
 
@@ -889,26 +905,34 @@ cudaError_t launch_single(const CUtensorMap& mA, const CUtensorMap& mA2, const C
   return cudaGetLastError();
 }
 
+// CTA-pair launch over at most `tiles` tiles on at most `pairs` resident clusters of two.
+template <int MODE>
+cudaError_t launch_pair(const CUtensorMap& mA, const CUtensorMap& mA2, const CUtensorMap& mB0,
+                        const CUtensorMap& mB1, const CUtensorMap& mOut, const TcArgs& a,
+                        long long tiles, int pairs, cudaStream_t s) {
+  const int units = (int)(tiles < pairs ? (tiles > 0 ? tiles : 1) : pairs);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(2 * units, 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.dynamicSmemBytes = smem_bytes<true>();
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, grouped_gemm_tc_kernel<MODE, true>, mA, mA2, mB0, mB1, mOut, a);
+}
+
 template <int MODE>
 cudaError_t launch_gemm(const CUtensorMap& mA, const CUtensorMap& mB0, const CUtensorMap& mB1,
                         const CUtensorMap& mOut, const TcArgs& a, int A, cudaStream_t s) {
   const int pairs = want_pair<MODE>(A, a.n) ? max_pairs<MODE>() : 0;
   if (pairs > 0) {
     const long long tiles = ((long long)(A + 255) / 256 + a.n) * a.ntiles;
-    const int units = (int)(tiles < pairs ? tiles : pairs);
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.gridDim = dim3(2 * units, 1, 1);
-    cfg.blockDim = dim3(256, 1, 1);
-    cfg.dynamicSmemBytes = smem_bytes<true>();
-    cfg.stream = s;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, grouped_gemm_tc_kernel<MODE, true>, mA, mA, mB0, mB1, mOut, a);
+    return launch_pair<MODE>(mA, mA, mB0, mB1, mOut, a, tiles, pairs, s);
   }
   const long long tiles = ((long long)(A + BM - 1) / BM + a.n) * a.ntiles;
   return launch_single<MODE>(mA, mA, mB0, mB1, mOut, a, tiles, s);
@@ -1065,12 +1089,18 @@ cudaError_t launch_bwd_wgrad(const bf16* P, const bf16* Q, const int32_t* poff, 
   a.n = n;
   a.kdim = 0;
   a.mdim = M;
-  a.mtiles_w = (M + BM - 1) / BM;
   a.ndim = N;
   a.ntiles = (N + BN - 1) / BN;
   a.out = dW;
   a.status = status;
   a.wait_ns = wait_ns;
+  const int pairs = want_pair<kWgrad>(rows_max, n) ? max_pairs<kWgrad>() : 0;
+  if (pairs > 0) {
+    a.mtiles_w = (M + 2 * BM - 1) / (2 * BM);
+    return launch_pair<kWgrad>(mP, mP, mQ, mQ, mP, a, (long long)n * a.mtiles_w * a.ntiles, pairs,
+                               s);
+  }
+  a.mtiles_w = (M + BM - 1) / BM;
   return launch_single<kWgrad>(mP, mP, mQ, mQ, mP, a, (long long)n * a.mtiles_w * a.ntiles, s);
 }
 

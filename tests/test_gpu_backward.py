@@ -99,6 +99,30 @@ def test_backward_is_deterministic(moe):
                            b[key].view(torch.uint8) if b[key].dtype != torch.float32 else b[key]), key
 
 
+@pytest.mark.parametrize("name", ["t300-d256-f384-skew", "t640-d384-f320-skew", "t5-empty-experts",
+                                  "n32-k2-t500", "t1100-d512-f768", "t1"])
+def test_weight_gradient_forms_agree(moe, name):
+    """The weight gradients from the CTA-pair form (256-row tiles of dW over two SMs, the
+    default) and from the single-CTA form are bit-identical: both reduce every dW element over
+    the expert's rows in the same 64-row blocks and 16-row MMA steps.  The shapes include
+    dW row counts (f = 384, 320, 768; d = 384) that end inside a 256-row tile, and experts
+    without rows (their dW is zero in both forms)."""
+    got = {}
+    for form in (moe.MOE_TC_FORM_SINGLE, moe.MOE_TC_FORM_AUTO):
+        moe.moe_set_tc_form(form)
+        try:
+            _, _, out, _ = _run(moe, name, 660 + sorted(CASES).index(name))
+        finally:
+            moe.moe_set_tc_form(moe.MOE_TC_FORM_AUTO)
+        got[form] = out
+    a, b = got[moe.MOE_TC_FORM_SINGLE], got[moe.MOE_TC_FORM_AUTO]
+    for key in a:
+        x1, x2 = a[key], b[key]
+        same = torch.equal(x1, x2) if x1.dtype == torch.float32 else \
+            torch.equal(x1.view(torch.int16), x2.view(torch.int16))
+        assert same, key
+
+
 def _f64(a, w):
     return workloads.as_f32(a, w).astype(np.float64)
 

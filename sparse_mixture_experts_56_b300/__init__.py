@@ -358,12 +358,17 @@ def moe_ep_regroup(recv_counts: torch.Tensor, R: int, *, local_offsets: Optional
     """recv_counts [G, E] int32 (device) -> (local_offsets [E+1], row_map [R], inv_row_map [R])."""
     G, E = recv_counts.shape
     dev = recv_counts.device
+    if recv_counts.dtype != torch.int32:
+        raise ValueError("recv_counts must be int32")
     if local_offsets is None:
         local_offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
     if row_map is None:
         row_map = torch.empty(R, dtype=torch.int32, device=dev)
     if inv_row_map is None:
         inv_row_map = torch.empty(R, dtype=torch.int32, device=dev)
+    for t, size in ((local_offsets, E + 1), (row_map, R), (inv_row_map, R)):
+        if t.dtype != torch.int32 or t.numel() < size:
+            raise ValueError("local_offsets, row_map and inv_row_map: int32 of E + 1, R and R")
     st = _native.lib().moe_ep_regroup(_ptr(recv_counts), G, E, R, _ptr(local_offsets),
                                       _ptr(row_map), _ptr(inv_row_map), _stream(stream))
     check("moe_ep_regroup", st)
@@ -374,11 +379,15 @@ def moe_gather_rows(src: torch.Tensor, index: torch.Tensor, k: int = 1, *,
                     dst: Optional[torch.Tensor] = None, stream=None):
     """dst[p] = src[index[p] // k] (zero rows for indices outside [0, rows(src) * k))."""
     rows = index.shape[0]
+    if index.dtype != torch.int32:
+        raise ValueError("index must be int32")
     if dst is None:
         dst = torch.empty((rows,) + tuple(src.shape[1:]), dtype=src.dtype, device=src.device)
     if rows == 0:
         return dst
     row_bytes = (dst.numel() // rows) * dst.element_size()
+    if dst.shape[0] != rows or (src.shape[0] and src[0].numel() * src.element_size() != row_bytes):
+        raise ValueError("src and dst rows must have the same size; dst one row per index")
     st = _native.lib().moe_gather_rows(_ptr(src), src.shape[0], _ptr(index), rows, k, row_bytes,
                                        _ptr(dst), _stream(stream))
     check("moe_gather_rows", st)

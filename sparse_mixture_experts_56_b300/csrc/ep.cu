@@ -17,21 +17,22 @@ constexpr int kMaxSources = 1024;
 
 // One block per (source s, local expert j): the block's rows sit at receive positions
 // src_base(s) + sum_{j' < j} c[s][j'] + i and at grouped positions
-// local_offsets[j] + sum_{s' < s} c[s'][j] + i, i < c[s][j].  Counts are clamped to >= 0 and
-// positions at or past R are never written.
+// local_offsets[j] + sum_{s' < s} c[s'][j] + i, i < c[s][j].  Counts are clamped to >= 0, the
+// sums taken in 64 bits, and positions outside [0, R) are never written.
 __global__ void __launch_bounds__(256) ep_regroup_kernel(const int32_t* __restrict__ counts,
                                                          int G, int E, int R,
                                                          int32_t* __restrict__ local_offsets,
                                                          int32_t* __restrict__ row_map,
                                                          int32_t* __restrict__ inv_row_map) {
   const int s = blockIdx.x / E, j = blockIdx.x % E;
-  __shared__ int s_recv0, s_group0, s_cnt;
+  __shared__ long long s_recv0, s_group0;
+  __shared__ int s_cnt;
   if (threadIdx.x == 0) {
-    auto c = [&](int ss, int jj) {
+    auto c = [&](int ss, int jj) -> long long {
       const int v = counts[ss * E + jj];
       return v > 0 ? v : 0;
     };
-    int recv0 = 0, group0 = 0;
+    long long recv0 = 0, group0 = 0;
     for (int ss = 0; ss < s; ++ss)
       for (int jj = 0; jj < E; ++jj) recv0 += c(ss, jj);
     for (int jj = 0; jj < j; ++jj) recv0 += c(s, jj);
@@ -40,23 +41,24 @@ __global__ void __launch_bounds__(256) ep_regroup_kernel(const int32_t* __restri
     for (int ss = 0; ss < s; ++ss) group0 += c(ss, j);
     s_recv0 = recv0;
     s_group0 = group0;
-    s_cnt = c(s, j);
+    s_cnt = (int)c(s, j);
     if (blockIdx.x == 0) {
-      int run = 0;
+      long long run = 0;
       for (int jj = 0; jj < E; ++jj) {
-        local_offsets[jj] = run < R ? run : R;
+        local_offsets[jj] = (int32_t)(run < R ? run : R);
         for (int ss = 0; ss < G; ++ss) run += c(ss, jj);
       }
-      local_offsets[E] = run < R ? run : R;
+      local_offsets[E] = (int32_t)(run < R ? run : R);
     }
   }
   __syncthreads();
-  const int recv0 = s_recv0, group0 = s_group0, cnt = s_cnt;
+  const long long recv0 = s_recv0, group0 = s_group0;
+  const int cnt = s_cnt;
   for (int i = threadIdx.x; i < cnt; i += blockDim.x) {
-    const int q = recv0 + i, p = group0 + i;
+    const long long q = recv0 + i, p = group0 + i;
     if (q < R && p < R) {
-      row_map[p] = q;
-      inv_row_map[q] = p;
+      row_map[p] = (int32_t)q;
+      inv_row_map[q] = (int32_t)p;
     }
   }
 }

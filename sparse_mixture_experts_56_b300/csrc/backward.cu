@@ -21,6 +21,7 @@ namespace {
 
 constexpr int kRowAlign = 128;
 constexpr int kDwgChunk = 128;   // tokens per partial sum of dW_g
+constexpr int kDwgBatch = 8;     // token rows of x in flight per thread (dW_g partial sums)
 
 __global__ void pad_offsets_kernel(const int32_t* __restrict__ off, int n,
                                    int32_t* __restrict__ poff) {
@@ -77,8 +78,9 @@ __global__ void __launch_bounds__(256) gather_bwd_kernel(
   }
 }
 
-// One warp per token.  dx[t] = sum_k dx_pad[q_k] + sum_k dl_k W_g[:, e_k]; dl [T, n] holds
-// the logit gradient (zero outside the kept experts) for the dW_g reduction.
+// One warp per token (bf16, d % 8 == 0, n != 8).  dx[t] = sum_k dx_pad[q_k] + sum_k dl_k
+// W_g[:, e_k]; dl [T, n] holds the logit gradient (zero outside the kept experts) for the dW_g
+// reduction.
 template <int KMAX>
 __global__ void __launch_bounds__(256) router_bwd_kernel(
     const int32_t* __restrict__ idx, const float* __restrict__ topk_w,
@@ -137,26 +139,9 @@ __global__ void __launch_bounds__(256) router_bwd_kernel(
             acc[2 * j] += f2.x;
             acc[2 * j + 1] += f2.y;
           }
-          if (n == 8) {
-            // row c0 + j of W_g is 8 bf16 = one 16-byte load holding every expert
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const uint4 wr = __ldg(reinterpret_cast<const uint4*>(wg + (size_t)(c0 + j) * 8));
-              const __nv_bfloat162* wp = reinterpret_cast<const __nv_bfloat162*>(&wr);
-              float wv = 0.f;
-#pragma unroll
-              for (int h = 0; h < 4; ++h) {
-                const float2 f2 = __bfloat1622float2(wp[h]);
-                if (es[s] == 2 * h) wv = f2.x;
-                if (es[s] == 2 * h + 1) wv = f2.y;
-              }
-              acc[j] = fmaf(dls[s], wv, acc[j]);
-            }
-          } else {
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-              acc[j] = fmaf(dls[s], __bfloat162float(wg[(size_t)(c0 + j) * n + es[s]]), acc[j]);
-          }
+          for (int j = 0; j < 8; ++j)
+            acc[j] = fmaf(dls[s], __bfloat162float(wg[(size_t)(c0 + j) * n + es[s]]), acc[j]);
         }
       }
       uint4 o;
@@ -165,6 +150,124 @@ __global__ void __launch_bounds__(256) router_bwd_kernel(
       for (int j = 0; j < 4; ++j) op[j] = __floats2bfloat162_rn(acc[2 * j], acc[2 * j + 1]);
       *reinterpret_cast<uint4*>(dx + (size_t)t * d + c0) = o;
     }
+  }
+}
+
+// n == 8, bf16, d % 8 == 0: one warp per kRbTpw tokens.  The logit gradient of a token is
+// kept as a dense row of 8 (zero outside its kept experts), so a row of W_g (8 bf16, one
+// 16-byte load) serves every token of the warp and every slot without selecting an expert:
+//     dx[t][c] = sum_k dx_pad[q_k][c] + sum_{e < 8} dl[t][e] W_g[c][e]
+// (the second sum in ascending e; the zero terms add exactly nothing).
+constexpr int kRbTpw = 4;
+template <int KMAX>
+__global__ void __launch_bounds__(256) router_bwd_n8_kernel(
+    const int32_t* __restrict__ idx, const float* __restrict__ topk_w,
+    const int32_t* __restrict__ off, const int32_t* __restrict__ poff,
+    const int32_t* __restrict__ inv_perm, const float* __restrict__ dwp, int ntiles,
+    const bf16* __restrict__ dx_pad, const bf16* __restrict__ wg, int T, int d, int k,
+    bf16* __restrict__ dx, float* __restrict__ dl) {
+  // per warp: the dense logit-gradient rows and the padded rows of its tokens
+  __shared__ float s_dl[8][kRbTpw][8];
+  __shared__ int s_q[8][kRbTpw][KMAX];
+  const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  for (int t0 = ((blockIdx.x * blockDim.x + threadIdx.x) >> 5) * kRbTpw; t0 < T;
+       t0 += warps * kRbTpw) {
+    const int nt = min(kRbTpw, T - t0);
+    const int slots = nt * k;   // (token i, slot s) pairs of the warp, p = i * k + s
+    // lane p < slots: the padded row, expert and gate of pair p
+    int my_e = 0, my_q = 0;
+    float my_gate = 0.f;
+    if (lane < slots) {
+      const int i = lane / k, sl = lane - (lane / k) * k;
+      const int a = (t0 + i) * k + sl;
+      my_e = __ldg(idx + a);
+      my_q = __ldg(poff + my_e) + (__ldg(inv_perm + a) - __ldg(off + my_e));
+      my_gate = __ldg(topk_w + a);
+      s_q[wib][i][sl] = my_q;
+    }
+    // dG of every pair: the sum of its column-tile partials of <dw2ᵀ dy, h>, lane-strided,
+    // then a fixed tree; lane p keeps pair p's
+    float my_dG = 0.f;
+#pragma unroll
+    for (int p = 0; p < kRbTpw * KMAX; ++p) {
+      if (p >= slots) break;
+      const int q = __shfl_sync(0xffffffffu, my_q, p);
+      float v = 0.f;
+      for (int j = lane; j < ntiles; j += 32) v += __ldg(dwp + (size_t)q * ntiles + j);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if (lane == p) my_dG = v;
+    }
+    // dl of pair p = G_p (dG_p - sum_s G_s dG_s over its token's slots, ascending s)
+    const int first = (lane / k) * k;
+    float sdot = 0.f;
+    for (int sl = 0; sl < k; ++sl) {
+      const float gv = __shfl_sync(0xffffffffu, my_gate, (first + sl) & 31);
+      const float dv = __shfl_sync(0xffffffffu, my_dG, (first + sl) & 31);
+      sdot = fmaf(gv, dv, sdot);
+    }
+    // the dense rows of 8 (zeros outside the kept experts), then the kept values
+    s_dl[wib][lane >> 3][lane & 7] = 0.f;
+    __syncwarp();
+    if (lane < slots) s_dl[wib][lane / k][my_e] = my_gate * (my_dG - sdot);
+    __syncwarp();
+    if (lane < nt * 8) dl[(size_t)t0 * 8 + lane] = s_dl[wib][lane >> 3][lane & 7];
+    // dx rows, 8 columns per lane and step: the 8 rows of W_g once for the warp's tokens
+#pragma unroll 1
+    for (int c0 = lane * 8; c0 < d; c0 += 256) {
+      uint4 wr[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        wr[j] = __ldg(reinterpret_cast<const uint4*>(wg + (size_t)(c0 + j) * 8));
+      // the dx_pad rows of every token of the warp are loaded before any is summed
+      uint4 u[kRbTpw][KMAX];
+#pragma unroll
+      for (int i = 0; i < kRbTpw; ++i)
+#pragma unroll
+        for (int s = 0; s < KMAX; ++s)
+          if (i < nt && s < k)
+            u[i][s] = __ldg(reinterpret_cast<const uint4*>(dx_pad + (size_t)s_q[wib][i][s] * d + c0));
+#pragma unroll
+      for (int i = 0; i < kRbTpw; ++i) {
+        if (i >= nt) break;
+        const int t = t0 + i;
+        float g[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) g[e] = s_dl[wib][i][e];
+        float acc[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+#pragma unroll
+        for (int s = 0; s < KMAX; ++s) {
+          if (s < k) {
+            const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&u[i][s]);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const float2 f2 = __bfloat1622float2(p[j]);
+              acc[2 * j] += f2.x;
+              acc[2 * j + 1] += f2.y;
+            }
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const __nv_bfloat162* wp = reinterpret_cast<const __nv_bfloat162*>(&wr[j]);
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            const float2 f2 = __bfloat1622float2(wp[h]);
+            acc[j] = fmaf(g[2 * h], f2.x, acc[j]);
+            acc[j] = fmaf(g[2 * h + 1], f2.y, acc[j]);
+          }
+        }
+        uint4 o;
+        __nv_bfloat162* op = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) op[j] = __floats2bfloat162_rn(acc[2 * j], acc[2 * j + 1]);
+        *reinterpret_cast<uint4*>(dx + (size_t)t * d + c0) = o;
+      }
+    }
+    __syncwarp();
   }
 }
 
@@ -272,8 +375,8 @@ __global__ void __launch_bounds__(128) dwg_partial_n8_kernel(const bf16* __restr
   for (int j = 0; j < 8; ++j)
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[j][e] = 0.f;
-  for (int tt = 0; tt < tn; ++tt) {
-    const uint4 u = __ldg(reinterpret_cast<const uint4*>(x + (size_t)(t0 + tt) * d + col0));
+  // tokens in ascending order; the rows of kDwgBatch tokens are loaded together
+  auto step = [&](const uint4& u, int tt) {
     const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&u);
     float g[8];
 #pragma unroll
@@ -287,7 +390,20 @@ __global__ void __launch_bounds__(128) dwg_partial_n8_kernel(const bf16* __restr
         acc[2 * j + 1][e] = fmaf(xf.y, g[e], acc[2 * j + 1][e]);
       }
     }
+  };
+  int tt = 0;
+#pragma unroll 1
+  for (; tt + kDwgBatch <= tn; tt += kDwgBatch) {
+    uint4 u[kDwgBatch];
+#pragma unroll
+    for (int b = 0; b < kDwgBatch; ++b)
+      u[b] = __ldg(reinterpret_cast<const uint4*>(x + (size_t)(t0 + tt + b) * d + col0));
+#pragma unroll
+    for (int b = 0; b < kDwgBatch; ++b) step(u[b], tt + b);
   }
+#pragma unroll 1
+  for (; tt < tn; ++tt)
+    step(__ldg(reinterpret_cast<const uint4*>(x + (size_t)(t0 + tt) * d + col0)), tt);
   float4* out = reinterpret_cast<float4*>(pc + (size_t)col0 * 8);
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
@@ -398,6 +514,18 @@ cudaError_t launch_router_bwd(const int32_t* idx, const float* topk_w, const int
   const bf16* dx_pad = (const bf16*)dx_pad_v;
   const bf16* wg = (const bf16*)wg_v;
   bf16* dx = (bf16*)dx_v;
+  if (n == 8) {
+    // four warps per block, so that small batches still spread over the SMs
+    const long long nb = ((long long)T + 4 * kRbTpw - 1) / (4 * kRbTpw);
+    const int g8 = (int)(nb < cap ? nb : cap);
+    if (k <= 2)
+      router_bwd_n8_kernel<2><<<g8, 128, 0, s>>>(idx, topk_w, off, poff, inv_perm, dwp, ntiles,
+                                                dx_pad, wg, T, d, k, dx, dl);
+    else
+      router_bwd_n8_kernel<8><<<g8, 128, 0, s>>>(idx, topk_w, off, poff, inv_perm, dwp, ntiles,
+                                                dx_pad, wg, T, d, k, dx, dl);
+    return cudaGetLastError();
+  }
   if (k <= 2)
     router_bwd_kernel<2><<<grid, 256, 0, s>>>(idx, topk_w, off, poff, inv_perm, dwp, ntiles,
                                               dx_pad, wg, T, d, n, k, dx, dl);

@@ -219,12 +219,11 @@ def peaks():
 def kernel_traffic(kernel: str, workload: str):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on the current
     source of the kernel (profiles/<kernel>__<workload>.md holds 'traffic_bytes_per_launch:'
-    and 'source_sha256:' lines); None otherwise."""
+    and 'source_sha256:' lines, and optionally 'source_file:', the kernel's file under csrc/,
+    grouped_tc.cu if absent); None otherwise."""
     path = os.path.join(ROOT, "profiles", f"{kernel}__{workload}.md")
-    src = os.path.join(ROOT, "sparse_mixture_experts_56_b300", "csrc", "grouped_tc.cu")
     try:
         text = open(path).read()
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
     except OSError:
         return None
     fields = {}
@@ -232,6 +231,12 @@ def kernel_traffic(kernel: str, workload: str):
         if ":" in line:
             k, v = line.split(":", 1)
             fields[k.strip().lstrip("-* ").strip("`")] = v.strip().strip("`")
+    name = os.path.basename(fields.get("source_file", "grouped_tc.cu"))
+    src = os.path.join(ROOT, "sparse_mixture_experts_56_b300", "csrc", name)
+    try:
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    except OSError:
+        return None
     if fields.get("source_sha256") != sha:
         return None
     try:
@@ -472,7 +477,11 @@ def forward_line(args, w, dist, dev, with_cpu):
         roof = {"bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s", "frac": ach / peak,
                 "peak_kind": kind, "frac_of_sustained": ach / sus,
                 "step_frac": flops_step / (ms_total / args.steps / 1e3) / 1e12 / peak}
-    roof.update({"traffic": kernel_traffic("expert_up", w.name), "kernel": "moe_expert_up (gather + w1|w3 tcgen05 GEMM + SwiGLU)",
+    # batches of at most 64 tokens take the swapped-operand form (weights as the MMA's 128-row
+    # side), larger ones the token-rows-as-M form
+    form = "swapped-operand " if T <= 64 else ""
+    roof.update({"traffic": kernel_traffic("expert_up", w.name),
+                 "kernel": f"moe_expert_up (gather + {form}w1|w3 tcgen05 GEMM + SwiGLU)",
                  "algorithmic": up_bytes if roof["bound"] == "hbm" else up_flops,
                  "ms_per_launch": up_ms, "peak_source": f"{pk_kind} (MEASURED_PEAKS.json)" if pk_kind == "measured" else "fallback",
                  "down_ms_per_launch": down_ms})

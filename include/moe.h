@@ -377,21 +377,30 @@ void moe_set_wait_limit_ns(unsigned long long ns);
 /*
  * Which form of the tensor-core expert GEMMs the bf16 calls use (process-wide; takes effect
  * at the next launch):
- *   MOE_TC_FORM_AUTO    (default) the CTA-pair form (tcgen05 cta_group::2, 256-row tiles
- *                       over two SMs) for the down-projection (w2) when the experts average
- *                       at least 256 rows (T*k >= 256*n) and for the up-projection (w1|w3
- *                       with SwiGLU) when they average at least 512 (T*k >= 512*n); the
- *                       single-CTA form (128-row tiles) otherwise.  In the backward the
- *                       weight-gradient GEMMs (dW1, dW3, dW2: 256-row tiles of dW) always
- *                       take the pair form and the other backward GEMMs the single form.
+ *   MOE_TC_FORM_AUTO    (default) for batches of at most 64 tokens (decode), the swapped
+ *                       form of both forward GEMMs: the weights are the 128-row side of
+ *                       every MMA and the expert's token rows, in blocks of 16-64 rows, the
+ *                       other side, so that each SM keeps more weight bytes in flight.  Else
+ *                       the CTA-pair form (tcgen05 cta_group::2, 256-row tiles over two SMs)
+ *                       for the down-projection (w2) when the experts average at least 256
+ *                       rows (T*k >= 256*n) and for the up-projection (w1|w3 with SwiGLU) when
+ *                       they average at least 512 (T*k >= 512*n); the single-CTA form (128-row
+ *                       tiles) otherwise.  The forward that keeps a|b for the backward
+ *                       (moe_layer_forward_train) never takes the swapped form for its
+ *                       up-projection.  In the backward the weight-gradient GEMMs (dW1, dW3,
+ *                       dW2: 256-row tiles of dW) always take the pair form and the other
+ *                       backward GEMMs the single form.
  *   MOE_TC_FORM_SINGLE  always the single-CTA form
  *   MOE_TC_FORM_PAIR    always the CTA-pair form for the forward GEMMs and the weight
  *                       gradients (where the device can co-schedule pairs)
- * Both forms compute the same results up to the fp32 accumulation order inside a tile
- * (which is the same: both accumulate K in ascending order), so outputs are identical.
+ *   MOE_TC_FORM_SWAP    the swapped form for the forward GEMMs at any batch size (token
+ *                       blocks of 64 rows above 64 tokens; an expert's weights are read once
+ *                       per block); the AUTO rules elsewhere
+ * The single-CTA and pair forms accumulate K in the same ascending order, so their outputs
+ * are identical; the swapped form agrees with them within the rounding of the fp32 sums.
  * Returns MOE_ERR_INVALID_ARG for any other value.
  */
-enum { MOE_TC_FORM_AUTO = 0, MOE_TC_FORM_SINGLE = 1, MOE_TC_FORM_PAIR = 2 };
+enum { MOE_TC_FORM_AUTO = 0, MOE_TC_FORM_SINGLE = 1, MOE_TC_FORM_PAIR = 2, MOE_TC_FORM_SWAP = 3 };
 moe_status moe_set_tc_form(int form);
 
 #ifdef __cplusplus

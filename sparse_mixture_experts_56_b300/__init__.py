@@ -15,7 +15,7 @@ import torch
 
 from . import _native
 from ._native import (MOE_BF16, MOE_F32, MOE_TC_FORM_AUTO, MOE_TC_FORM_PAIR, MOE_TC_FORM_SINGLE,
-                      MoEError, check)
+                      MOE_TC_FORM_SWAP, MoEError, check)
 
 __all__ = [
     "MOE_F32", "MOE_BF16", "MoEError", "dtype_code", "moe_workspace_size", "workspace",
@@ -24,7 +24,7 @@ __all__ = [
     "backward_workspace", "moe_layer_backward", "moe_train_saved_size", "train_saved",
     "moe_layer_forward_train", "moe_layer_backward_saved", "moe_attention_gqa",
     "moe_layer_forward", "moe_check_device_error", "moe_set_wait_limit_ns", "moe_set_tc_form",
-    "MOE_TC_FORM_AUTO", "MOE_TC_FORM_SINGLE", "MOE_TC_FORM_PAIR", "moe_version",
+    "MOE_TC_FORM_AUTO", "MOE_TC_FORM_SINGLE", "MOE_TC_FORM_PAIR", "MOE_TC_FORM_SWAP", "moe_version",
     "library_path", "moe_ep_regroup", "moe_gather_rows", "moe_decoder_workspace_size",
     "decoder_workspace", "moe_decoder_layer_forward",
 ]
@@ -82,7 +82,7 @@ def moe_set_wait_limit_ns(ns: int) -> None:
 
 
 def moe_set_tc_form(form: int) -> None:
-    """Selects the tensor-core GEMM form: MOE_TC_FORM_AUTO, _SINGLE or _PAIR."""
+    """Selects the tensor-core GEMM form: MOE_TC_FORM_AUTO, _SINGLE, _PAIR or _SWAP."""
     check("moe_set_tc_form", _native.lib().moe_set_tc_form(int(form)))
 
 

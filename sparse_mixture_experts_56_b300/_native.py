@@ -17,6 +17,7 @@ MOE_BF16 = 1
 MOE_TC_FORM_AUTO = 0
 MOE_TC_FORM_SINGLE = 1
 MOE_TC_FORM_PAIR = 2
+MOE_TC_FORM_SWAP = 3
 
 STATUS_NAMES = {
     0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",

@@ -146,7 +146,11 @@ moe_status up_impl(const void* x, const int32_t* perm, const int32_t* offsets, c
   const size_t esz = dtype == MOE_BF16 ? 2 : 4;
   cudaError_t e = launch_gather_rows(x, perm, A, k, (size_t)d * esz, x_perm, s);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
-  if (use_tc(dtype, d, f))
+  const int nb = use_tc(dtype, d, f) ? swap_rows(T) : 0;
+  if (nb > 0)
+    e = launch_up_swap((const bf16*)x_perm, offsets, (const bf16*)w1, (const bf16*)w3, A, d, f, n,
+                       nb, (bf16*)h, status_word(ws), g_wait_ns.load(), s);
+  else if (use_tc(dtype, d, f))
     e = launch_up_tc((const bf16*)x_perm, offsets, (const bf16*)w1, (const bf16*)w3, A, d, f, n,
                      (bf16*)h, status_word(ws), g_wait_ns.load(), s);
   else
@@ -159,7 +163,11 @@ moe_status down_impl(const void* h, const int32_t* offsets, const void* w2, int 
   const int A = T * k;
   if (A == 0) return MOE_OK;
   cudaError_t e;
-  if (use_tc(dtype, d, f))
+  const int nb = use_tc(dtype, d, f) ? swap_rows(T) : 0;
+  if (nb > 0)
+    e = launch_down_swap((const bf16*)h, offsets, (const bf16*)w2, A, d, f, n, nb, (bf16*)y_perm,
+                         status_word(ws), g_wait_ns.load(), s);
+  else if (use_tc(dtype, d, f))
     e = launch_down_tc((const bf16*)h, offsets, (const bf16*)w2, A, d, f, n, (bf16*)y_perm,
                        status_word(ws), g_wait_ns.load(), s);
   else
@@ -675,9 +683,11 @@ moe_status moe_check_device_error(void* ws, size_t ws_bytes, void* stream) {
 void moe_set_wait_limit_ns(unsigned long long ns) { g_wait_ns.store(ns ? ns : kDefaultWaitNs); }
 
 moe_status moe_set_tc_form(int form) {
-  if (form != MOE_TC_FORM_AUTO && form != MOE_TC_FORM_SINGLE && form != MOE_TC_FORM_PAIR)
+  if (form != MOE_TC_FORM_AUTO && form != MOE_TC_FORM_SINGLE && form != MOE_TC_FORM_PAIR &&
+      form != MOE_TC_FORM_SWAP)
     return MOE_ERR_INVALID_ARG;
   set_tc_form(form);
+  set_swap_form(form);
   return MOE_OK;
 }
 

@@ -79,6 +79,19 @@ cudaError_t launch_down_tc(const bf16* h, const int32_t* offsets, const bf16* w2
                            int f, int n, bf16* y_perm, uint32_t* status, unsigned long long wait_ns,
                            cudaStream_t s);
 
+// The same two GEMMs for small token batches, operands swapped (weights as the 128-row MMA
+// operand, the expert's token rows, in blocks of nb = 16..64, as the N operand); inference
+// only (no a|b saved).  swap_rows(T): the block size the launchers use for a batch of T
+// tokens, or 0 for the forms above.
+int swap_rows(int T);
+void set_swap_form(int form);
+cudaError_t launch_up_swap(const bf16* x_perm, const int32_t* offsets, const bf16* w1,
+                           const bf16* w3, int A, int d, int f, int n, int nb, bf16* h,
+                           uint32_t* status, unsigned long long wait_ns, cudaStream_t s);
+cudaError_t launch_down_swap(const bf16* h, const int32_t* offsets, const bf16* w2, int A, int d,
+                             int f, int n, int nb, bf16* y_perm, uint32_t* status,
+                             unsigned long long wait_ns, cudaStream_t s);
+
 // Backward on the tensor cores, rows in the expert-padded layout (segments of `poff` are
 // multiples of 128 rows; rows_max bounds the padded row count):
 //   store_ab: ab[q] = [x_pad[q] w1_eᵀ | x_pad[q] w3_eᵀ]                         [rows, 2f]

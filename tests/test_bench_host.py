@@ -63,9 +63,13 @@ def test_committed_decode_summary_is_consistent():
     (each weight byte read once).  After a source change the figure is withheld (and this
     check skipped) until the counters are taken again."""
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-    src = os.path.join(root, "sparse_mixture_experts_56_b300", "csrc", "grouped_tc.cu")
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
     text = open(os.path.join(root, "profiles", "expert_up__mixtral-decode-t32.md")).read()
+    name = "grouped_tc.cu"
+    for line in text.splitlines():
+        if line.lstrip("-* ").startswith("source_file:"):
+            name = line.split(":", 1)[1].strip().strip("`")
+    src = os.path.join(root, "sparse_mixture_experts_56_b300", "csrc", name)
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
     traffic = bench.kernel_traffic("expert_up", "mixtral-decode-t32")
     if f"source_sha256: {sha}" not in text:
         assert traffic is None

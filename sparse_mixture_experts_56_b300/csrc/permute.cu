@@ -41,34 +41,54 @@ __device__ __forceinline__ ChunkBounds warp_range(int chunk_begin, int chunk_end
   return {b, e};
 }
 
-// Bucket of assignment i: its expert, n (the trailing bucket) for an index outside [0, n),
-// which is reported when `status` is not null, or -1 past the end of the range.  Buckets
-// run from 0 to n <= kMaxExperts, so every per-bucket row below has kMaxExperts + 1 entries.
-__device__ __forceinline__ int load_expert(const int32_t* __restrict__ idx, int i, int end, int n,
-                                           uint32_t* status) {
-  if (i >= end) return -1;
-  const int e = __ldg(idx + i);
-  if (e < 0 || e >= n) {
-    if (status) atomicOr(status, kDevErrIndex);
-    return n;
-  }
-  return e;
-}
-
 // Zeroes the kMaxExperts + 1 counters of one warp's row.
 __device__ __forceinline__ void clear_row(int* row, int lane) {
   row[lane] = 0;
   if (lane == 0) row[kMaxExperts] = 0;
 }
 
+// A warp's range holds at most kPermuteChunk / kWarps = 1024 assignments: 32 rounds of 32.
+// Each lane loads the raw indices of a batch of 16 rounds first, with nothing between the
+// loads so that they are all in flight together; the rounds then classify them (reporting
+// bad ones) and run from registers.
+constexpr int kBatch = 16;
+static_assert(kPermuteChunk / kWarps % (32 * kBatch) == 0, "a warp's range is whole batches");
+
+__device__ __forceinline__ void load_batch(const int32_t* __restrict__ idx, int base, int end,
+                                           int lane, int (&v)[kBatch]) {
+#pragma unroll
+  for (int j = 0; j < kBatch; ++j) {
+    const int i = base + 32 * j + lane;
+    v[j] = i < end ? __ldg(idx + i) : 0;
+  }
+}
+
+// Bucket of assignment i with raw expert index v: the expert, n (the trailing bucket) for an
+// index outside [0, n), which is reported when `status` is not null, or -1 past the range.
+__device__ __forceinline__ int bucket_of(int v, int i, int end, int n, uint32_t* status) {
+  if (i >= end) return -1;
+  if (v < 0 || v >= n) {
+    if (status) atomicOr(status, kDevErrIndex);
+    return n;
+  }
+  return v;
+}
+
 // cnt[w][e] <- number of assignments of warp w's range that go to bucket e.
 __device__ void count_warp(const int32_t* __restrict__ idx, ChunkBounds r, int n, int lane,
                            int* cnt_row, uint32_t* status) {
-  for (int base = r.begin; base < r.end; base += 32) {
-    const int e = load_expert(idx, base + lane, r.end, n, status);
-    const unsigned m = __match_any_sync(0xffffffffu, e);
-    if (e >= 0 && lane == __ffs(m) - 1) cnt_row[e] += __popc(m);
-    __syncwarp();
+  for (int b0 = r.begin; b0 < r.end; b0 += 32 * kBatch) {
+    int ev[kBatch];
+    load_batch(idx, b0, r.end, lane, ev);
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int base = b0 + 32 * j;
+      if (base >= r.end) break;
+      const int e = bucket_of(ev[j], base + lane, r.end, n, status);
+      const unsigned m = __match_any_sync(0xffffffffu, e);
+      if (e >= 0 && lane == __ffs(m) - 1) cnt_row[e] += __popc(m);
+      __syncwarp();
+    }
   }
 }
 
@@ -78,19 +98,26 @@ __device__ void scatter_warp(const int32_t* __restrict__ idx, ChunkBounds r, int
                              int* run_row, int32_t* __restrict__ perm,
                              int32_t* __restrict__ inv_perm, uint32_t* status) {
   const unsigned lt = (1u << lane) - 1u;
-  for (int base = r.begin; base < r.end; base += 32) {
-    const int i = base + lane;
-    const int e = load_expert(idx, i, r.end, n, status);
-    const unsigned m = __match_any_sync(0xffffffffu, e);
-    int pos = 0;
-    if (e >= 0) {
-      pos = run_row[e] + __popc(m & lt);
-      perm[pos] = i;
-      inv_perm[i] = pos;
+  for (int b0 = r.begin; b0 < r.end; b0 += 32 * kBatch) {
+    int ev[kBatch];
+    load_batch(idx, b0, r.end, lane, ev);
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int base = b0 + 32 * j;
+      if (base >= r.end) break;
+      const int i = base + lane;
+      const int e = bucket_of(ev[j], i, r.end, n, status);
+      const unsigned m = __match_any_sync(0xffffffffu, e);
+      int pos = 0;
+      if (e >= 0) {
+        pos = run_row[e] + __popc(m & lt);
+        perm[pos] = i;
+        inv_perm[i] = pos;
+      }
+      __syncwarp();
+      if (e >= 0 && lane == __ffs(m) - 1) run_row[e] += __popc(m);
+      __syncwarp();
     }
-    __syncwarp();
-    if (e >= 0 && lane == __ffs(m) - 1) run_row[e] += __popc(m);
-    __syncwarp();
   }
 }
 

@@ -174,12 +174,23 @@ __global__ void __launch_bounds__(256) router_bf16_n8_kernel(const bf16* __restr
 }
 
 // Large batches: W_g (d x 8 bf16, 64 KB at d = 4096) is staged in shared memory once per
-// block, so the only global loads in the loop are the rows of x (unrolled so that 16 loads
-// of 16 bytes per lane are in flight).  Two tokens per warp share each read of W_g from
-// shared memory.  Each lane accumulates its elements in the same order as the kernel above,
-// so the logits are identical.
-constexpr int kRouterSmemTPW = 2;
-__global__ void __launch_bounds__(256) router_bf16_n8_smem_kernel(const bf16* __restrict__ x,
+// block, so the only global loads in the loop are the rows of x.  Four tokens per warp share
+// each read of W_g from shared memory and its conversion to fp32, and the eight products of
+// an element go through four packed two-wide fp32 FMAs (each half rounded as fmaf).  Each
+// lane accumulates its elements in the same order as the kernel above, so the logits are
+// identical.
+constexpr int kRouterSmemTPW = 4;
+
+// acc = (xs, xs) * (w_lo, w_hi) + acc, one packed fp32 FMA; w2 holds two bf16 (lo, hi)
+__device__ __forceinline__ void fma2_bf16(uint64_t& acc, float xs, uint32_t w2) {
+  const float wlo = __uint_as_float(w2 << 16), whi = __uint_as_float(w2 & 0xffff0000u);
+  asm("{\n .reg .b64 a, b;\n mov.b64 a, {%1, %1};\n mov.b64 b, {%2, %3};\n"
+      " fma.rn.f32x2 %0, a, b, %0;\n}\n"
+      : "+l"(acc)
+      : "f"(xs), "f"(wlo), "f"(whi));
+}
+
+__global__ void __launch_bounds__(256, 2) router_bf16_n8_smem_kernel(const bf16* __restrict__ x,
                                                                   const bf16* __restrict__ wg,
                                                                   const float* __restrict__ bias,
                                                                   int Tn, int d, int k,
@@ -198,38 +209,29 @@ __global__ void __launch_bounds__(256) router_bf16_n8_smem_kernel(const bf16* __
   constexpr int TPW = kRouterSmemTPW;
   for (int t0 = ((blockIdx.x * blockDim.x + threadIdx.x) >> 5) * TPW; t0 < Tn;
        t0 += warps * TPW) {
-    float acc[TPW][8];
+    uint64_t acc2[TPW][4];   // experts (2e, 2e + 1) of token t0 + j in acc2[j][e]
 #pragma unroll
     for (int j = 0; j < TPW; ++j)
 #pragma unroll
-      for (int e = 0; e < 8; ++e) acc[j][e] = 0.f;
+      for (int e = 0; e < 4; ++e) acc2[j][e] = 0ull;
     const int nt = Tn - t0 < TPW ? Tn - t0 : TPW;
-#pragma unroll 4
+#pragma unroll 2
     for (int i0 = lane * 8; i0 < d; i0 += 256) {
       uint4 xv[TPW];
 #pragma unroll
       for (int j = 0; j < TPW; ++j)
         xv[j] = j < nt ? __ldg(reinterpret_cast<const uint4*>(x + (size_t)(t0 + j) * d + i0))
                        : make_uint4(0u, 0u, 0u, 0u);
-      uint4 wr[8];
 #pragma unroll
-      for (int r = 0; r < 8; ++r) wr[r] = s_wg[i0 | ((r ^ (i0 >> 3)) & 7)];
+      for (int r = 0; r < 8; ++r) {
+        const uint4 wr = s_wg[i0 | ((r ^ (i0 >> 3)) & 7)];
+        const uint32_t wq[4] = {wr.x, wr.y, wr.z, wr.w};
 #pragma unroll
-      for (int j = 0; j < TPW; ++j) {
-        {
-          const __nv_bfloat162* xp = reinterpret_cast<const __nv_bfloat162*>(&xv[j]);
+        for (int j = 0; j < TPW; ++j) {
+          const uint32_t xw = (&xv[j].x)[r >> 1];
+          const float xs = __uint_as_float((r & 1) ? (xw & 0xffff0000u) : (xw << 16));
 #pragma unroll
-          for (int r = 0; r < 8; ++r) {
-            const float2 xf = __bfloat1622float2(xp[r >> 1]);
-            const float xs = (r & 1) ? xf.y : xf.x;
-            const __nv_bfloat162* wp = reinterpret_cast<const __nv_bfloat162*>(&wr[r]);
-#pragma unroll
-            for (int e2 = 0; e2 < 4; ++e2) {
-              const float2 wf = __bfloat1622float2(wp[e2]);
-              acc[j][2 * e2] = fmaf(xs, wf.x, acc[j][2 * e2]);
-              acc[j][2 * e2 + 1] = fmaf(xs, wf.y, acc[j][2 * e2 + 1]);
-            }
-          }
+          for (int e2 = 0; e2 < 4; ++e2) fma2_bf16(acc2[j][e2], xs, wq[e2]);
         }
       }
     }
@@ -237,19 +239,25 @@ __global__ void __launch_bounds__(256) router_bf16_n8_smem_kernel(const bf16* __
     for (int j = 0; j < TPW; ++j) {
       const int t = t0 + j;
       if (t >= Tn) break;
-      warp_allreduce<8>(acc[j]);
+      float acc[8];
+#pragma unroll
+      for (int e2 = 0; e2 < 4; ++e2) {
+        acc[2 * e2] = __uint_as_float((uint32_t)acc2[j][e2]);
+        acc[2 * e2 + 1] = __uint_as_float((uint32_t)(acc2[j][e2] >> 32));
+      }
+      warp_allreduce<8>(acc);
       if (bias) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc[j][e] += bias[e];
+        for (int e = 0; e < 8; ++e) acc[e] += bias[e];
       }
       if (logits && lane < 8) {
         float v = 0.f;
 #pragma unroll
         for (int e = 0; e < 8; ++e)
-          if (e == lane) v = acc[j][e];
+          if (e == lane) v = acc[e];
         logits[(size_t)t * 8 + lane] = v;
       }
-      if (lane == 0) select_and_write<8>(acc[j], 8, k, idx + (size_t)t * k, w + (size_t)t * k);
+      if (lane == 0) select_and_write<8>(acc, 8, k, idx + (size_t)t * k, w + (size_t)t * k);
     }
   }
 }
@@ -412,7 +420,7 @@ cudaError_t launch_router_topk(const void* x, const void* wg, const float* bias,
              router_smem_ready() == cudaSuccess) {
     const long long warps_needed = (T + kRouterSmemTPW - 1) / kRouterSmemTPW;
     long long blocks = (warps_needed + 7) / 8;
-    const long long cap = (long long)device_sm_count() * 3;
+    const long long cap = (long long)device_sm_count() * 2;   // two blocks fit per SM
     if (blocks > cap) blocks = cap;
     router_bf16_n8_smem_kernel<<<(int)blocks, 256, (size_t)d * 16, s>>>(
         (const bf16*)x, (const bf16*)wg, bias, T, d, k, idx, w, logits);

@@ -612,7 +612,14 @@ __global__ void __launch_bounds__(256, 1)
           decode_tile<MODE, C::kTileM>(sh.tile_base, sh.mtiles, sh.off, n, args.ntiles, tile);
       int ok = 1;
       if (lane == 0) {
-        ok = wait_fast(smem_u32(&sh.tfull[acc]), acc_phase, abort, limit) ? 1 : 0;
+        // The accumulator is ready once per tile.  A tile reducing over d or f runs for tens
+        // of microseconds, so the epilogue sleeps between tests; a weight-gradient tile
+        // reduces over an expert's rows only (a microsecond at small batches) and polls.
+        const uint32_t tf = smem_u32(&sh.tfull[acc]);
+        ok = (MODE == kWgrad ? wait_fast(tf, acc_phase, abort, limit)
+                             : wait_phase_sleepy(tf, acc_phase, abort, limit))
+                 ? 1
+                 : 0;
         if (!ok) raise_abort(abort, args.status);
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);

@@ -171,6 +171,25 @@ __device__ __forceinline__ bool wait_fast(uint32_t bar, uint32_t parity, volatil
   return mbar_test(bar, parity) || wait_phase(bar, parity, abort, limit_ns);
 }
 
+// wait_phase for a role that waits long and whose wake-up can be a little late (an epilogue
+// waiting for the next accumulator while the MMAs of a whole tile run): between tests the
+// thread sleeps, 64 ns at first and doubling up to 2 us, instead of polling.  In a GEMM held
+// back by the power limit the polling threads' power is taken from the tensor cores (1 % of
+// the layer step at 16384 tokens in interleaved runs).
+static __device__ __noinline__ bool wait_phase_sleepy(uint32_t bar, uint32_t parity,
+                                                      volatile int* abort, uint64_t limit_ns) {
+  if (mbar_test(bar, parity)) return true;
+  const uint64_t t0 = gtimer();
+  uint32_t ns = 64;
+  for (;;) {
+    __nanosleep(ns);
+    if (mbar_test(bar, parity)) return true;
+    if (*abort) return false;
+    if (gtimer() - t0 > limit_ns) return false;
+    if (ns < 2048) ns <<= 1;
+  }
+}
+
 // Same, ignoring the abort flag (used to drain work already in flight).
 static __device__ __noinline__ bool drain_phase(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
   const uint64_t t0 = gtimer();

@@ -346,21 +346,6 @@ __device__ __forceinline__ void store_row32(bf16* dst, const float (&v)[32]) {
   }
 }
 
-__device__ __forceinline__ void load_row32(const bf16* src, float (&v)[32]) {
-  const uint4* q = reinterpret_cast<const uint4*>(src);
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const uint4 u = __ldg(q + j);
-    const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&u);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float2 f = __bfloat1622float2(p[i]);
-      v[8 * j + 2 * i] = f.x;
-      v[8 * j + 2 * i + 1] = f.y;
-    }
-  }
-}
-
 __device__ __forceinline__ float sigmoidf_(float z) { return __fdividef(1.0f, 1.0f + __expf(-z)); }
 
 // ------------------------------------------------------------------------------------------
@@ -751,9 +736,17 @@ __global__ void __launch_bounds__(256, 1)
         // dh' = g w2 for 256 columns of f; with the recomputed a, b of the same columns:
         //   h = SiLU(a) b,  partial <dh', h>,  da = G dh' b SiLU'(a),  db = G dh' SiLU(a),
         //   hw = G h  (G = this row's gate weight, 0 on padding rows)
+        // A thread holds one row of the tile, so a, b and the three outputs pass through this
+        // warp's 8 KB of the staging buffer: each 32-column block of 32 rows (64 bytes a row)
+        // is read and written by the warp with 16-byte accesses covering 8 whole rows per
+        // instruction, and each thread reads or writes its own row in shared memory (16-byte
+        // chunk c of row i at chunk c ^ ((i / 2) % 4): no bank conflicts either way).
         const int col0 = t.nt * BN;
         const size_t grow = (size_t)(t.row0 + row);
-        const float gate = args.wq[grow];
+        const float gate = row_ok ? args.wq[grow] : 0.f;
+        uint8_t* wsm = smem + STAGES * C::kStageBytes + q * (kStageOutBytes / 4);
+        const int rows_here = t.rows - q * 32;   // rows of this warp's 32 that exist
+        auto slot = [](int i, int ch) { return i * 64 + 16 * (ch ^ ((i >> 1) & 3)); };
         float dot = 0.f;
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
@@ -762,26 +755,81 @@ __global__ void __launch_bounds__(256, 1)
           tmem_wait(dr);
           if (c == BN / 32 - 1) release_acc();
           const int col = col0 + c * 32;
-          if (row_ok && col < args.ndim) {
-            float av[32], bv[32], o1[32], o2[32];
-            load_row32(args.ab + grow * 2 * args.ndim + col, av);
-            load_row32(args.ab + grow * 2 * args.ndim + args.ndim + col, bv);
+          if (col >= args.ndim) continue;   // the same for the whole warp
+          // a | b of the warp's 32 rows into shared memory (a at 0, b at 2 KB)
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const float dh = __uint_as_float(dr[j]);
-              const float sg = sigmoidf_(av[j]);
-              const float si = av[j] * sg;
-              const float h = si * bv[j];
-              dot = fmaf(dh, h, dot);
-              o1[j] = gate * dh * bv[j] * sg * (1.0f + av[j] * (1.0f - sg));
-              o2[j] = gate * dh * si;
-              bv[j] = gate * h;
+          for (int s8 = 0; s8 < 4; ++s8) {
+            const int i = s8 * 8 + (lane >> 2), ch = lane & 3;
+            if (i < rows_here) {
+              const bf16* src = args.ab + (size_t)(t.row0 + q * 32 + i) * 2 * args.ndim + col + ch * 8;
+              *reinterpret_cast<uint4*>(wsm + slot(i, ch)) = __ldg(reinterpret_cast<const uint4*>(src));
+              *reinterpret_cast<uint4*>(wsm + 2048 + slot(i, ch)) =
+                  __ldg(reinterpret_cast<const uint4*>(src + args.ndim));
             }
-            const size_t oo = grow * args.ndim + col;
-            store_row32(args.da + oo, o1);
-            store_row32(args.db + oo, o2);
-            store_row32(args.hw + oo, bv);
           }
+          __syncwarp();
+          float av[32], bv[32], o1[32], o2[32];
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch) {
+            const uint4 ua = *reinterpret_cast<const uint4*>(wsm + slot(lane, ch));
+            const uint4 ub = *reinterpret_cast<const uint4*>(wsm + 2048 + slot(lane, ch));
+            const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&ua);
+            const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&ub);
+#pragma unroll
+            for (int i2 = 0; i2 < 4; ++i2) {
+              const float2 fa = __bfloat1622float2(pa[i2]), fb = __bfloat1622float2(pb[i2]);
+              av[8 * ch + 2 * i2] = fa.x;
+              av[8 * ch + 2 * i2 + 1] = fa.y;
+              bv[8 * ch + 2 * i2] = fb.x;
+              bv[8 * ch + 2 * i2 + 1] = fb.y;
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float dh = __uint_as_float(dr[j]);
+            const float sg = sigmoidf_(av[j]);
+            const float si = av[j] * sg;
+            const float h = si * bv[j];
+            dot = fmaf(dh, h, dot);
+            o1[j] = gate * dh * bv[j] * sg * (1.0f + av[j] * (1.0f - sg));
+            o2[j] = gate * dh * si;
+            bv[j] = gate * h;
+          }
+          __syncwarp();   // every row of a | b has been read before the outputs overwrite it
+          // da at 0, db at 2 KB, hw at 4 KB; then out to global memory by whole rows
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch) {
+            uint4 u1, u2, u3;
+            u1.x = pack_bf16x2(o1[8 * ch + 0], o1[8 * ch + 1]);
+            u1.y = pack_bf16x2(o1[8 * ch + 2], o1[8 * ch + 3]);
+            u1.z = pack_bf16x2(o1[8 * ch + 4], o1[8 * ch + 5]);
+            u1.w = pack_bf16x2(o1[8 * ch + 6], o1[8 * ch + 7]);
+            u2.x = pack_bf16x2(o2[8 * ch + 0], o2[8 * ch + 1]);
+            u2.y = pack_bf16x2(o2[8 * ch + 2], o2[8 * ch + 3]);
+            u2.z = pack_bf16x2(o2[8 * ch + 4], o2[8 * ch + 5]);
+            u2.w = pack_bf16x2(o2[8 * ch + 6], o2[8 * ch + 7]);
+            u3.x = pack_bf16x2(bv[8 * ch + 0], bv[8 * ch + 1]);
+            u3.y = pack_bf16x2(bv[8 * ch + 2], bv[8 * ch + 3]);
+            u3.z = pack_bf16x2(bv[8 * ch + 4], bv[8 * ch + 5]);
+            u3.w = pack_bf16x2(bv[8 * ch + 6], bv[8 * ch + 7]);
+            *reinterpret_cast<uint4*>(wsm + slot(lane, ch)) = u1;
+            *reinterpret_cast<uint4*>(wsm + 2048 + slot(lane, ch)) = u2;
+            *reinterpret_cast<uint4*>(wsm + 4096 + slot(lane, ch)) = u3;
+          }
+          __syncwarp();
+#pragma unroll
+          for (int s8 = 0; s8 < 4; ++s8) {
+            const int i = s8 * 8 + (lane >> 2), ch = lane & 3;
+            if (i < rows_here) {
+              const size_t oo = (size_t)(t.row0 + q * 32 + i) * args.ndim + col + ch * 8;
+              *reinterpret_cast<uint4*>(args.da + oo) = *reinterpret_cast<const uint4*>(wsm + slot(i, ch));
+              *reinterpret_cast<uint4*>(args.db + oo) =
+                  *reinterpret_cast<const uint4*>(wsm + 2048 + slot(i, ch));
+              *reinterpret_cast<uint4*>(args.hw + oo) =
+                  *reinterpret_cast<const uint4*>(wsm + 4096 + slot(i, ch));
+            }
+          }
+          __syncwarp();   // the next block's a | b may overwrite the outputs only after this
         }
         if (row_ok) args.dwp[grow * args.ntiles + t.nt] = dot;
       } else {

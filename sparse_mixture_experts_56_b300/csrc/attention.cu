@@ -527,13 +527,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 cudaError_t attn_smem_attr() {
-  static cudaError_t err = cudaErrorNotReady;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    err = cudaFuncSetAttribute(attention_gqa_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)kAttnSmem);
+  static PerDeviceSetting setting;
+  return setting.get([] {
+    return cudaFuncSetAttribute(attention_gqa_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)kAttnSmem);
   });
-  return err;
 }
 
 }  // namespace

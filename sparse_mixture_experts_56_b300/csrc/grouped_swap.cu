@@ -411,18 +411,16 @@ int swap_stages(int nb) {
 
 template <int MODE>
 cudaError_t set_swap_smem_attr() {
-  static cudaError_t err = cudaErrorNotReady;
-  static std::once_flag once;
-  std::call_once(once, [] {
+  static PerDeviceSetting setting;
+  return setting.get([] {
     size_t most = 0;   // the largest layout any block size uses
     for (int nb = 16; nb <= kMaxNB; nb += 16) {
       const size_t b = swap_smem_bytes(swap_stages(nb), nb);
       most = b > most ? b : most;
     }
-    err = cudaFuncSetAttribute(grouped_gemm_swap_kernel<MODE>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)most);
+    return cudaFuncSetAttribute(grouped_gemm_swap_kernel<MODE>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)most);
   });
-  return err;
 }
 
 template <int MODE>

@@ -882,14 +882,12 @@ __global__ void __launch_bounds__(256, 1)
 
 template <int MODE, bool PAIR>
 cudaError_t set_smem_attr() {
-  static cudaError_t err = cudaErrorNotReady;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    err = cudaFuncSetAttribute(grouped_gemm_tc_kernel<MODE, PAIR>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)smem_bytes<PAIR>());
+  static PerDeviceSetting setting;
+  return setting.get([] {
+    return cudaFuncSetAttribute(grouped_gemm_tc_kernel<MODE, PAIR>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)smem_bytes<PAIR>());
   });
-  return err;
 }
 
 // Clusters of two that can be resident at once (0 if the pair form cannot run here).

@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "moe.h"
 
 namespace moe {
@@ -33,6 +35,28 @@ template <>
 __device__ __forceinline__ float from_f32<float>(float v) { return v; }
 template <>
 __device__ __forceinline__ bf16 from_f32<bf16>(float v) { return __float2bfloat16_rn(v); }
+
+// A setting that belongs to each device's context (a kernel's dynamic shared-memory limit):
+// applied once per device, the first time a launch on that device needs it, and its result
+// kept.  A process that drives several GPUs applies it on each.
+constexpr int kMaxDevices = 64;
+struct PerDeviceSetting {
+  std::mutex mu;
+  bool done[kMaxDevices] = {};
+  cudaError_t err[kMaxDevices] = {};
+  template <typename Apply>
+  cudaError_t get(Apply apply) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+      return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!done[dev]) {
+      err[dev] = apply();
+      done[dev] = true;
+    }
+    return err[dev];
+  }
+};
 
 // ---------------------------------------------------------------------------------------
 // Launchers (host functions; every one returns the launch error of its kernels)

@@ -391,13 +391,11 @@ constexpr int kRouterBlockPerTokenMax = 1024;
 constexpr int kRouterSmemMaxD = 12288;
 
 cudaError_t router_smem_ready() {
-  static cudaError_t err = cudaErrorNotReady;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    err = cudaFuncSetAttribute(router_bf16_n8_smem_kernel,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, kRouterSmemMaxD * 16);
+  static PerDeviceSetting setting;
+  return setting.get([] {
+    return cudaFuncSetAttribute(router_bf16_n8_smem_kernel,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, kRouterSmemMaxD * 16);
   });
-  return err;
 }
 
 int grid_for_warps(long long warps_needed) {

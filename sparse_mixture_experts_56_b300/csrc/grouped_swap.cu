@@ -37,7 +37,6 @@
 #include <cuda.h>
 
 #include <atomic>
-#include <mutex>
 
 #include "moe_internal.cuh"
 #include "tc_ptx.cuh"
@@ -444,8 +443,10 @@ void set_swap_form(int form) { g_swap_form.store(form, std::memory_order_relaxed
 
 // Token rows per block of the swapped form for a batch of T tokens (no expert of a routed
 // batch holds more than T rows: the K experts of a token are distinct), or 0 for the
-// token-rows-as-M form.  Measured on B300 at the decode size (T = 32, d = 4096, f = 14336):
-// see the design notes; above 64 tokens per expert the token-rows-as-M form is used.
+// token-rows-as-M form.  On B300 at T = 32, d = 4096, f = 14336 the swapped up-projection
+// streams its weights at 6.4 TB/s against 6.1 TB/s for the token-rows-as-M form (layer step
+// 0.461 against 0.479 ms); above 64 tokens the token-rows-as-M form is used, whose larger
+// token tiles suit the tensor-bound sizes.
 int swap_rows(int T) {
   const int form = g_swap_form.load(std::memory_order_relaxed);
   if (form == MOE_TC_FORM_SINGLE || form == MOE_TC_FORM_PAIR) return 0;

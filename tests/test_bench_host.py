@@ -57,6 +57,28 @@ def test_kernel_traffic_only_for_the_source_it_was_taken_on(tmp_path, monkeypatc
     assert bench.kernel_traffic("expert_up", "other") is None
 
 
+def test_kernel_traffic_follows_the_named_source_file(tmp_path, monkeypatch):
+    """A summary that names its kernel's file (source_file:) is checked against that file's
+    hash, not against the default grouped_tc.cu."""
+    csrc = tmp_path / "sparse_mixture_experts_56_b300" / "csrc"
+    csrc.mkdir(parents=True)
+    (csrc / "grouped_tc.cu").write_bytes(b"// the other GEMM\n")
+    swap = b"// swapped form\n"
+    (csrc / "grouped_swap.cu").write_bytes(swap)
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    (prof / "expert_up__dec.md").write_text(
+        "- source_file: grouped_swap.cu\n- traffic_bytes_per_launch: 777\n"
+        f"- source_sha256: {hashlib.sha256(swap).hexdigest()}\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.kernel_traffic("expert_up", "dec") == 777.0
+    # a change to the default file does not matter; one to the named file withholds the figure
+    (csrc / "grouped_tc.cu").write_bytes(b"// changed\n")
+    assert bench.kernel_traffic("expert_up", "dec") == 777.0
+    (csrc / "grouped_swap.cu").write_bytes(swap + b" ")
+    assert bench.kernel_traffic("expert_up", "dec") is None
+
+
 def test_committed_decode_summary_is_consistent():
     """While the GEMM source is the one the committed decode summary was taken on, bench.py
     reports that summary's traffic for the default line, and it is the algorithmic bytes

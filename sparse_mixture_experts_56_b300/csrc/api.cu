@@ -340,6 +340,7 @@ size_t moe_workspace_size(int T, int d, int f, int n, int k, int dtype) {
 moe_status moe_router_topk(const void* x, const void* w_gate, const float* logit_bias, int T, int d,
                            int n, int k, int dtype, int32_t* topk_idx, float* topk_w, float* logits,
                            void* stream) {
+  MOE_CALL_RANGE();
   if (!dtype_ok(dtype) || !sizes_ok(T, d, 1, n, k)) return MOE_ERR_INVALID_ARG;
   if (T == 0) return MOE_OK;
   if (!x || !w_gate || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
@@ -350,6 +351,7 @@ moe_status moe_router_topk(const void* x, const void* w_gate, const float* logit
 
 moe_status moe_permute(const int32_t* topk_idx, int T, int k, int n, int32_t* expert_offsets,
                        int32_t* perm, int32_t* inv_perm, void* ws, size_t ws_bytes, void* stream) {
+  MOE_CALL_RANGE();
   if (!sizes_ok(T, 64, 64, n, k)) return MOE_ERR_INVALID_ARG;
   if (!expert_offsets || (T > 0 && (!topk_idx || !perm || !inv_perm))) return MOE_ERR_INVALID_ARG;
   const Layout L = layout(T, 64, 64, n, k, MOE_BF16);
@@ -364,6 +366,7 @@ moe_status moe_grouped_swiglu(const void* x, const int32_t* perm, const int32_t*
                               const void* w1, const void* w3, const void* w2, int T, int d, int f,
                               int n, int k, int dtype, void* y_perm, void* ws, size_t ws_bytes,
                               void* stream) {
+  MOE_CALL_RANGE();
   if (!dtype_ok(dtype) || !sizes_ok(T, d, f, n, k)) return MOE_ERR_INVALID_ARG;
   if (T == 0) return MOE_OK;
   if (!x || !perm || !expert_offsets || !w1 || !w3 || !w2 || !y_perm) return MOE_ERR_INVALID_ARG;
@@ -378,6 +381,7 @@ moe_status moe_grouped_swiglu(const void* x, const int32_t* perm, const int32_t*
 moe_status moe_expert_up(const void* x, const int32_t* perm, const int32_t* expert_offsets,
                          const void* w1, const void* w3, int T, int d, int f, int n, int k,
                          int dtype, void* h, void* ws, size_t ws_bytes, void* stream) {
+  MOE_CALL_RANGE();
   if (!dtype_ok(dtype) || !sizes_ok(T, d, f, n, k)) return MOE_ERR_INVALID_ARG;
   if (T == 0) return MOE_OK;
   if (!x || !perm || !expert_offsets || !w1 || !w3 || !h) return MOE_ERR_INVALID_ARG;
@@ -391,6 +395,7 @@ moe_status moe_expert_up(const void* x, const int32_t* perm, const int32_t* expe
 moe_status moe_expert_down(const void* h, const int32_t* expert_offsets, const void* w2, int T,
                            int d, int f, int n, int k, int dtype, void* y_perm, void* ws,
                            size_t ws_bytes, void* stream) {
+  MOE_CALL_RANGE();
   if (!dtype_ok(dtype) || !sizes_ok(T, d, f, n, k)) return MOE_ERR_INVALID_ARG;
   if (T == 0) return MOE_OK;
   if (!h || !expert_offsets || !w2 || !y_perm) return MOE_ERR_INVALID_ARG;
@@ -401,6 +406,7 @@ moe_status moe_expert_down(const void* h, const int32_t* expert_offsets, const v
 
 moe_status moe_combine(const void* y_perm, const int32_t* inv_perm, const float* topk_w,
                        const void* residual, int T, int d, int k, int dtype, void* y, void* stream) {
+  MOE_CALL_RANGE();
   if (!dtype_ok(dtype) || !sizes_ok(T, d, 1, k, k)) return MOE_ERR_INVALID_ARG;
   if (T == 0) return MOE_OK;
   if (!y_perm || !inv_perm || !topk_w || !y) return MOE_ERR_INVALID_ARG;
@@ -411,6 +417,7 @@ moe_status moe_combine(const void* y_perm, const int32_t* inv_perm, const float*
 }
 
 moe_status moe_rmsnorm(const void* h, int T, int d, float eps, int dtype, void* x, void* stream) {
+  MOE_CALL_RANGE();
   if (!dtype_ok(dtype) || !sizes_ok(T, d, 1, 1, 1) || !(eps >= 0.f)) return MOE_ERR_INVALID_ARG;
   if (T == 0) return MOE_OK;
   if (!h || !x || h == x || !aligned16(h) || !aligned16(x)) return MOE_ERR_INVALID_ARG;
@@ -422,6 +429,7 @@ moe_status moe_layer_forward(const void* x, const void* w_gate, const float* log
                              int T, int d, int f, int n, int k, int dtype, void* y,
                              int32_t* topk_idx_out, int32_t* expert_offsets_out, void* ws,
                              size_t ws_bytes, void* stream) {
+  MOE_CALL_RANGE();
   if (!dtype_ok(dtype) || !sizes_ok(T, d, f, n, k)) return MOE_ERR_INVALID_ARG;
   cudaStream_t s = (cudaStream_t)stream;
   if (T == 0) {
@@ -472,6 +480,7 @@ moe_status moe_layer_backward(const void* x, const void* w_gate, const float* lo
                               int T, int d, int f, int n, int k, int dtype, void* dx,
                               float* dw_gate, float* dlogit_bias, void* dw1, void* dw3, void* dw2,
                               void* ws, size_t ws_bytes, void* stream) {
+  MOE_CALL_RANGE();
   moe_status st = check_backward_args(x, w_gate, w1, w3, w2, dy, T, d, f, n, k, dtype, dx,
                                       dw_gate, dw1, dw3, dw2);
   if (st != MOE_OK) return st;
@@ -510,6 +519,7 @@ moe_status moe_layer_forward_train(const void* x, const void* w_gate, const floa
                                    const void* residual, int T, int d, int f, int n, int k,
                                    int dtype, void* y, void* saved, size_t saved_bytes, void* ws,
                                    size_t ws_bytes, void* stream) {
+  MOE_CALL_RANGE();
   if (!dtype_ok(dtype) || !sizes_ok(T, d, f, n, k)) return MOE_ERR_INVALID_ARG;
   if (!use_tc(dtype, d, f)) return MOE_ERR_UNSUPPORTED;
   if (T == 0) return MOE_OK;
@@ -558,6 +568,7 @@ moe_status moe_layer_backward_saved(const void* x, const void* w_gate, const voi
                                     size_t saved_bytes, void* dx, float* dw_gate,
                                     float* dlogit_bias, void* dw1, void* dw3, void* dw2, void* ws,
                                     size_t ws_bytes, void* stream) {
+  MOE_CALL_RANGE();
   moe_status st = check_backward_args(x, w_gate, w1, w3, w2, dy, T, d, f, n, k, dtype, dx,
                                       dw_gate, dw1, dw3, dw2);
   if (st != MOE_OK) return st;
@@ -583,6 +594,7 @@ moe_status moe_layer_backward_saved(const void* x, const void* w_gate, const voi
 moe_status moe_attention_gqa(const void* q, const void* k, const void* v, int T, int seq_len,
                              int hq, int hkv, int dh, int dtype, void* out, void* ws,
                              size_t ws_bytes, void* stream) {
+  MOE_CALL_RANGE();
   if (!dtype_ok(dtype) || T < 0 || seq_len < 0 || hq < 1 || hkv < 1 || dh < 1 || hq % hkv)
     return MOE_ERR_INVALID_ARG;
   if ((long long)T * hq * dh >= (1ll << 40)) return MOE_ERR_INVALID_ARG;
@@ -607,6 +619,7 @@ moe_status moe_decoder_layer_forward(const void* h, const void* wq, const void* 
                                      int f, int n, int k, int hq, int hkv, int seq_len, float eps,
                                      int dtype, void* y, int32_t* topk_idx_out, void* ws,
                                      size_t ws_bytes, void* stream) {
+  MOE_CALL_RANGE();
   if (!dtype_ok(dtype) || !sizes_ok(T, d, f, n, k) || hq < 1 || hkv < 1 || hq % hkv ||
       seq_len < 0 || !(eps >= 0.f))
     return MOE_ERR_INVALID_ARG;
@@ -655,6 +668,7 @@ moe_status moe_decoder_layer_forward(const void* h, const void* wq, const void* 
 
 moe_status moe_routing_stats(const int32_t* topk_idx, int T, int k, int n, int seq_len,
                              int64_t* expert_counts, int64_t* pair_counts, void* stream) {
+  MOE_CALL_RANGE();
   if (!sizes_ok(T, 1, 1, n, k) || seq_len < 0) return MOE_ERR_INVALID_ARG;
   if (!expert_counts || !pair_counts || (T > 0 && !topk_idx)) return MOE_ERR_INVALID_ARG;
   if (((uintptr_t)expert_counts & 7u) || ((uintptr_t)pair_counts & 7u) ||

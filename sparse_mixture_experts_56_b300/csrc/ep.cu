@@ -99,6 +99,7 @@ __global__ void __launch_bounds__(256) gather_index_byte_kernel(const uint8_t* _
 extern "C" moe_status moe_ep_regroup(const int32_t* recv_counts, int G, int E, int R,
                                      int32_t* local_offsets, int32_t* row_map,
                                      int32_t* inv_row_map, void* stream) {
+  MOE_CALL_RANGE();
   using namespace moe;
   if (G < 1 || G > kMaxSources || E < 1 || E > kMaxExperts || R < 0) return MOE_ERR_INVALID_ARG;
   if (!recv_counts || !local_offsets || (R > 0 && (!row_map || !inv_row_map)))
@@ -112,6 +113,7 @@ extern "C" moe_status moe_ep_regroup(const int32_t* recv_counts, int G, int E, i
 extern "C" moe_status moe_gather_rows(const void* src, int rows_src, const int32_t* index,
                                       int rows, int k, size_t row_bytes, void* dst,
                                       void* stream) {
+  MOE_CALL_RANGE();
   using namespace moe;
   if (rows < 0 || rows_src < 0 || k < 1 || row_bytes == 0) return MOE_ERR_INVALID_ARG;
   if (rows == 0) return MOE_OK;

@@ -8,6 +8,8 @@
 
 #include <mutex>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "moe.h"
 
 namespace moe {
@@ -35,6 +37,17 @@ template <>
 __device__ __forceinline__ float from_f32<float>(float v) { return v; }
 template <>
 __device__ __forceinline__ bf16 from_f32<bf16>(float v) { return __float2bfloat16_rn(v); }
+
+// A named NVTX range around one call of the C ABI, so that a timeline tool (Nsight Systems,
+// ncu's range filters) shows each call by name; without a tool attached the push and pop
+// cost a few nanoseconds and do nothing.
+struct CallRange {
+  explicit CallRange(const char* name) { nvtxRangePushA(name); }
+  ~CallRange() { nvtxRangePop(); }
+  CallRange(const CallRange&) = delete;
+  CallRange& operator=(const CallRange&) = delete;
+};
+#define MOE_CALL_RANGE() ::moe::CallRange moe_call_range_(__func__)
 
 // A setting that belongs to each device's context (a kernel's dynamic shared-memory limit):
 // applied once per device, the first time a launch on that device needs it, and its result

@@ -38,6 +38,12 @@ class Guarded:
         self.raw = torch.full((2 * PAD + self.n,), FILL, dtype=torch.uint8, device=DEV)
         self.t = self.raw[PAD:PAD + self.n].view(dtype).view(shape)
 
+    def workspace(self):
+        """As a workspace: its 256-byte status header starts at zero, as every workspace's
+        must; the rest keeps the fill."""
+        self.t[:256].zero_()
+        return self
+
     def check(self, what):
         torch.cuda.synchronize()
         lo = self.raw[:PAD].cpu().numpy()
@@ -63,7 +69,7 @@ def test_layer_calls_write_inside_their_buffers(moe, T, d, f, n, k, skew):
     w, g, bias = _inputs(T, d, f, n, k, 1300 + T, skew)
     A = T * k
     bf = torch.bfloat16
-    ws = Guarded((moe.moe_workspace_size(T, d, f, n, k, bf),), torch.uint8)
+    ws = Guarded((moe.moe_workspace_size(T, d, f, n, k, bf),), torch.uint8).workspace()
     idx, wts = Guarded((T, k), torch.int32), Guarded((T, k), torch.float32)
     logits = Guarded((T, n), torch.float32)
     off, perm, inv = Guarded((n + 1,), torch.int32), Guarded((A,), torch.int32), Guarded((A,), torch.int32)
@@ -93,7 +99,7 @@ def test_backward_and_attention_write_inside_their_buffers(moe):
     w, g, bias = _inputs(T, d, f, n, k, 1350, True)
     bf = torch.bfloat16
     dy = to_device(workloads.make_inputs(w, tensors=("dy",))["dy"], w, DEV)
-    bws = Guarded((moe.moe_backward_workspace_size(T, d, f, n, k, bf),), torch.uint8)
+    bws = Guarded((moe.moe_backward_workspace_size(T, d, f, n, k, bf),), torch.uint8).workspace()
     dx, dwg = Guarded((T, d), bf), Guarded((d, n), torch.float32)
     dw1, dw3, dw2 = Guarded((n, f, d), bf), Guarded((n, f, d), bf), Guarded((n, d, f), bf)
     db = Guarded((n,), torch.float32)
@@ -111,7 +117,7 @@ def test_backward_and_attention_write_inside_their_buffers(moe):
     q = torch.from_numpy(rng.standard_normal((Ta, hq, 128), dtype=np.float32)).to(DEV).to(bf)
     kk = torch.from_numpy(rng.standard_normal((Ta, hkv, 128), dtype=np.float32)).to(DEV).to(bf)
     v = torch.from_numpy(rng.standard_normal((Ta, hkv, 128), dtype=np.float32)).to(DEV).to(bf)
-    aws = Guarded((256,), torch.uint8)   # the attention only needs the status header
+    aws = Guarded((256,), torch.uint8).workspace()   # the attention needs only the header
     out = Guarded((Ta, hq, 128), bf)
     moe.moe_attention_gqa(q, kk, v, aws.t, seq_len=200, out=out.t)
     assert moe.moe_check_device_error(aws.t) == 0

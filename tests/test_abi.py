@@ -41,6 +41,25 @@ def test_every_declared_symbol_is_exported(lib):
         assert name in _native.SIGNATURES, f"{name} has no ctypes signature"
 
 
+def header_constants():
+    """NAME = value pairs of the enums in include/moe.h."""
+    src = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    return {m.group(1): int(m.group(2)) for m in re.finditer(r"\b(MOE_[A-Z0-9_]+)\s*=\s*(\d+)", src)}
+
+
+def test_binding_constants_match_the_header():
+    """The Python binding's copies of the header's enum values (dtypes, GEMM forms, status
+    codes) are the header's."""
+    consts = header_constants()
+    for name in ("MOE_F32", "MOE_BF16", "MOE_TC_FORM_AUTO", "MOE_TC_FORM_SINGLE",
+                 "MOE_TC_FORM_PAIR", "MOE_TC_FORM_SWAP"):
+        assert getattr(_native, name) == consts[name], name
+    for code, name in _native.STATUS_NAMES.items():
+        assert consts[name] == code, name
+    assert sorted(v for k, v in consts.items() if k.startswith("MOE_ERR") or k == "MOE_OK") == \
+        sorted(_native.STATUS_NAMES)
+
+
 def test_status_strings(lib):
     for code, name in _native.STATUS_NAMES.items():
         assert lib.moe_status_string(code).decode() == name

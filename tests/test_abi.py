@@ -60,6 +60,19 @@ def test_binding_constants_match_the_header():
         sorted(_native.STATUS_NAMES)
 
 
+def test_tc_form_selection_is_validated(lib):
+    """Every declared GEMM form is accepted and anything else rejected (no launch happens);
+    the default is restored afterwards."""
+    try:
+        for form in (_native.MOE_TC_FORM_SINGLE, _native.MOE_TC_FORM_PAIR, _native.MOE_TC_FORM_SWAP,
+                     _native.MOE_TC_FORM_AUTO):
+            assert lib.moe_set_tc_form(form) == OK
+        for bad in (-1, 4, 99):
+            assert lib.moe_set_tc_form(bad) == INVALID
+    finally:
+        lib.moe_set_tc_form(_native.MOE_TC_FORM_AUTO)
+
+
 def test_status_strings(lib):
     for code, name in _native.STATUS_NAMES.items():
         assert lib.moe_status_string(code).decode() == name
